@@ -1,0 +1,75 @@
+"""Workload registry: the five MoE expert-parallel layer shapes plus small test shapes.
+
+Notation follows the FlashInfer MoE-EP design page ("MoE-EP implementation & usage",
+section 3 "Algorithm / layout contracts") and the Mooncake EP guide (Buffer.dispatch
+parameters): W logical ranks ("world"), Tr tokens per rank
+(num_max_dispatch_tokens_per_rank), E experts, k = top_k, H = hidden, I = FFN
+intermediate size.  Token t belongs to logical rank t // Tr; expert e lives on logical
+rank e // (E // W).
+
+This module holds shapes and seeds only; it contains none of the layer's arithmetic.
+"""
+from dataclasses import dataclass, replace
+
+LAYOUTS = ("EM", "RM", "FLAT")          # EXPERT_MAJOR, RANK_MAJOR, FLAT
+LAYOUT_CODE = {"EM": 0, "RM": 1, "FLAT": 2}
+ALGO_CODE = {"LL": 0, "HT": 1}
+
+
+@dataclass(frozen=True)
+class MoeConfig:
+    name: str
+    W: int            # logical ranks
+    Tr: int           # max tokens per logical rank
+    H: int            # hidden
+    E: int            # experts (global)
+    k: int            # top_k
+    I: int            # FFN intermediate
+    layout: str       # "EM" | "RM" | "FLAT"
+    algo: str         # "LL" | "HT"
+    routing: str      # "uniform" | "zipf" | "dirichlet"
+    T: int = -1       # tokens in the batch; -1 means W*Tr
+    zipf_s: float = 1.1
+    dirichlet_alpha: float = 0.1
+    seed: int = 0
+    ids_dtype: str = "int64"
+    mask_frac: float = 0.0   # fraction of picks replaced by -1 (masked picks)
+
+    @property
+    def tokens(self) -> int:
+        return self.W * self.Tr if self.T < 0 else self.T
+
+    @property
+    def local_experts(self) -> int:
+        return self.E // self.W
+
+    def with_(self, **kw) -> "MoeConfig":
+        return replace(self, **kw)
+
+
+# The five workloads of the layer (shapes of the pages' EP deployments; synthetic data).
+CONFIGS = {
+    "tiny_ll_em": MoeConfig("tiny_ll_em", W=2, Tr=32, H=256, E=8, k=2, I=512,
+                            layout="EM", algo="LL", routing="uniform"),
+    "mixtral_ll_em": MoeConfig("mixtral_ll_em", W=8, Tr=128, H=4096, E=8, k=2, I=14336,
+                               layout="EM", algo="LL", routing="uniform"),
+    "dsv3_ll_rm": MoeConfig("dsv3_ll_rm", W=8, Tr=128, H=7168, E=256, k=8, I=2048,
+                            layout="RM", algo="LL", routing="zipf"),
+    "dsv3_ht_flat": MoeConfig("dsv3_ht_flat", W=8, Tr=4096, H=7168, E=256, k=8, I=2048,
+                              layout="FLAT", algo="HT", routing="uniform"),
+    "ragged_em": MoeConfig("ragged_em", W=8, Tr=2048, H=2048, E=128, k=4, I=1024,
+                           layout="EM", algo="LL", routing="dirichlet"),
+}
+
+# Mid-size shapes that the oracle finishes in seconds but that still span several
+# 128-row tiles, several 256-column tiles and a ragged row tail, one per layout.
+SMALL = {
+    "small_em": MoeConfig("small_em", W=4, Tr=96, H=512, E=16, k=4, I=384,
+                          layout="EM", algo="LL", routing="dirichlet", T=350),
+    "small_rm": MoeConfig("small_rm", W=4, Tr=96, H=512, E=16, k=4, I=384,
+                          layout="RM", algo="LL", routing="zipf", T=350),
+    "small_flat": MoeConfig("small_flat", W=4, Tr=96, H=512, E=16, k=4, I=384,
+                            layout="FLAT", algo="HT", routing="uniform", T=350),
+}
+
+ALL = {**CONFIGS, **SMALL}

@@ -1,0 +1,272 @@
+"""CPU oracle of the MoE expert-parallel layer: dispatch -> per-expert SwiGLU FFN -> combine.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the benchmark's
+CPU-baseline leg (bench.py --impl reference / cpu_baseline) may import this package.
+The product library never calls it and shares no code with it.
+
+Plain and slow on purpose: routing is the literal (t, j)-ordered loop in moe_oracle.c;
+the FFN and combine are numpy in float64, one expert at a time; bf16 rounding happens
+exactly where the layer stores bf16 values.
+
+Sources (page title, section):
+  * FlashInfer "MoE-EP implementation & usage", section 2 "Call stack": dispatch ->
+    EP->compute bridge -> per-expert grouped GEMM (no routing) -> combine ->
+    [num_tokens, hidden] bf16.
+  * same page, section 3 "Algorithm / layout contracts": EXPERT_MAJOR computes top_k=1
+    per dispatched row and reweights per token on combine; RANK_MAJOR / HT FLAT compute
+    the real top_k over the received routing with non-local picks masked to weight 0,
+    and combine is an unweighted sum across ranks.
+  * same page, section 4 step 1: w1 [E, 2*I, H], w2 [E, H, I].
+  * Mooncake EP guide, "Buffer.combine(...)": expert outputs are returned by routing
+    weight and reduced to the token's owner.
+Readings where the pages are silent (each listed in the design notes):
+  * gate = rows [0, I) of w1[e], up = rows [I, 2I); SwiGLU act = silu(gate) * up with
+    silu(g) = g / (1 + exp(-g))  (parity unpinned by the pages: a fixed convention);
+  * act is rounded to bf16 (it is the bf16 operand of the second grouped GEMM);
+    expert_out stays float (float64 here); the final output is rounded to bf16;
+  * RANK_MAJOR / FLAT apply topk_weights in the FFN stage's reduction over the local
+    picks of a received row (ascending j), and combine sums over destinations without
+    weights (ascending d).
+
+Functions whose values the pages never print ("parity unpinned" by the pages; pinned in
+tests by brute force, closed forms, a library special case and exact invariants):
+route, pick_outputs, ffn_ranks, combine_em, combine_ranks, layer.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from .build import build as _build_c, LIB_PATH
+
+_lib = None
+
+
+def _c():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            _build_c()
+        _lib = ctypes.CDLL(LIB_PATH)
+        i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
+        i64p = np.ctypeslib.ndpointer(np.int64, flags="C_CONTIGUOUS")
+        f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+        ci = ctypes.c_int
+        _lib.oracle_route_experts.argtypes = [ci, ci, ci, ci, ci, ctypes.c_int64, i64p, i32p, i32p,
+                                              i32p, i32p, i32p, i32p]
+        _lib.oracle_route_experts.restype = ci
+        _lib.oracle_route_ranks.argtypes = [ci, ci, ci, ci, ci, ci, i64p, f32p,
+                                            i32p, i32p, i32p, i32p, i32p, f32p]
+        _lib.oracle_route_ranks.restype = None
+    return _lib
+
+
+LAYOUT = {"EM": 0, "RM": 1, "FLAT": 2}
+
+
+def round_bf16(a):
+    """Nearest bf16 value (8 significant bits, ties to even) of float64 values, as float64.
+
+    Single rounding from float64.  Values below 2**-126 keep 8 significant bits (bf16
+    subnormals are not modelled; no tested quantity lands there).
+    """
+    a = np.asarray(a, dtype=np.float64)
+    m, ex = np.frexp(a)
+    return np.ldexp(np.rint(m * 256.0), ex - 8)
+
+
+def bf16_bits_to_f64(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def route(geom, ids, topk_w):
+    """All routing metadata of one dispatch (Mooncake EP "Buffer.dispatch" outputs and the
+    FlashInfer layout contracts).  geom: dict with W, Tr, T, E, k, layout ("EM"|"RM"|"FLAT").
+
+    Returns a dict of int32 arrays: counts, offsets, pick_pos, pick_src (first R entries),
+    layout_range [E, W, 2], slot (EM recv row per pick or -1), and for RM/FLAT recv_row
+    [T, W], recv_count [W, W], num_recv [W], recv_src, recv_topk_idx, recv_topk_w
+    (the last three as [W, cap(, k)] with cap = W*Tr; rows >= count are unspecified and
+    left at -1 / 0 here), plus n_bad (ids outside [-1, E)) and n_over (EXPERT_MAJOR picks
+    dropped because their expert's region of W*Tr rows was full, which only a token that
+    names one expert twice can cause).
+    """
+    W, Tr, T, E, k = geom["W"], geom["Tr"], geom["T"], geom["E"], geom["k"]
+    lay = LAYOUT[geom["layout"]]
+    ids64 = np.ascontiguousarray(np.asarray(ids).reshape(T, k), dtype=np.int64)
+    w32 = np.ascontiguousarray(np.asarray(topk_w).reshape(T, k), dtype=np.float32)
+    lib = _c()
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    pick_pos = np.full(T * k, -1, np.int32)
+    pick_src = np.full(max(T * k, 1), -1, np.int32)
+    lrange = np.zeros(E * W * 2, np.int32)
+    n_over = np.zeros(1, np.int32)
+    cap = W * Tr
+    # only the EXPERT_MAJOR region has a per-expert row capacity (W*Tr rows)
+    n_bad = lib.oracle_route_experts(T, k, E, W, Tr, cap if lay == 0 else -1, ids64, counts,
+                                     offsets, pick_pos, pick_src, lrange, n_over)
+    R = int(offsets[E])
+    out = dict(ids=ids64, counts=counts, offsets=offsets, pick_pos=pick_pos.reshape(T, k),
+               pick_src=pick_src[:R], layout_range=lrange.reshape(E, W, 2), n_bad=n_bad,
+               n_over=int(n_over[0]), R=R)
+    # EXPERT_MAJOR receive row: expert e's region starts at e*cap, packed from its row 0.
+    slot = np.full(T * k, -1, np.int64)
+    valid = (pick_pos >= 0) & (lay == 0)
+    e_of = ids64.reshape(-1)
+    slot[valid] = e_of[valid] * cap + (pick_pos[valid] - offsets[e_of[valid]])
+    out["slot"] = slot.reshape(T, k)
+    if lay != 0:
+        recv_row = np.full(T * W, -1, np.int32)
+        recv_count = np.zeros(W * W, np.int32)
+        num_recv = np.zeros(W, np.int32)
+        recv_src = np.full(W * cap, -1, np.int32)
+        rti = np.full(W * cap * k, -1, np.int32)
+        rtw = np.zeros(W * cap * k, np.float32)
+        lib.oracle_route_ranks(T, k, E, W, Tr, lay, ids64, w32, recv_row, recv_count,
+                               num_recv, recv_src, rti, rtw)
+        out.update(recv_row=recv_row.reshape(T, W), recv_count=recv_count.reshape(W, W),
+                   num_recv=num_recv, recv_src=recv_src.reshape(W, cap),
+                   recv_topk_idx=rti.reshape(W, cap, k), recv_topk_w=rtw.reshape(W, cap, k))
+    return out
+
+
+def dispatch_rows(geom, rt):
+    """Where each token row lands: arrays (recv_row_index, token) for every received row.
+
+    EXPERT_MAJOR: one row per valid pick, recv index e*cap + position in e's region.
+    RANK_MAJOR / FLAT: one row per (token, destination) pair, recv index d*cap + row.
+    The expected content of recv row `r` is x[token]: dispatch is a bit copy.
+    """
+    W, Tr = geom["W"], geom["Tr"]
+    cap = W * Tr
+    if geom["layout"] == "EM":
+        T, k = rt["slot"].shape
+        s = rt["slot"].reshape(-1)
+        tok = np.repeat(np.arange(T), k)
+        m = s >= 0
+        return s[m], tok[m]
+    rr = rt["recv_row"]
+    t_idx, d_idx = np.nonzero(rr >= 0)
+    return d_idx.astype(np.int64) * cap + rr[t_idx, d_idx], t_idx
+
+
+def swiglu_expert(xrows, w1e, w2e):
+    """One expert's FFN on the rows xrows [n, H] (float64 values of bf16 inputs):
+    h = x W1e^T, act = bf16(silu(h[:, :I]) * h[:, I:]), y = act W2e^T (float64)."""
+    I = w2e.shape[1]
+    h = xrows @ w1e.T
+    g, u = h[:, :I], h[:, I:]
+    with np.errstate(over="ignore"):
+        act = round_bf16(g / (1.0 + np.exp(-g)) * u)
+    return act @ w2e.T
+
+
+def _expert_weights(w1, w2, e):
+    """float64 values of expert e's weights; w1/w2 are uint16 bf16 bit arrays or callables
+    returning them for one expert (large weight sets are fetched one expert at a time)."""
+    a = w1(e) if callable(w1) else w1[e]
+    b = w2(e) if callable(w2) else w2[e]
+    return bf16_bits_to_f64(a), bf16_bits_to_f64(b)
+
+
+def pick_outputs(geom, rt, x_bits, w1, w2, picks=None, expert_fn=None):
+    """Expert output y(t, j) = FFN_e(x[t]) of each valid pick, e = topk_ids[t, j].
+
+    This is EXPERT_MAJOR's expert stage (top_k = 1 per dispatched row) and the per-pick
+    term of the RANK_MAJOR / FLAT stage.  Returns {pick index t*k+j: float64 [H]} for
+    `picks` (default: all valid picks).  expert_fn(e, xrows) replaces the SwiGLU expert
+    (the identity-expert pin uses it).
+    """
+    k = geom["k"]
+    pp = rt["pick_pos"].reshape(-1)
+    ids = rt["ids"].reshape(-1)
+    want = np.nonzero(pp >= 0)[0] if picks is None else np.asarray(picks)
+    out = {}
+    by_e = {}
+    for i in want:
+        e = int(ids[i])
+        by_e.setdefault(e, []).append(int(i))
+    for e, lst in sorted(by_e.items()):
+        xr = bf16_bits_to_f64(x_bits[np.array(lst) // k])
+        if expert_fn is not None:
+            y = expert_fn(e, xr)
+        else:
+            a, b = _expert_weights(w1, w2, e)
+            y = swiglu_expert(xr, a, b)
+        for n, i in enumerate(lst):
+            out[i] = y[n]
+    return out
+
+
+def combine_em(geom, rt, topk_w, y_of_pick, tokens):
+    """EXPERT_MAJOR combine: out[t] = bf16( sum_j w[t, j] * expert_out[slot[t, j]] ),
+    masked picks contribute nothing; float64 sum in ascending j."""
+    k = geom["k"]
+    pp = rt["pick_pos"]
+    w = np.asarray(topk_w, dtype=np.float64).reshape(-1, k)
+    res = []
+    for t in tokens:
+        acc = None
+        for j in range(k):
+            if pp[t, j] < 0:
+                continue
+            term = w[t, j] * y_of_pick(t * k + j)
+            acc = term if acc is None else acc + term
+        res.append(np.zeros(geom["H"]) if acc is None else acc)
+    return round_bf16(np.array(res))
+
+
+def ffn_ranks(geom, rt, topk_w, y_of_pick, dest_rows):
+    """RANK_MAJOR / FLAT expert stage on received rows: for destination d and row r with
+    token t, expert_out[d, r] = sum over j ascending of recv_topk_w[d, r, j] * y(t, j),
+    non-local picks (recv_topk_idx == -1) masked to weight 0 (skipped).
+    dest_rows: iterable of (d, r).  Returns float64 [len, H]."""
+    k = geom["k"]
+    res = []
+    for d, r in dest_rows:
+        t = int(rt["recv_src"][d, r])
+        acc = np.zeros(geom["H"])
+        for j in range(k):
+            if rt["recv_topk_idx"][d, r, j] < 0:
+                continue
+            acc = acc + float(rt["recv_topk_w"][d, r, j]) * y_of_pick(t * k + j)
+        res.append(acc)
+    return np.array(res)
+
+
+def combine_ranks(geom, rt, expert_out_of, tokens):
+    """RANK_MAJOR / FLAT combine: out[t] = bf16( sum over destinations d ascending that
+    received t of expert_out[d, recv_row[t, d]] ), unweighted."""
+    res = []
+    for t in tokens:
+        acc = np.zeros(geom["H"])
+        for d in range(geom["W"]):
+            r = int(rt["recv_row"][t, d])
+            if r >= 0:
+                acc = acc + expert_out_of(d, r)
+        res.append(acc)
+    return round_bf16(np.array(res))
+
+
+def layer(geom, x_bits, ids, topk_w, w1, w2, tokens=None, expert_fn=None):
+    """The whole layer for `tokens` (default all): route -> dispatch -> expert FFN ->
+    combine, returning (route metadata, out [len(tokens), H] float64 holding bf16 values).
+    Only the picks of the requested tokens are evaluated."""
+    T, k = geom["T"], geom["k"]
+    rt = route(geom, ids, topk_w)
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens)
+    picks = [t * k + j for t in tokens for j in range(k) if rt["pick_pos"][t, j] >= 0]
+    ys = pick_outputs(geom, rt, x_bits, w1, w2, picks=picks, expert_fn=expert_fn)
+    if geom["layout"] == "EM":
+        return rt, combine_em(geom, rt, topk_w, ys.__getitem__, tokens)
+    rows = sorted({(d, int(rt["recv_row"][t, d])) for t in tokens for d in range(geom["W"])
+                   if rt["recv_row"][t, d] >= 0})
+    eo = dict(zip(rows, ffn_ranks(geom, rt, topk_w, ys.__getitem__, rows)))
+    return rt, combine_ranks(geom, rt, lambda d, r: eo[(d, r)], tokens)
+
+
+def geom_of(cfg):
+    """Geometry dict of a gen.configs.MoeConfig."""
+    return dict(W=cfg.W, Tr=cfg.Tr, T=cfg.tokens, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I,
+                layout=cfg.layout)

@@ -1,0 +1,321 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+- routing metadata vs brute-force enumeration on tiny random inputs and vs a hand-worked
+  example of the layout contracts (tests/golden/route_hand_example.json);
+- the expert FFN vs torch's silu/matmul in float64 (dense SwiGLU MLP special case);
+- the whole layer vs the textbook dense MoE (every expert applied to every token, gated
+  by a dense [T, E] routing matrix) computed with torch;
+- closed forms and exact invariants: identity expert, masked picks, power-of-two
+  scaling, zero weights, expert relabelling, layout equivalence;
+- planted mistakes in the oracle are caught by these pins.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------- routing
+def brute_route(W, Tr, T, E, k, ids, w, cap=None):
+    """Enumeration: every quantity counted directly from its definition, O(n^2).
+    cap: EXPERT_MAJOR region rows; a pick with that many earlier picks of its expert is dropped."""
+    ids = np.asarray(ids).reshape(T, k)
+    Le = E // W
+    picks = [(t, j) for t in range(T) for j in range(k)]
+    in_range = lambda t, j: 0 <= ids[t, j] < E  # noqa: E731
+    earlier = lambda t, j: sum(1 for (a, b) in picks  # noqa: E731
+                               if (a, b) < (t, j) and in_range(a, b) and ids[a, b] == ids[t, j])
+    valid = lambda t, j: in_range(t, j) and (cap is None or earlier(t, j) < cap)  # noqa: E731
+    counts = [sum(1 for (t, j) in picks if valid(t, j) and ids[t, j] == e) for e in range(E)]
+    offsets = [sum(counts[:e]) for e in range(E + 1)]
+    pos = np.full((T, k), -1)
+    for (t, j) in picks:
+        if valid(t, j):
+            e = ids[t, j]
+            pos[t, j] = offsets[e] + sum(1 for (a, b) in picks
+                                         if (a, b) < (t, j) and valid(a, b) and ids[a, b] == e)
+    lr = np.zeros((E, W, 2), int)
+    for e in range(E):
+        for r in range(W):
+            lr[e, r, 0] = sum(1 for (t, j) in picks if valid(t, j) and ids[t, j] == e and t // Tr < r)
+            lr[e, r, 1] = sum(1 for (t, j) in picks if valid(t, j) and ids[t, j] == e and t // Tr == r)
+    on = lambda t, d: any(valid(t, j) and ids[t, j] // Le == d for j in range(k))  # noqa: E731
+    rm = np.full((T, W), -1)
+    fl = np.full((T, W), -1)
+    for t in range(T):
+        for d in range(W):
+            if on(t, d):
+                s = t // Tr
+                rm[t, d] = s * Tr + sum(1 for u in range(s * Tr, t) if on(u, d))
+                fl[t, d] = sum(1 for u in range(t) if on(u, d))
+    return dict(counts=counts, offsets=offsets, pos=pos, lr=lr, rm=rm, fl=fl)
+
+
+def _rand_case(seed):
+    rng = np.random.default_rng(seed)
+    W = int(rng.choice([1, 2, 4]))
+    E = W * int(rng.integers(1, 4))
+    Tr = int(rng.integers(1, 9))
+    T = int(rng.integers(0, W * Tr + 1))
+    k = int(rng.integers(1, 5))
+    ids = rng.integers(-1, E, size=(T, k))        # duplicates and -1 included
+    w = rng.random((T, k)).astype(np.float32)
+    return W, Tr, T, E, k, ids, w
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_route_matches_brute_force(seed):
+    W, Tr, T, E, k, ids, w = _rand_case(seed)
+    for layout in ("EM", "RM", "FLAT"):
+        b = brute_route(W, Tr, T, E, k, ids, w, cap=W * Tr if layout == "EM" else None)
+        g = dict(W=W, Tr=Tr, T=T, E=E, k=k, layout=layout)
+        rt = oracle.route(g, ids, w)
+        assert list(rt["counts"]) == b["counts"]
+        assert list(rt["offsets"]) == b["offsets"]
+        np.testing.assert_array_equal(rt["pick_pos"], b["pos"])
+        np.testing.assert_array_equal(rt["layout_range"], b["lr"])
+        if layout != "EM":
+            np.testing.assert_array_equal(rt["recv_row"], b["rm"] if layout == "RM" else b["fl"])
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_route_invariants(seed):
+    W, Tr, T, E, k, ids, w = _rand_case(100 + seed)
+    for layout in ("EM", "RM", "FLAT"):
+        g = dict(W=W, Tr=Tr, T=T, E=E, k=k, layout=layout)
+        rt = oracle.route(g, ids, w)
+        n_masked = int((ids == -1).sum())
+        # every valid pick counted once (EM may drop picks beyond its region's W*Tr rows)
+        assert int(rt["counts"].sum()) == T * k - n_masked - rt["n_over"]
+        assert layout == "EM" or rt["n_over"] == 0
+        assert rt["counts"].max(initial=0) <= W * Tr or layout != "EM"
+        pp = rt["pick_pos"].reshape(-1)
+        valid = pp >= 0
+        # bijection between valid picks and pick-list positions
+        assert sorted(pp[valid].tolist()) == list(range(rt["R"]))
+        np.testing.assert_array_equal(rt["pick_src"][pp[valid]], np.nonzero(valid)[0])
+        if layout == "EM":  # EM slots are distinct and inside their expert's region
+            s = rt["slot"].reshape(-1)[valid]
+            assert len(set(s.tolist())) == len(s)
+            assert np.all(s // (W * Tr) == ids.reshape(-1)[valid])
+        else:
+            Le = E // W
+            for t in range(T):
+                for d in range(W):
+                    has = any(0 <= ids[t, j] < E and ids[t, j] // Le == d for j in range(k))
+                    r = rt["recv_row"][t, d]
+                    assert (r >= 0) == has
+                    if has:
+                        assert rt["recv_src"][d, r] == t
+                        for j in range(k):
+                            e = ids[t, j]
+                            loc = rt["recv_topk_idx"][d, r, j]
+                            if 0 <= e < E and e // Le == d:
+                                assert loc == e - d * Le and rt["recv_topk_w"][d, r, j] == w[t, j]
+                            else:
+                                assert loc == -1 and rt["recv_topk_w"][d, r, j] == 0.0
+            assert rt["recv_count"].sum() == rt["num_recv"].sum() == (rt["recv_row"] >= 0).sum()
+
+
+def test_route_hand_example():
+    gd = json.load(open(os.path.join(GOLDEN, "route_hand_example.json")))
+    g = dict(gd["geom"])
+    ids = np.array(gd["topk_ids"])
+    w = np.array(gd["topk_weights"], np.float32)
+    rt = oracle.route(dict(g, layout="EM"), ids, w)
+    assert rt["counts"].tolist() == gd["counts"]
+    assert rt["offsets"].tolist() == gd["offsets"]
+    assert rt["pick_pos"].tolist() == gd["pick_pos"]
+    assert rt["slot"].tolist() == gd["em_slot"]
+    assert rt["layout_range"].tolist() == gd["layout_range"]
+    rm = oracle.route(dict(g, layout="RM"), ids, w)
+    assert rm["recv_row"].tolist() == gd["rm_recv_row"]
+    assert rm["recv_count"].tolist() == gd["rm_recv_count"]
+    assert rm["num_recv"].tolist() == gd["num_recv"]
+    fl = oracle.route(dict(g, layout="FLAT"), ids, w)
+    assert fl["recv_row"].tolist() == gd["flat_recv_row"]
+    for rt_ in (rm, fl):
+        for dn, rows in gd["recv_topk_idx_by_token"].items():
+            d = int(dn[1:])
+            for t, loc in rows.items():
+                r = rt_["recv_row"][int(t), d]
+                assert rt_["recv_topk_idx"][d, r].tolist() == loc
+
+
+def test_route_flags_bad_ids():
+    ids = np.array([[0, 5], [-2, 1]])
+    rt = oracle.route(dict(W=1, Tr=2, T=2, E=4, k=2, layout="EM"), ids, np.ones((2, 2), np.float32))
+    assert rt["n_bad"] == 2 and rt["counts"].tolist() == [1, 1, 0, 0]
+    assert rt["pick_pos"].tolist() == [[0, -1], [-1, 1]]
+
+
+# ------------------------------------------------------------------------ bf16 rounding
+def test_round_bf16_matches_torch_on_float32_values():
+    rng = np.random.default_rng(0)
+    a = np.concatenate([rng.standard_normal(100000).astype(np.float32) * 10.0 ** rng.integers(-30, 30, 100000),
+                        np.array([0.0, -0.0, 1.0, 1.00390625, 1.01171875, 3.0e38])]).astype(np.float32)
+    # 1.00390625 = 1 + 2^-8 is a tie -> even (1.0); 1.01171875 = 1 + 3*2^-8 -> 1 + 2^-6
+    want = torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_bf16(a.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+    assert oracle.round_bf16(1.00390625) == 1.0 and oracle.round_bf16(1.01171875) == 1.015625
+
+
+# --------------------------------------------------------------------------- FFN pins
+def _tiny_cfg(layout="EM", **kw):
+    c = gen.MoeConfig("t", W=2, Tr=8, H=64, E=4, k=2, I=32, layout=layout, algo="LL",
+                      routing="uniform", T=13, **kw)
+    return c
+
+
+def _inputs(c):
+    x = gen.gen_x(c)
+    ids, w = gen.gen_routing(c)
+    w1, w2 = gen.gen_weights_numpy(c)
+    return x, ids, w, w1, w2
+
+
+def _f64(bits):
+    return torch.from_numpy(oracle.bf16_bits_to_f64(bits))
+
+
+def test_swiglu_expert_vs_torch_dense_mlp():
+    """E=1, k=1, w=1: the layer is a dense SwiGLU MLP (library special case)."""
+    c = gen.MoeConfig("d", W=1, Tr=40, H=128, E=1, k=1, I=96, layout="EM", algo="LL", routing="uniform")
+    x, ids, w, w1, w2 = _inputs(c)
+    w = np.ones_like(w)
+    _, out = oracle.layer(oracle.geom_of(c), x, ids, w, w1, w2)
+    X, W1, W2 = _f64(x), _f64(w1[0]), _f64(w2[0])
+    gate, up = X @ W1[:96].T, X @ W1[96:].T
+    act = (torch.nn.functional.silu(gate) * up).to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    ref = (act @ W2.T).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(out, ref)
+
+
+def _dense_moe_torch(c, x, ids, w, w1, w2):
+    """Textbook dense MoE: out = sum_e G[:, e] * FFN_e(X) with G[t, e] = sum_j w[t,j][ids[t,j]==e]."""
+    X = _f64(x)
+    G = torch.zeros(c.tokens, c.E, dtype=torch.float64)
+    for j in range(c.k):
+        m = torch.from_numpy(ids[:, j] >= 0)
+        G[m, torch.from_numpy(ids[:, j])[m]] += torch.from_numpy(w[:, j].astype(np.float64))[m]
+    out = torch.zeros(c.tokens, c.H, dtype=torch.float64)
+    for e in range(c.E):
+        W1, W2 = _f64(w1[e]), _f64(w2[e])
+        act = torch.nn.functional.silu(X @ W1[:c.I].T) * (X @ W1[c.I:].T)
+        act = act.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+        out += G[:, e:e + 1] * (act @ W2.T)
+    return out.numpy()
+
+
+@pytest.mark.parametrize("layout", ["EM", "RM", "FLAT"])
+@pytest.mark.parametrize("mask", [0.0, 0.25])
+def test_layer_vs_dense_moe(layout, mask):
+    c = _tiny_cfg(layout, mask_frac=mask)
+    x, ids, w, w1, w2 = _inputs(c)
+    _, out = oracle.layer(oracle.geom_of(c), x, ids, w, w1, w2)
+    ref = _dense_moe_torch(c, x, ids, w, w1, w2)
+    # out is bf16-rounded; ref is the exact float64 sum: within half a bf16 ulp (+ tiny slack)
+    np.testing.assert_allclose(out, ref, rtol=2 ** -8 + 1e-9, atol=1e-12)
+
+
+@pytest.mark.parametrize("layout", ["EM", "RM", "FLAT"])
+def test_identity_expert_closed_form(layout):
+    """expert_out = recv row: combine(dispatch(x)) = bf16(x * sum of valid weights)."""
+    c = _tiny_cfg(layout, mask_frac=0.2)
+    x, ids, w, w1, w2 = _inputs(c)
+    _, out = oracle.layer(oracle.geom_of(c), x, ids, w, w1, w2, expert_fn=lambda e, xr: xr)
+    ws = np.where(ids >= 0, w.astype(np.float64), 0.0).sum(axis=1)
+    ref = oracle.round_bf16(oracle.bf16_bits_to_f64(x) * ws[:, None])
+    np.testing.assert_array_equal(out, ref)
+
+
+def test_masked_pick_equals_zero_weight():
+    c = _tiny_cfg("EM")
+    x, ids, w, w1, w2 = _inputs(c)
+    g = oracle.geom_of(c)
+    ids_m, w_z = ids.copy(), w.copy()
+    ids_m[::3, 1] = -1
+    w_z[::3, 1] = 0.0
+    _, a = oracle.layer(g, x, ids_m, w, w1, w2)
+    _, b = oracle.layer(g, x, ids, w_z, w1, w2)
+    np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("layout", ["EM", "RM", "FLAT"])
+def test_power_of_two_and_zero_weights(layout):
+    c = _tiny_cfg(layout)
+    x, ids, w, w1, w2 = _inputs(c)
+    g = oracle.geom_of(c)
+    _, base = oracle.layer(g, x, ids, w, w1, w2)
+    w2x2 = (w2.astype(np.uint32) + (1 << 7)).astype(np.uint16)   # exponent + 1 = times 2 (no zeros/infs here)
+    assert np.all(oracle.bf16_bits_to_f64(w2x2) == 2 * oracle.bf16_bits_to_f64(w2))
+    _, dbl = oracle.layer(g, x, ids, w, w1, w2x2)
+    np.testing.assert_array_equal(dbl, 2 * base)
+    _, zero = oracle.layer(g, x, ids, w, w1, np.zeros_like(w2))
+    assert np.all(zero == 0)
+
+
+def test_expert_relabelling_invariance():
+    c = _tiny_cfg("EM")
+    x, ids, w, w1, w2 = _inputs(c)
+    perm = np.array([2, 0, 3, 1])               # new id of old expert e
+    inv = np.argsort(perm)
+    ids_p = np.where(ids >= 0, perm[np.maximum(ids, 0)], -1)
+    g = oracle.geom_of(c)
+    _, a = oracle.layer(g, x, ids, w, w1, w2)
+    _, b = oracle.layer(g, x, ids_p, w, w1[inv], w2[inv])
+    np.testing.assert_array_equal(a, b)
+
+
+def test_layouts_agree():
+    c = _tiny_cfg("EM", mask_frac=0.1)
+    x, ids, w, w1, w2 = _inputs(c)
+    outs = [oracle.layer(oracle.geom_of(c.with_(layout=L)), x, ids, w, w1, w2)[1]
+            for L in ("EM", "RM", "FLAT")]
+    np.testing.assert_allclose(outs[1], outs[0], rtol=2 ** -7, atol=1e-12)
+    np.testing.assert_array_equal(outs[1], outs[2])   # same per-destination grouping
+
+
+# ------------------------------------------------------------- planted mistakes fail
+def test_planted_mistakes_are_caught(monkeypatch):
+    c = _tiny_cfg("RM")
+    x, ids, w, w1, w2 = _inputs(c)
+    ref = _dense_moe_torch(c, x, ids, w, w1, w2)
+    good = oracle.swiglu_expert
+
+    def check():
+        _, out = oracle.layer(oracle.geom_of(c), x, ids, w, w1, w2)
+        return np.allclose(out, ref, rtol=2 ** -8 + 1e-9, atol=1e-12)
+
+    assert check()
+    I = c.I
+    mutants = {
+        "gate/up swapped": lambda xr, a, b: good(xr, np.concatenate([a[I:], a[:I]]), b),
+        "W2 transposed use": lambda xr, a, b: (lambda h: oracle.round_bf16(
+            h[:, :I] / (1 + np.exp(-h[:, :I])) * h[:, I:]) @ b.reshape(b.shape[1], b.shape[0]))(xr @ a.T),
+        "silu sign": lambda xr, a, b: (lambda h: oracle.round_bf16(
+            h[:, :I] / (1 + np.exp(h[:, :I])) * h[:, I:]) @ b.T)(xr @ a.T),
+    }
+    for name, fn in mutants.items():
+        monkeypatch.setattr(oracle, "swiglu_expert", fn)
+        assert not check(), name
+    monkeypatch.setattr(oracle, "swiglu_expert", good)
+    # a dropped term in the per-destination reduction
+    good_fr = oracle.ffn_ranks
+
+    def drop_last(geom, rt, topk_w, y_of_pick, rows):
+        rt2 = dict(rt)
+        rti = rt["recv_topk_idx"].copy()
+        rti[..., -1] = -1
+        rt2["recv_topk_idx"] = rti
+        return good_fr(geom, rt2, topk_w, y_of_pick, rows)
+    monkeypatch.setattr(oracle, "ffn_ranks", drop_last)
+    assert not check()
