@@ -1,0 +1,380 @@
+#!/usr/bin/env python
+"""Benchmark of the one-GPU MoE expert-parallel layer: dispatch -> grouped SwiGLU FFN ->
+combine through the C ABI, on seeded synthetic inputs.
+
+One step = one pass of the whole layer over one batch already resident in HBM.  Each
+timed step is bracketed by CUDA events on the launching stream; the L2 is flushed (a
+512 MiB write) before every step, outside the events.  Per-kernel times come from the
+library's event slots (moe_handle.events).  The JSON line reports tokens/s, per-stage
+microseconds, the roofline of the dominant kernel, the end-to-end number from host
+buffers (moe_forward_host), the CPU oracle timed on a bounded sample, and the SM clocks
+sampled during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer (the path has no
+cross-GPU exchange on one GPU); the timed region is bracketed by a barrier and the max over
+ranks is reported.  --impl reference times the CPU oracle instead (rank 0 only).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s (dispatch+grouped FFN+combine), % of bf16/HBM roofline"
+DEFAULT_CONFIG = "mixtral_ll_em"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# tokens of the workload the CPU oracle evaluates per timed sample (bounded CPU work)
+ORACLE_SAMPLE_TOKENS = {"tiny_ll_em": 64, "mixtral_ll_em": 4, "dsv3_ll_rm": 4, "dsv3_ht_flat": 2,
+                        "ragged_em": 16}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_work(cfg, rt):
+    """Bytes and FLOPs each kernel must move / compute at minimum (padding never counted).
+
+    rt: counts per expert and received-row totals of this batch (from the device)."""
+    T, k, H, I = cfg.tokens, cfg.k, cfg.H, cfg.I
+    R = rt["R"]
+    active = rt["active_experts"]
+    nrecv = rt["n_recv"]
+    em = cfg.layout == "EM"
+    ids_b = 8 if cfg.ids_dtype == "int64" else 4
+    w = {}
+    w["routing"] = dict(bytes=2 * T * k * ids_b + T * k * 4 * (3 if em else 2) +
+                        (0 if em else T * k * 4 + nrecv * (4 + 8 * k) + T * cfg.W * 4), flops=0)
+    w["dispatch_copy"] = dict(bytes=T * H * 2 + (R if em else nrecv) * H * 2, flops=0)
+    if not em:
+        w["gather_picks"] = dict(bytes=2 * R * H * 2, flops=0)
+    w["gemm1_swiglu"] = dict(bytes=active * 2 * I * H * 2 + R * H * 2 + R * I * 2, flops=4 * R * H * I)
+    w["gemm2"] = dict(bytes=active * H * I * 2 + R * I * 2 + R * H * 4, flops=2 * R * H * I)
+    if not em:
+        w["reduce_ranks"] = dict(bytes=R * H * 4 + nrecv * H * 4 + R * 8, flops=0)
+    w["combine"] = dict(bytes=(R * H * 4 + T * k * 8 if em else nrecv * H * 4) + T * H * 2, flops=0)
+    return w
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples (every 200 ms) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.devnull if False else "/tmp/_bench_clocks_%d.csv" % os.getpid(), "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
+
+
+def src_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.join(ROOT, "combine_topk_ids_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "combine_topk_ids_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("src_sha") != src_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------- CPU oracle timing
+def oracle_sample_time(cfg, case, n_tokens):
+    """Seconds the CPU oracle takes for the whole layer on the first n_tokens tokens of
+    the batch (routing of the full batch, FFN and combine of the sample)."""
+    import numpy as np
+    import oracle
+    g = oracle.geom_of(cfg)
+    # host copies of the expert weights the sample touches, fetched before timing
+    ids = case.ids_np[:n_tokens]
+    experts = sorted({int(e) for e in ids.reshape(-1) if e >= 0})
+    if callable(case.w1_host):
+        w1 = {e: case.w1_host(e) for e in experts}
+        w2 = {e: case.w2_host(e) for e in experts}
+        f1, f2 = w1.__getitem__, w2.__getitem__
+    else:
+        f1, f2 = case.w1_host, case.w2_host
+    t0 = time.perf_counter()
+    oracle.layer(g, case.x_bits, case.ids_np, case.w_np, f1, f2, tokens=np.arange(n_tokens))
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------------- main arms
+def run_reference(args, cfg, rank):
+    """The CPU oracle as it stands, timed on the host cores on bounded samples."""
+    if rank != 0:
+        return
+    from gen.device import make_case
+    case = make_case(cfg, "cpu")
+    n = min(ORACLE_SAMPLE_TOKENS.get(cfg.name, 8), cfg.tokens)
+    for _ in range(args.warmup):
+        oracle_sample_time(cfg, case, n)
+    total = sum(oracle_sample_time(cfg, case, n) for _ in range(args.steps))
+    value = n * args.steps / total
+    sample = "first %d of %d tokens per step (full routing, FFN+combine of the sample)" % (n, cfg.tokens)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": workload_config(cfg, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg, n):
+    return {"workload": cfg.name, "layout": {"EM": "EXPERT_MAJOR", "RM": "RANK_MAJOR", "FLAT": "FLAT"}[cfg.layout],
+            "algorithm": {"LL": "LOW_LATENCY", "HT": "HIGH_THROUGHPUT"}[cfg.algo],
+            "tokens": cfg.tokens, "world": cfg.W, "max_tok_per_rank": cfg.Tr, "hidden": cfg.H,
+            "experts": cfg.E, "top_k": cfg.k, "intermediate": cfg.I, "routing": cfg.routing,
+            "ids_dtype": cfg.ids_dtype, "l2": "flushed (512 MiB write) before every timed step",
+            "parallelism": "replicas x%d" % n if n > 1 else "single GPU"}
+
+
+def run_ours(args, cfg, rank, world, dist):
+    import numpy as np
+    import torch
+
+    import combine_topk_ids_gb300 as moe
+    from gen.device import make_case
+
+    if not os.path.exists(moe.LIB_PATH):
+        moe.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    case = make_case(cfg, dev)
+    layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout, cfg.algo)
+    layer.set_weights(case.w1, case.w2)
+    layer.enable_timing(True)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        layer.forward(case.x, case.ids, case.w)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    steps_ms, ktimes = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        ev0.record()
+        layer.forward(case.x, case.ids, case.w)
+        ev1.record()
+        ev1.synchronize()
+        steps_ms.append(ev0.elapsed_time(ev1))
+        ktimes.append(layer.kernel_times_ms())
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    status = layer.status()
+    if status != 0:
+        raise RuntimeError("device status %d after the timed steps" % status)
+
+    total_s = sum(steps_ms) / 1e3
+    if dist is not None:
+        t = torch.tensor([total_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    value = cfg.tokens * args.steps * world / total_s
+    kmean = {k: statistics.mean(d[k] for d in ktimes) for k in ktimes[0]}
+
+    # batch statistics for the algorithmic work (read once, outside the timed region)
+    counts = layer.view("counts", (cfg.E,), torch.int32).cpu().numpy()
+    rt = {"R": int(counts.sum()), "active_experts": int((counts > 0).sum()),
+          "n_recv": 0 if cfg.layout == "EM" else int(layer.view("num_recv", (cfg.W,), torch.int32).sum().item())}
+    work = algorithmic_work(cfg, rt)
+    peaks, peak_src = load_peaks()
+    bw = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    kernels = [k for k in work if k in kmean]
+    dom = max(kernels, key=lambda k: kmean[k])
+    wd = work[dom]
+    t_dom = kmean[dom] / 1e3
+    bound = "tensor" if wd["flops"] / tc > wd["bytes"] / bw else "hbm"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": wd["bytes"] / t_dom / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": wd["flops"] / t_dom / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = ncu_traffic(cfg.name, dom)
+    roof["kernel"] = dom
+    roof["algorithmic_bytes"] = wd["bytes"]
+    roof["algorithmic_flops"] = wd["flops"]
+    roof["peak_source"] = "%s (MEASURED_PEAKS.json)" % peak_src if peak_src == "measured" else "fallback"
+    sum_b = sum(v["bytes"] for v in work.values())
+    sum_f = sum(v["flops"] for v in work.values())
+    t_roof = max(sum_b / bw, sum_f / tc)
+    step_s = total_s / args.steps
+    layer_roof = {"t_roofline_us": t_roof * 1e6, "t_step_us": step_s * 1e6, "frac": t_roof / step_s,
+                  "bytes": sum_b, "flops": sum_f}
+
+    # end to end from host buffers through moe_forward_host (copies inside the events)
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        x_h, ids_h, w_h = pin(case.x), pin(case.ids), pin(case.w)
+        out_h = torch.empty((cfg.tokens, cfg.H), dtype=torch.bfloat16).pin_memory()
+        x_d, ids_d, w_d = torch.empty_like(case.x), torch.empty_like(case.ids), torch.empty_like(case.w)
+        h = moe.MoeHandle()
+        call = lambda: moe.moe_forward_host(layer.geom, x_h, ids_h, w_h, out_h, x_d, ids_d, w_d,  # noqa: E731
+                                            layer.out, layer.w1p, layer.w2, layer.expert_out,
+                                            layer.workspace, h)
+        for _ in range(max(args.warmup, 3)):
+            flush.zero_()
+            call()
+        torch.cuda.synchronize()
+        e2e_ms = []
+        for _ in range(args.steps):
+            flush.zero_()
+            ev0.record()
+            call()
+            ev1.record()
+            ev1.synchronize()
+            e2e_ms.append(ev0.elapsed_time(ev1))
+        if moe.moe_get_status(h) != 0:
+            raise RuntimeError("device status after e2e steps")
+        if not torch.equal(out_h.view(torch.int16), layer.out.cpu().view(torch.int16)):
+            raise RuntimeError("host-buffer output differs from the device output")
+        e2e_s = sum(e2e_ms) / 1e3
+        if dist is not None:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": cfg.tokens * args.steps * world / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": x_h.numel() * 2 + ids_h.numel() * ids_h.element_size() + w_h.numel() * 4,
+               "d2h_bytes_per_step": out_h.numel() * 2}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = min(ORACLE_SAMPLE_TOKENS.get(cfg.name, 8), cfg.tokens)
+        reps = 2
+        secs = min(oracle_sample_time(cfg, case, n) for _ in range(reps))
+        cpu = {"value": n / secs, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": "first %d of %d tokens (full routing; FFN + combine of the sample), best of %d"
+                         % (n, cfg.tokens, reps)}
+
+    per_step = 7 if cfg.layout == "EM" else 9
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "ours",
+            "config": workload_config(cfg, world),
+            "stages_us": {k: round(v * 1e3, 2) for k, v in kmean.items()},
+            "roofline": roof, "layer_roofline": layer_roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": per_step * args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    import gen
+    cfg = gen.ALL[args.config]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group(backend="nccl")
+        dist = tdist
+    run_ours(args, cfg, rank, world, dist)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

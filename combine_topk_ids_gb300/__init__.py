@@ -1,0 +1,257 @@
+"""Python binding of libmoe, the one-GPU MoE expert-parallel layer (include/moe.h).
+
+Argument marshalling only: every step of dispatch -> grouped SwiGLU FFN -> combine runs in
+the library's sm_103a kernels.  PyTorch provides device memory and the current stream.
+There is no fallback: if libmoe.so is missing, or the device is not a GB300, the calls
+raise.
+
+Functions carry the C names: moe_workspace_size, moe_expert_out_size, moe_dispatch,
+moe_prepare_weights, moe_expert_ffn, moe_combine, moe_get_status.  MoELayer1GPU bundles
+them with the buffers of one geometry.
+"""
+import ctypes
+import os
+
+from .build import LIB_PATH, build  # noqa: F401
+
+LAYOUT = {"EM": 0, "RM": 1, "FLAT": 2}
+ALGO = {"LL": 0, "HT": 1}
+IDS_INT32, IDS_INT64 = 0, 1
+STATUS_BAD_EXPERT_ID, STATUS_EM_OVERFLOW, STATUS_TIMEOUT = 0x1, 0x2, 0x4
+
+
+class MoeGeom(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "world", "max_tok", "num_tokens", "hidden", "num_experts", "top_k", "intermediate",
+        "layout", "algorithm")]
+
+
+_P = ctypes.c_void_p
+_HANDLE_PTRS = ("recv_x", "counts", "offsets", "pick_pos", "pick_src", "slot", "layout_range",
+                "recv_row", "recv_count", "num_recv", "recv_src", "recv_topk_idx",
+                "recv_topk_weights", "status", "workspace")
+
+
+class MoeHandle(ctypes.Structure):
+    _fields_ = ([("geom", MoeGeom)] + [(n, _P) for n in _HANDLE_PTRS] +
+                [("workspace_bytes", ctypes.c_size_t), ("events", ctypes.POINTER(ctypes.c_void_p)),
+                 ("num_events", ctypes.c_int32), ("magic", ctypes.c_uint64)])
+
+
+# event slots of MoeHandle.events (MOE_EV_* in include/moe.h)
+EV_DISPATCH_BEGIN, EV_ROUTING_END, EV_DISPATCH_END, EV_FFN_BEGIN, EV_GATHER_END, \
+    EV_GEMM1_END, EV_GEMM2_END, EV_FFN_END, EV_COMBINE_BEGIN, EV_COMBINE_END = range(10)
+EV_COUNT = 10
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (where, strerror(code), code))
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libmoe.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libmoe.so is not built (%s); run combine_topk_ids_gb300.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        G, H = ctypes.POINTER(MoeGeom), ctypes.POINTER(MoeHandle)
+        sz = ctypes.POINTER(ctypes.c_size_t)
+        L.moe_workspace_size.argtypes = [G, sz]
+        L.moe_expert_out_size.argtypes = [G, sz]
+        L.moe_dispatch.argtypes = [G, _P, _P, ctypes.c_int, _P, _P, ctypes.c_size_t, H, _P]
+        L.moe_prepare_weights.argtypes = [G, _P, _P, _P]
+        L.moe_expert_ffn.argtypes = [H, _P, _P, _P, _P]
+        L.moe_combine.argtypes = [H, _P, _P, _P, _P]
+        L.moe_get_status.argtypes = [H, ctypes.POINTER(ctypes.c_int32), _P]
+        L.moe_forward_host.argtypes = [G, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, ctypes.c_size_t, H, _P]
+        L.moe_strerror.argtypes = [ctypes.c_int]
+        L.moe_strerror.restype = ctypes.c_char_p
+        for f in ("moe_workspace_size", "moe_expert_out_size", "moe_dispatch",
+                  "moe_prepare_weights", "moe_expert_ffn", "moe_combine", "moe_get_status",
+                  "moe_forward_host"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().moe_strerror(int(code)).decode()
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise MoeError(rc, where)
+
+
+def make_geom(W, Tr, T, H, E, k, I, layout="EM", algo="LL") -> MoeGeom:
+    return MoeGeom(W, Tr, T, H, E, k, I, LAYOUT[layout] if isinstance(layout, str) else layout,
+                   ALGO[algo] if isinstance(algo, str) else algo)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def moe_workspace_size(g: MoeGeom) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_workspace_size(ctypes.byref(g), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_expert_out_size(g: MoeGeom) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_expert_out_size(ctypes.byref(g), ctypes.byref(n)), "moe_expert_out_size")
+    return n.value
+
+
+def _ids_dtype(t):
+    import torch
+    return {torch.int64: IDS_INT64, torch.int32: IDS_INT32}.get(t.dtype, 99)
+
+
+def moe_dispatch(g, x, topk_ids, topk_weights, workspace, stream=None, handle=None) -> MoeHandle:
+    """handle: optional MoeHandle to fill (its events fields are kept)."""
+    h = MoeHandle() if handle is None else handle
+    ids_dtype = _ids_dtype(topk_ids)
+    _check(lib().moe_dispatch(ctypes.byref(g), _ptr(x), _ptr(topk_ids), ids_dtype,
+                              _ptr(topk_weights), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              ctypes.byref(h), _stream(stream)), "moe_dispatch")
+    return h
+
+
+def moe_prepare_weights(g, w1, w1_prepared, stream=None):
+    _check(lib().moe_prepare_weights(ctypes.byref(g), _ptr(w1), _ptr(w1_prepared), _stream(stream)),
+           "moe_prepare_weights")
+
+
+def moe_expert_ffn(h, w1_prepared, w2, expert_out, stream=None):
+    _check(lib().moe_expert_ffn(ctypes.byref(h), _ptr(w1_prepared), _ptr(w2), _ptr(expert_out),
+                                _stream(stream)), "moe_expert_ffn")
+
+
+def moe_combine(h, expert_out, topk_weights, out, stream=None):
+    _check(lib().moe_combine(ctypes.byref(h), _ptr(expert_out), _ptr(topk_weights), _ptr(out),
+                             _stream(stream)), "moe_combine")
+
+
+def moe_forward_host(g, x_host, ids_host, w_host, out_host, x_dev, ids_dev, w_dev, out_dev,
+                     w1_prepared, w2, expert_out, workspace, handle, stream=None):
+    """The whole layer from host buffers (pinned torch CPU tensors), one C call."""
+    _check(lib().moe_forward_host(
+        ctypes.byref(g), _ptr(x_host), _ptr(ids_host), _ids_dtype(ids_host), _ptr(w_host),
+        _ptr(out_host), _ptr(x_dev), _ptr(ids_dev), _ptr(w_dev), _ptr(out_dev), _ptr(w1_prepared),
+        _ptr(w2), _ptr(expert_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        ctypes.byref(handle), _stream(stream)), "moe_forward_host")
+
+
+def moe_get_status(h, stream=None) -> int:
+    v = ctypes.c_int32()
+    _check(lib().moe_get_status(ctypes.byref(h), ctypes.byref(v), _stream(stream)), "moe_get_status")
+    return v.value
+
+
+def handle_view(h: MoeHandle, workspace, field: str, shape, dtype):
+    """A torch view of one handle array (it lives inside `workspace`), for inspection."""
+    import torch
+    ptr = getattr(h, field)
+    off = ptr - workspace.data_ptr()
+    n = 1
+    for s in shape:
+        n *= s
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    return workspace.view(torch.uint8)[off:off + nbytes].view(dtype).view(*shape)
+
+
+class MoELayer1GPU:
+    """One MoE EP layer of a fixed geometry with its buffers on the current CUDA device.
+
+    forward(x, topk_ids, topk_weights) = moe_dispatch -> moe_expert_ffn -> moe_combine,
+    all on the current stream, no host synchronisation.
+    """
+
+    def __init__(self, W, Tr, T, H, E, k, I, layout="EM", algo="LL", device="cuda"):
+        import torch
+        self.geom = make_geom(W, Tr, T, H, E, k, I, layout, algo)
+        self.device = torch.device(device)
+        self.workspace = torch.empty(moe_workspace_size(self.geom), dtype=torch.uint8, device=self.device)
+        self.expert_out = torch.empty(moe_expert_out_size(self.geom) // 4, dtype=torch.float32,
+                                      device=self.device)
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=self.device)
+        self.w1p = None
+        self.w2 = None
+        self.handle = MoeHandle()
+        self.events = None
+        self._ev_array = None
+
+    def enable_timing(self, on=True):
+        """Record MOE_EV_* CUDA events between the kernels of every call (per-kernel times)."""
+        import torch
+        if not on:
+            self.events, self._ev_array = None, None
+            self.handle.events, self.handle.num_events = None, 0
+            return
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(EV_COUNT)]
+        for e in self.events:
+            e.record()   # creates the underlying cudaEvent_t
+        self._ev_array = (ctypes.c_void_p * EV_COUNT)(*[e.cuda_event for e in self.events])
+        self.handle.events = ctypes.cast(self._ev_array, ctypes.POINTER(ctypes.c_void_p))
+        self.handle.num_events = EV_COUNT
+
+    def kernel_times_ms(self):
+        """Per-kernel milliseconds of the last forward (enable_timing must be on)."""
+        e = self.events
+        t = lambda a, b: e[a].elapsed_time(e[b])  # noqa: E731
+        em = self.geom.layout == LAYOUT["EM"]
+        d = {"routing": t(EV_DISPATCH_BEGIN, EV_ROUTING_END),
+             "dispatch_copy": t(EV_ROUTING_END, EV_DISPATCH_END),
+             "gemm1_swiglu": t(EV_GATHER_END, EV_GEMM1_END),
+             "gemm2": t(EV_GEMM1_END, EV_GEMM2_END),
+             "combine": t(EV_COMBINE_BEGIN, EV_COMBINE_END)}
+        if not em:
+            d["gather_picks"] = t(EV_FFN_BEGIN, EV_GATHER_END)
+            d["reduce_ranks"] = t(EV_GEMM2_END, EV_FFN_END)
+        d["dispatch"] = t(EV_DISPATCH_BEGIN, EV_DISPATCH_END)
+        d["ffn"] = t(EV_FFN_BEGIN, EV_FFN_END)
+        return d
+
+    def set_weights(self, w1, w2):
+        import torch
+        self.w1p = torch.empty_like(w1)
+        moe_prepare_weights(self.geom, w1, self.w1p)
+        self.w2 = w2
+
+    def dispatch(self, x, topk_ids, topk_weights):
+        moe_dispatch(self.geom, x, topk_ids, topk_weights, self.workspace, handle=self.handle)
+        return self.handle
+
+    def expert_ffn(self):
+        moe_expert_ffn(self.handle, self.w1p, self.w2, self.expert_out)
+        return self.expert_out
+
+    def combine(self, topk_weights):
+        moe_combine(self.handle, self.expert_out, topk_weights, self.out)
+        return self.out
+
+    def forward(self, x, topk_ids, topk_weights):
+        self.dispatch(x, topk_ids, topk_weights)
+        self.expert_ffn()
+        return self.combine(topk_weights)
+
+    def status(self) -> int:
+        return moe_get_status(self.handle)
+
+    def view(self, field, shape, dtype):
+        return handle_view(self.handle, self.workspace, field, shape, dtype)

@@ -1,0 +1,480 @@
+// Grouped SwiGLU expert FFN on 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// Operation (FlashInfer "MoE-EP implementation & usage", section 2 "Call stack": a pure
+// per-expert grouped GEMM with no routing; section 4 step 1: w1 [E, 2I, H], w2 [E, H, I]):
+// for every expert e and each of its n_e rows x,
+//     GEMM1   h   = x W1[e]^T            [n_e, 2I], fp32 accumulate in tensor memory
+//     SwiGLU  act = bf16(silu(h[:, :I]) * h[:, I:])      (fused into GEMM1's epilogue)
+//     GEMM2   y   = act W2[e]^T          [n_e, H],  fp32, written as fp32
+//
+// One persistent kernel per GEMM, one CTA per SM, 256 threads:
+//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage (SWIZZLE_128B),
+//               a 4-stage mbarrier ring
+//   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16, M=128,
+//               N=256, K=16, bf16 x bf16 -> fp32 into one of two 256-column TMEM
+//               accumulators, tcgen05.commit frees smem stages and hands tiles over
+//   warp 2      TMEM allocator (512 columns)
+//   warps 4-7   epilogue: tcgen05.ld 32x32b rows -> registers -> SwiGLU / fp32 store,
+//               overlapped with the next tile's mainloop (double-buffered accumulator)
+// Tiles: per expert ceil(n_e/128) m-blocks x (N/256) n-blocks, enumerated expert by expert,
+// n-block-major with the m-blocks of one weight tile adjacent (they run on neighbouring
+// SMs at the same time and share the weight tile through L2).  Experts with no rows issue
+// no tiles and read no weights.  Every mbarrier wait is bounded: on timeout the kernel
+// sets MOE_STATUS_TIMEOUT, drains and frees its tensor memory, and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;   // BN: widest n-tile (GEMM2 may use 128)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int THREADS = 256;
+constexpr int TMEM_COLS = 2 * BN;               // two fp32 accumulators of 128 x 256
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A bf16
+// (bits 7-9 = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15/16 = 0),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(BM >> 4) << 24);
+}
+
+struct FfnArgs {
+    const int32_t *counts, *offsets, *mprefix;
+    int E;
+    int bn;        // n-tile width: 256 or 128
+    int nb;        // n-blocks per expert (N / bn)
+    int kb;        // k-blocks (K / BK)
+    int a_mode;    // 0: A row = e*a_cap + m; 1: A row = offsets[e] + m
+    int64_t a_cap;
+    int64_t b_rows;   // rows of B per expert (N)
+    int mode;      // 0: SwiGLU epilogue -> bf16 act; 1: fp32 store
+    void *out;
+    int64_t out_ld;   // elements per output row
+    int out_mode;  // 0: row = e*out_cap + m; 1: row = offsets[e] + m
+    int64_t out_cap;
+    int32_t *status;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete.  Returns false (and raises the
+// CTA-wide abort flag and the device status bit) when it gave up or another role did.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(status, MOE_STATUS_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format) of a K-major SWIZZLE_128B operand tile:
+// start address >> 4 (bits 0-13), leading byte offset 16 >> 4 (unused for swizzled
+// K-major), stride byte offset 1024 >> 4 (8 rows x 128 B; bits 32-45), descriptor version
+// 1 (bits 46-47), base offset 0 (tiles are 1024-byte aligned), layout SWIZZLE_128B = 2
+// (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets row (lane base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Tile index -> (expert, m-block, n-block).  Experts are laid out by the m-block prefix:
+// expert e owns tiles [mprefix[e]*nb, mprefix[e+1]*nb); inside, n-block-major.
+__device__ __forceinline__ void decode_tile(const FfnArgs &a, int tile, int &e, int &mb, int &nbk) {
+    const int q = tile / a.nb;
+    int lo = 0, hi = a.E - 1;   // largest e with mprefix[e] <= q
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.mprefix + mid) <= q) lo = mid;
+        else hi = mid - 1;
+    }
+    e = lo;
+    const int m0 = __ldg(a.mprefix + e);
+    const int mt = __ldg(a.mprefix + e + 1) - m0;
+    const int local = tile - m0 * a.nb;
+    nbk = local / mt;
+    mb = local - nbk * mt;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return g / (1.0f + __expf(-g)) * u;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    FfnArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(tfull0 + 8 * s, 1);
+            mbar_init(tempty0 + 8 * s, 128);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = __ldg(a.mprefix + a.E) * a.nb;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------- TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            int e, mb, nbk;
+            decode_tile(a, tile, e, mb, nbk);
+            const int64_t arow = (a.a_mode == 0 ? (int64_t)e * a.a_cap : (int64_t)__ldg(a.offsets + e)) +
+                                 (int64_t)mb * BM;
+            const int64_t brow = (int64_t)e * a.b_rows + (int64_t)nbk * a.bn;
+            const uint32_t tx = (uint32_t)(A_BYTES + a.bn * BK * 2);
+            for (int kb = 0; kb < a.kb; ++kb) {
+                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+                const uint32_t fb = full0 + 8 * stage;
+                mbar_expect_tx(fb, tx);
+                tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmA, kb * BK, (int)arow, fb);
+                tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmB, kb * BK, (int)brow, fb);
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        const uint32_t idesc = make_idesc(a.bn);
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, a.status)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < a.kb; ++kb) {
+                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
+                const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                             (kb | kk) != 0 ? 1u : 0u);
+                mma_commit(empty0 + 8 * stage);   // stage reusable once these MMAs finish
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+            mma_commit(tfull0 + 8 * acc);          // accumulator ready for the epilogue
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------------ epilogue
+        const int quad = warp & 3;                 // TMEM lanes 32*quad .. 32*quad+31
+        const int row = quad * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            int e, mb, nbk;
+            decode_tile(a, tile, e, mb, nbk);
+            const int valid = min(BM, __ldg(a.counts + e) - mb * BM);
+            const int64_t orow = (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) +
+                                 (int64_t)mb * BM + row;
+            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, a.status)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
+            if (a.mode == 0) {
+                // columns [0,128) gate, [128,256) up of act columns nbk*128 .. +128
+                __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) + orow * a.out_ld +
+                                     (int64_t)nbk * (BN / 2);
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 32) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(tbase + c, g);
+                    tmem_ld32(tbase + BN / 2 + c, u);
+                    tmem_wait_ld();
+                    if (row < valid) {
+                        uint4 *o = reinterpret_cast<uint4 *>(out + c);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const int i = v * 8 + h * 2;
+                                __nv_bfloat162 p = __floats2bfloat162_rn(
+                                    silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i])),
+                                    silu_mul(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1])));
+                                w[h] = *reinterpret_cast<uint32_t *>(&p);
+                            }
+                            o[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+            } else {
+                float *out = reinterpret_cast<float *>(a.out) + orow * a.out_ld + (int64_t)nbk * a.bn;
+#pragma unroll 1
+                for (int c = 0; c < a.bn; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c, v);
+                    tmem_wait_ld();
+                    if (row < valid) {
+                        float4 *o = reinterpret_cast<float4 *>(out + c);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            o[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty0 + 8 * acc);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag) {
+        // Give in-flight TMA copies and MMAs time to land before the memory is released.
+        unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 1000000ull) {}
+    }
+    if (warp == 2) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 row-major [rows, cols] tensor map with a box of box_rows x 64 columns,
+// SWIZZLE_128B (the box's 128-byte rows land in shared memory in the canonical K-major
+// 128B-swizzled layout the MMA descriptors above describe).
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const FfnArgs &args, int64_t max_tiles,
+                cudaStream_t s) {
+    if (max_tiles <= 0) return MOE_OK;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(ffn_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+    int grid = num_sms();
+    if ((int64_t)grid > max_tiles) grid = (int)max_tiles;
+    ffn_gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, args);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace {
+// upper bound of the m-blocks over all experts: sum ceil(n_e/128) <= P/128 + E
+int64_t max_mblocks(const Plan &p) { return p.P / BM + p.E; }
+
+FfnArgs base_args(const Routing &r) {
+    const Plan &p = *r.p;
+    FfnArgs g{};
+    g.counts = r.counts; g.offsets = r.offsets; g.mprefix = r.mprefix; g.E = (int)p.E;
+    g.status = r.status;
+    return g;
+}
+}  // namespace
+
+int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s) {
+    const Plan &p = *r.p;
+    if (p.P == 0) return MOE_OK;
+    const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    CUtensorMap mA, mB;
+    const void *a1 = em ? (const void *)r.recv_x : (const void *)r.apick;
+    const int64_t a1_rows = em ? p.E * p.cap : p.P;
+    if (!make_map(&mA, a1, a1_rows, p.H, BM) || !make_map(&mB, w1p, p.E * 2 * p.I, p.H, BN))
+        return MOE_ERR_CUDA;
+    FfnArgs g = base_args(r);
+    g.bn = BN; g.nb = (int)(2 * p.I / BN); g.kb = (int)(p.H / BK);
+    g.a_mode = em ? 0 : 1; g.a_cap = p.cap; g.b_rows = 2 * p.I;
+    g.mode = 0; g.out = r.act; g.out_ld = p.I; g.out_mode = 1; g.out_cap = 0;
+    return launch_gemm(mA, mB, g, max_mblocks(p) * g.nb, s);
+}
+
+int launch_gemm2(const Routing &r, const uint16_t *w2, float *expert_out, cudaStream_t s) {
+    const Plan &p = *r.p;
+    if (p.P == 0) return MOE_OK;
+    const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    const int bn = (p.H % 256 == 0) ? 256 : 128;
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, r.act, p.P, p.I, BM) || !make_map(&mB, w2, p.E * p.H, p.I, bn))
+        return MOE_ERR_CUDA;
+    FfnArgs g = base_args(r);
+    g.bn = bn; g.nb = (int)(p.H / bn); g.kb = (int)(p.I / BK);
+    g.a_mode = 1; g.a_cap = 0; g.b_rows = p.H; g.mode = 1; g.out_ld = p.H;
+    if (em) { g.out = expert_out; g.out_mode = 0; g.out_cap = p.cap; }
+    else { g.out = r.ypick; g.out_mode = 1; g.out_cap = 0; }
+    return launch_gemm(mA, mB, g, max_mblocks(p) * g.nb, s);
+}
+
+}  // namespace moe

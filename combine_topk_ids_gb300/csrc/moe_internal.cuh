@@ -1,0 +1,63 @@
+// Internal declarations shared by the library's translation units: workspace plan,
+// kernel launch wrappers and small device helpers.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kRouteThreads = 256;   // 8 warps per routing block
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kTileM = 128;          // GEMM rows per tile (one tcgen05 M=128 MMA)
+constexpr uint64_t kHandleMagic = 0x4d6f4545702d3130ull;
+
+// Byte offsets of every region of the workspace, derived from the geometry alone.
+struct Plan {
+    int64_t T, W, Tr, cap, E, k, H, I, P;   // P = T*k picks
+    int layout;
+    int tb;         // tokens per routing block
+    int nbpr;       // routing blocks per logical rank
+    int nb;         // routing blocks in total (W * nbpr)
+    size_t status, counts, offsets, mprefix, pick_pos, pick_src, slot, layout_range,
+        blk_hist, blk_base, recv_row, recv_count, num_recv, recv_src, recv_topk_idx,
+        recv_topk_w, blk_dhist, blk_dbase, recv_x, act, apick, ypick, total;
+};
+
+// Returns MOE_OK or a moe_error for an invalid geometry.
+int make_plan(const moe_geom &g, Plan *p);
+
+// Workspace pointers of one dispatch.
+struct Routing {
+    const Plan *p;
+    int32_t *status, *counts, *offsets, *mprefix, *pick_pos, *pick_src, *slot, *layout_range,
+        *blk_hist, *blk_base, *recv_row, *recv_count, *num_recv, *recv_src, *recv_topk_idx,
+        *blk_dhist, *blk_dbase;
+    float *recv_topk_w;
+    uint16_t *recv_x, *act, *apick;
+    float *ypick;
+};
+
+Routing carve(const Plan &p, void *ws);
+
+// ---- launchers (return cudaGetLastError of the launch) -------------------------------
+cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const float *topk_w,
+                           cudaStream_t s);
+cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream_t s);
+cudaError_t launch_gather_picks(const Routing &r, cudaStream_t s);
+cudaError_t launch_reduce_ranks(const Routing &r, float *expert_out, cudaStream_t s);
+cudaError_t launch_combine(const Routing &r, const float *expert_out, const float *topk_w,
+                           uint16_t *out, cudaStream_t s);
+cudaError_t launch_prepare_w1(const moe_geom &g, const uint16_t *w1, uint16_t *w1p,
+                              cudaStream_t s);
+// Grouped SwiGLU FFN: GEMM1 (+SiLU*mul) into act, GEMM2 into expert_out (EM) or the
+// per-pick scratch (RM/FLAT).  Return MOE_OK or a moe_error.
+int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s);
+int launch_gemm2(const Routing &r, const uint16_t *w2, float *expert_out, cudaStream_t s);
+
+int num_sms();   // SM count of the current device (cached per device)
+
+}  // namespace moe

@@ -1,0 +1,359 @@
+// Routing kernels of moe_dispatch: per-expert / per-destination histograms, block prefix
+// sums, and deterministic slot assignment in ascending (token, pick) order.
+//
+// Operation (Mooncake EP guide, "Buffer.dispatch(...)": topk_idx with -1 for masked picks,
+// the local-expert-major packed layout with packed_recv_count / packed_recv_layout_range;
+// FlashInfer "MoE-EP implementation & usage", section 3 "Algorithm / layout contracts":
+// EXPERT_MAJOR rows pre-assigned to experts, RANK_MAJOR rows grouped by source rank,
+// FLAT token-major, received topk_idx LOCAL with -1 for non-local picks).
+//
+// Three launches, no atomics deciding any position:
+//   route_count   one block per (logical rank, token chunk): shared-memory histogram of the
+//                 chunk's expert ids (and of the destination ranks of its tokens)
+//   route_scan    one block: per expert / destination an exclusive scan over the chunks,
+//                 split at logical-rank boundaries (layout ranges, RANK_MAJOR rows), then
+//                 the expert offsets and the GEMM m-block prefix
+//   route_assign  one block per chunk: every warp owns a contiguous run of picks, counts its
+//                 run, takes an exclusive prefix over the block's warps, and then ranks its
+//                 picks 32 at a time with __match_any_sync / __ballot_sync.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+struct RouteArgs {
+    const void *ids;
+    int ids64;
+    const float *topk_w;
+    int T, W, Tr, E, k, Le, layout, tb, nbpr, nb;
+    int64_t cap;
+    int32_t *status, *counts, *offsets, *mprefix, *pick_pos, *pick_src, *slot, *layout_range;
+    int32_t *blk_hist, *blk_base;   // [E][nb]
+    int32_t *recv_row, *recv_count, *num_recv, *recv_src, *recv_topk_idx;
+    int32_t *blk_dhist, *blk_dbase; // [W][nb]
+    float *recv_topk_w;
+};
+
+// Expert id of pick i: [0, E) valid, -1 masked, -2 outside [-1, E).
+__device__ __forceinline__ int load_id(const RouteArgs &a, int64_t i) {
+    long long v = a.ids64 ? reinterpret_cast<const long long *>(a.ids)[i]
+                          : (long long)reinterpret_cast<const int *>(a.ids)[i];
+    if (v == -1) return -1;
+    if (v < -1 || v >= a.E) return -2;
+    return (int)v;
+}
+
+// Bit d set iff token t has a valid pick on destination rank d.
+__device__ __forceinline__ unsigned long long dest_mask(const RouteArgs &a, int t) {
+    unsigned long long m = 0;
+    for (int j = 0; j < a.k; ++j) {
+        int e = load_id(a, (int64_t)t * a.k + j);
+        if (e >= 0) m |= 1ull << (e / a.Le);
+    }
+    return m;
+}
+
+// Tokens [t0, t1) of routing block b: chunk (b % nbpr) of logical rank b / nbpr.
+__device__ __forceinline__ void block_tokens(const RouteArgs &a, int b, int &t0, int &t1) {
+    int r = b / a.nbpr;
+    t0 = r * a.Tr + (b % a.nbpr) * a.tb;
+    t1 = min(min(t0 + a.tb, (r + 1) * a.Tr), a.T);
+    if (t0 > t1) t0 = t1;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+    int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_count_kernel(RouteArgs a) {
+    extern __shared__ int sm[];
+    int *hist = sm;          // [E]
+    int *dhist = sm + a.E;   // [W]
+    for (int i = threadIdx.x; i < a.E + a.W; i += blockDim.x) sm[i] = 0;
+    __syncthreads();
+    int t0, t1;
+    block_tokens(a, blockIdx.x, t0, t1);
+    bool bad = false;
+    for (int64_t i = (int64_t)t0 * a.k + threadIdx.x; i < (int64_t)t1 * a.k; i += blockDim.x) {
+        int e = load_id(a, i);
+        if (e >= 0) atomicAdd(&hist[e], 1);   // counts only; positions come later
+        else if (e == -2) bad = true;
+    }
+    if (a.layout != MOE_LAYOUT_EXPERT_MAJOR) {
+        for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+            unsigned long long m = dest_mask(a, t);
+            while (m) {
+                int d = __ffsll((long long)m) - 1;
+                m &= m - 1;
+                atomicAdd(&dhist[d], 1);
+            }
+        }
+    }
+    if (bad) atomicOr(a.status, MOE_STATUS_BAD_EXPERT_ID);
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x)
+        a.blk_hist[(int64_t)e * a.nb + blockIdx.x] = hist[e];
+    if (a.layout != MOE_LAYOUT_EXPERT_MAJOR)
+        for (int d = threadIdx.x; d < a.W; d += blockDim.x)
+            a.blk_dhist[(int64_t)d * a.nb + blockIdx.x] = dhist[d];
+}
+
+// Exclusive scan of one row hist[0..nb) (blocks grouped by logical rank) into base[],
+// warp-cooperative.  RANK_MAJOR destinations restart each rank at s*Tr.  Lane 0 gets the
+// per-rank sums through the callback.
+template <typename RankFn>
+__device__ __forceinline__ int scan_row(const RouteArgs &a, const int32_t *hist, int32_t *base,
+                                        bool restart_per_rank, RankFn on_rank) {
+    int lane = threadIdx.x & 31;
+    int run = 0;
+    for (int s = 0; s < a.W; ++s) {
+        if (restart_per_rank) run = s * a.Tr;
+        int begin = run;
+        int b_end = (s + 1) * a.nbpr;
+        for (int b0 = s * a.nbpr; b0 < b_end; b0 += 32) {
+            int b = b0 + lane;
+            int v = b < b_end ? hist[b] : 0;
+            int incl = warp_incl_scan(v);
+            if (b < b_end) base[b] = run + incl - v;
+            run += __shfl_sync(kFull, incl, 31);
+        }
+        on_rank(s, begin, run - begin);
+    }
+    return run;
+}
+
+__global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
+    __shared__ int wsum[2][32];
+    __shared__ int carry[2];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    // (1) per expert: chunk bases, layout ranges, counts (EM clamps to the region size)
+    for (int e = warp; e < a.E; e += nwarps) {
+        int total = scan_row(a, a.blk_hist + (int64_t)e * a.nb, a.blk_base + (int64_t)e * a.nb,
+                             false, [&](int s, int begin, int cnt) {
+                                 if (lane == 0) {
+                                     int64_t lim = em ? a.cap : (int64_t)1 << 40;
+                                     int64_t b = begin < lim ? begin : lim;
+                                     int64_t kept = lim - begin;
+                                     kept = kept < 0 ? 0 : (kept > cnt ? cnt : kept);
+                                     a.layout_range[((int64_t)e * a.W + s) * 2 + 0] = (int)b;
+                                     a.layout_range[((int64_t)e * a.W + s) * 2 + 1] = (int)kept;
+                                 }
+                             });
+        if (lane == 0) a.counts[e] = (em && total > a.cap) ? (int)a.cap : total;
+    }
+    // (1b) per destination rank (RANK_MAJOR / FLAT): chunk row bases and received counts
+    if (!em) {
+        for (int d = warp; d < a.W; d += nwarps) {
+            int total = scan_row(a, a.blk_dhist + (int64_t)d * a.nb, a.blk_dbase + (int64_t)d * a.nb,
+                                 a.layout == MOE_LAYOUT_RANK_MAJOR, [&](int s, int, int cnt) {
+                                     if (lane == 0) a.recv_count[d * a.W + s] = cnt;
+                                 });
+            if (lane == 0) {
+                // RANK_MAJOR's running value includes the s*Tr row base of the last rank
+                int n = 0;
+                for (int s = 0; s < a.W; ++s) n += a.recv_count[d * a.W + s];
+                a.num_recv[d] = n;
+                (void)total;
+            }
+        }
+    }
+    __syncthreads();
+    // (2) expert offsets and m-block (128-row GEMM tile) prefix over experts
+    if (threadIdx.x == 0) carry[0] = carry[1] = 0;
+    __syncthreads();
+    for (int e0 = 0; e0 < a.E; e0 += blockDim.x) {
+        int e = e0 + threadIdx.x;
+        int c = e < a.E ? a.counts[e] : 0;
+        int m = (c + kTileM - 1) / kTileM;
+        int ic = warp_incl_scan(c), im = warp_incl_scan(m);
+        if (lane == 31) { wsum[0][warp] = ic; wsum[1][warp] = im; }
+        __syncthreads();
+        if (warp == 0) {
+            int v0 = lane < nwarps ? wsum[0][lane] : 0, v1 = lane < nwarps ? wsum[1][lane] : 0;
+            int s0 = warp_incl_scan(v0), s1 = warp_incl_scan(v1);
+            wsum[0][lane] = s0 - v0;
+            wsum[1][lane] = s1 - v1;
+        }
+        __syncthreads();
+        if (e < a.E) {
+            a.offsets[e] = carry[0] + wsum[0][warp] + ic - c;
+            a.mprefix[e] = carry[1] + wsum[1][warp] + im - m;
+        }
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) {
+            carry[0] += wsum[0][warp] + ic;
+            carry[1] += wsum[1][warp] + im;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        a.offsets[a.E] = carry[0];
+        a.mprefix[a.E] = carry[1];
+    }
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(RouteArgs a) {
+    extern __shared__ int sm[];
+    int *cur = sm;                          // [warps][E] running position inside expert
+    int *dcur = sm + kRouteWarps * a.E;     // [warps][W] running row inside destination
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, b = blockIdx.x;
+    const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    for (int i = threadIdx.x; i < kRouteWarps * (a.E + a.W); i += blockDim.x) sm[i] = 0;
+    int t0, t1;
+    block_tokens(a, b, t0, t1);
+    // this warp's contiguous run of picks [wp0, wp1) and tokens [wt0, wt1)
+    const int64_t p0 = (int64_t)t0 * a.k, np = (int64_t)(t1 - t0) * a.k;
+    const int64_t ppw = (np + kRouteWarps * 32 - 1) / (kRouteWarps * 32) * 32;
+    const int64_t wp0 = min(p0 + warp * ppw, p0 + np), wp1 = min(wp0 + ppw, p0 + np);
+    const int tpw = ((t1 - t0) + kRouteWarps * 32 - 1) / (kRouteWarps * 32) * 32;
+    const int wt0 = min(t0 + warp * tpw, t1), wt1 = min(wt0 + tpw, t1);
+    __syncthreads();
+    // pass 1: per-warp counts
+    for (int64_t i0 = wp0; i0 < wp1; i0 += 32) {
+        int64_t i = i0 + lane;
+        int e = i < wp1 ? load_id(a, i) : -1;
+        int key = e >= 0 ? e : -1;
+        unsigned peers = __match_any_sync(kFull, key);
+        if (key >= 0 && lane == __ffs(peers) - 1) cur[warp * a.E + key] += __popc(peers);
+        __syncwarp();
+    }
+    if (!em) {
+        for (int tt = wt0; tt < wt1; tt += 32) {
+            int t = tt + lane;
+            unsigned long long m = t < wt1 ? dest_mask(a, t) : 0ull;
+            for (int d = 0; d < a.W; ++d) {
+                unsigned bal = __ballot_sync(kFull, (m >> d) & 1ull);
+                if (lane == 0) dcur[warp * a.W + d] += __popc(bal);
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // exclusive prefix over the block's warps, on top of the chunk's base
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+        int run = a.blk_base[(int64_t)e * a.nb + b];
+        for (int w = 0; w < kRouteWarps; ++w) {
+            int c = cur[w * a.E + e];
+            cur[w * a.E + e] = run;
+            run += c;
+        }
+    }
+    if (!em) {
+        for (int d = threadIdx.x; d < a.W; d += blockDim.x) {
+            int run = a.blk_dbase[(int64_t)d * a.nb + b];
+            for (int w = 0; w < kRouteWarps; ++w) {
+                int c = dcur[w * a.W + d];
+                dcur[w * a.W + d] = run;
+                run += c;
+            }
+        }
+    }
+    __syncthreads();
+    // pass 2: ranks of the picks
+    bool overflow = false;
+    for (int64_t i0 = wp0; i0 < wp1; i0 += 32) {
+        int64_t i = i0 + lane;
+        int e = i < wp1 ? load_id(a, i) : -1;
+        int key = e >= 0 ? e : -1;
+        unsigned peers = __match_any_sync(kFull, key);
+        int pos = key >= 0 ? cur[warp * a.E + key] + __popc(peers & lanemask_lt()) : 0;
+        __syncwarp();
+        if (key >= 0 && lane == __ffs(peers) - 1) cur[warp * a.E + key] += __popc(peers);
+        __syncwarp();
+        if (i < wp1) {
+            int pp = -1, sl = -1;
+            if (key >= 0) {
+                if (pos < a.counts[key]) {   // EM counts are clamped to the region's rows
+                    pp = a.offsets[key] + pos;
+                    sl = (int)((int64_t)key * a.cap + pos);
+                    a.pick_src[pp] = (int)i;
+                } else {
+                    overflow = true;
+                }
+            }
+            a.pick_pos[i] = pp;
+            if (em) a.slot[i] = sl;
+        }
+    }
+    if (overflow) atomicOr(a.status, MOE_STATUS_EM_OVERFLOW);
+    if (em) return;
+    // pass 2 for destinations: rows, source tokens, local ids and weights
+    for (int tt = wt0; tt < wt1; tt += 32) {
+        int t = tt + lane;
+        bool valid = t < wt1;
+        unsigned long long m = valid ? dest_mask(a, t) : 0ull;
+        for (int d = 0; d < a.W; ++d) {
+            bool has = (m >> d) & 1ull;
+            unsigned bal = __ballot_sync(kFull, has);
+            int row = dcur[warp * a.W + d] + __popc(bal & lanemask_lt());
+            __syncwarp();
+            if (lane == 0) dcur[warp * a.W + d] += __popc(bal);
+            __syncwarp();
+            if (!valid) continue;
+            if (!has) {
+                a.recv_row[(int64_t)t * a.W + d] = -1;
+                continue;
+            }
+            a.recv_row[(int64_t)t * a.W + d] = row;
+            int64_t o = (int64_t)d * a.cap + row;
+            a.recv_src[o] = t;
+            for (int j = 0; j < a.k; ++j) {
+                int ej = load_id(a, (int64_t)t * a.k + j);
+                bool local = ej >= 0 && ej / a.Le == d;
+                a.recv_topk_idx[o * a.k + j] = local ? ej - d * a.Le : -1;
+                a.recv_topk_w[o * a.k + j] = local ? a.topk_w[(int64_t)t * a.k + j] : 0.0f;
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const float *topk_w,
+                           cudaStream_t s) {
+    const Plan &p = *r.p;
+    RouteArgs a;
+    a.ids = ids;
+    a.ids64 = ids64;
+    a.topk_w = topk_w;
+    a.T = (int)p.T; a.W = (int)p.W; a.Tr = (int)p.Tr; a.E = (int)p.E; a.k = (int)p.k;
+    a.Le = (int)(p.E / p.W);
+    a.layout = p.layout;
+    a.tb = p.tb; a.nbpr = p.nbpr; a.nb = p.nb;
+    a.cap = p.cap;
+    a.status = r.status; a.counts = r.counts; a.offsets = r.offsets; a.mprefix = r.mprefix;
+    a.pick_pos = r.pick_pos; a.pick_src = r.pick_src; a.slot = r.slot;
+    a.layout_range = r.layout_range; a.blk_hist = r.blk_hist; a.blk_base = r.blk_base;
+    a.recv_row = r.recv_row; a.recv_count = r.recv_count; a.num_recv = r.num_recv;
+    a.recv_src = r.recv_src; a.recv_topk_idx = r.recv_topk_idx; a.recv_topk_w = r.recv_topk_w;
+    a.blk_dhist = r.blk_dhist; a.blk_dbase = r.blk_dbase;
+
+    size_t sm1 = (size_t)(a.E + a.W) * sizeof(int);
+    route_count_kernel<<<a.nb, kRouteThreads, sm1, s>>>(a);
+    route_scan_kernel<<<1, 1024, 0, s>>>(a);
+    size_t sm3 = (size_t)kRouteWarps * (a.E + a.W) * sizeof(int);
+    if (sm3 > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(route_assign_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3);
+        if (e != cudaSuccess) return e;
+    }
+    route_assign_kernel<<<a.nb, kRouteThreads, sm3, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

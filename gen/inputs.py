@@ -84,18 +84,24 @@ def weights_on_host(cfg: MoeConfig) -> bool:
     return cfg.E * 3 * cfg.H * cfg.I <= NUMPY_WEIGHT_LIMIT
 
 
+def expert_weights_numpy(cfg: MoeConfig, e: int):
+    """Expert e's W1 [2I, H] and W2 [H, I] as bf16 bit patterns, from its own numpy streams."""
+    st = _streams(cfg.seed)
+    s1 = st[_STREAM_W1].spawn(cfg.E)[e]
+    s2 = st[_STREAM_W2].spawn(cfg.E)[e]
+    r1 = np.random.Generator(np.random.PCG64(s1))
+    r2 = np.random.Generator(np.random.PCG64(s2))
+    w1 = f32_to_bf16_bits(0.02 * r1.standard_normal((2 * cfg.I, cfg.H), dtype=np.float32))
+    w2 = f32_to_bf16_bits(0.02 * r2.standard_normal((cfg.H, cfg.I), dtype=np.float32))
+    return w1, w2
+
+
 def gen_weights_numpy(cfg: MoeConfig):
     """W1 [E, 2I, H] and W2 [E, H, I] as bf16 bit patterns, one numpy stream per expert."""
-    st = _streams(cfg.seed)
-    s1 = st[_STREAM_W1].spawn(cfg.E)
-    s2 = st[_STREAM_W2].spawn(cfg.E)
     w1 = np.empty((cfg.E, 2 * cfg.I, cfg.H), dtype=np.uint16)
     w2 = np.empty((cfg.E, cfg.H, cfg.I), dtype=np.uint16)
     for e in range(cfg.E):
-        r1 = np.random.Generator(np.random.PCG64(s1[e]))
-        r2 = np.random.Generator(np.random.PCG64(s2[e]))
-        w1[e] = f32_to_bf16_bits(0.02 * r1.standard_normal((2 * cfg.I, cfg.H), dtype=np.float32))
-        w2[e] = f32_to_bf16_bits(0.02 * r2.standard_normal((cfg.H, cfg.I), dtype=np.float32))
+        w1[e], w2[e] = expert_weights_numpy(cfg, e)
     return w1, w2
 
 

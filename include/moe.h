@@ -1,0 +1,257 @@
+/*
+ * moe.h - C ABI of a one-GPU Mixture-of-Experts expert-parallel layer for GB300 (sm_103a):
+ *
+ *     moe_dispatch  ->  moe_expert_ffn  ->  moe_combine
+ *
+ * The "world" of source ranks is a logical partition of one token batch that lives in one
+ * device buffer: token t belongs to logical rank t / max_tok and expert e lives on logical
+ * rank e / (num_experts / world).  There is no transport and no collective; the pages'
+ * all-to-all exchange becomes a row permutation inside one HBM.
+ *
+ * Sources (page title, section):
+ *   [MC-EP]  Mooncake EP user guide, "Mooncake EP API reference": Buffer.dispatch /
+ *            Buffer.combine / Buffer.get_ep_buffer_size_hint, the packed
+ *            local-expert-major receive layout and its handle, the input assertions.
+ *   [FI-3]   FlashInfer "MoE-EP implementation & usage", section 3 "Algorithm / layout
+ *            contracts": EXPERT_MAJOR / RANK_MAJOR / FLAT receive buffers, compute
+ *            routing and combine rules.
+ *   [FI-2]   same page, section 2 "Call stack": dispatch -> per-expert grouped GEMM
+ *            (no routing) -> combine -> [num_tokens, hidden] bf16.
+ *   [FI-4]   same page, section 4 step 1: w1 [E, 2*I, H], w2 [E, H, I].
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument named *_dev, every pointer inside moe_handle and the
+ *     workspace are DEVICE pointers of the current CUDA device.  Host pointers are named
+ *     *_host.  The caller owns and allocates all memory; the library never allocates,
+ *     frees or keeps global state beyond cached device attributes.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     stream-ordered and asynchronous: they return once the kernels are queued and never
+ *     synchronise the host (moe_get_status excepted).
+ *   - Return value: MOE_OK (0) or a negative moe_error.  Host-detected errors return
+ *     before anything is queued.  Errors found by the kernels (bad expert ids, an
+ *     overflowing expert region, a device wait that gave up) set bits of the handle's
+ *     device status word, read with moe_get_status; the offending pick is dropped,
+ *     never written out of bounds.
+ *   - bf16 arrays hold IEEE bfloat16 bit patterns (uint16).
+ */
+#ifndef COMBINE_TOPK_IDS_MOE_H
+#define COMBINE_TOPK_IDS_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Receive layout [FI-3]. */
+typedef enum {
+    MOE_LAYOUT_EXPERT_MAJOR = 0, /* [num_experts, world*max_tok, hidden], rows pre-assigned to experts */
+    MOE_LAYOUT_RANK_MAJOR = 1,   /* per destination rank: [world(source), max_tok, hidden]             */
+    MOE_LAYOUT_FLAT = 2          /* per destination rank: [num_recv, hidden] token-major               */
+} moe_layout;
+
+/* EpAlgorithm [FI-3]: recorded in the geometry; both run the same kernels on one GPU. */
+typedef enum { MOE_ALGO_LOW_LATENCY = 0, MOE_ALGO_HIGH_THROUGHPUT = 1 } moe_algorithm;
+
+typedef enum { MOE_IDS_INT32 = 0, MOE_IDS_INT64 = 1 } moe_ids_dtype;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARGUMENT = -1,      /* null pointer, non-positive size, bad enum          */
+    MOE_ERR_EXPERTS_NOT_DIVISIBLE = -2, /* num_experts % world != 0            [MC-EP] asserts */
+    MOE_ERR_HIDDEN_ALIGNMENT = -3,      /* hidden % 128 != 0                    [MC-EP] asserts */
+    MOE_ERR_INTERMEDIATE_ALIGNMENT = -4,/* intermediate % 128 != 0 (GEMM tiling)               */
+    MOE_ERR_TOO_MANY_TOKENS = -5,       /* num_tokens > world*max_tok  [MC-EP] max_tok rule     */
+    MOE_ERR_TOPK = -6,                  /* top_k < 1 or > MOE_MAX_TOPK                          */
+    MOE_ERR_IDS_DTYPE = -7,             /* ids dtype not int32/int64                            */
+    MOE_ERR_WORKSPACE_TOO_SMALL = -8,   /* workspace_bytes < moe_workspace_size()               */
+    MOE_ERR_MISALIGNED = -9,            /* a device pointer breaks its alignment rule           */
+    MOE_ERR_BAD_HANDLE = -10,           /* handle not filled by moe_dispatch                    */
+    MOE_ERR_CUDA = -11,                 /* a CUDA runtime call or kernel launch failed          */
+    MOE_ERR_NOT_BUILT_FOR_DEVICE = -12, /* device is not compute capability 10.3 (sm_103a)      */
+    MOE_ERR_LIMIT = -13                 /* world, num_experts or hidden beyond the limits below */
+} moe_error;
+
+/* Device status bits (moe_get_status). */
+#define MOE_STATUS_BAD_EXPERT_ID 0x1  /* an id outside [-1, num_experts): pick dropped          */
+#define MOE_STATUS_EM_OVERFLOW 0x2    /* EXPERT_MAJOR region full (a token named one expert
+                                         twice): the later picks were dropped                 */
+#define MOE_STATUS_TIMEOUT 0x4        /* a bounded device wait gave up; outputs are invalid    */
+
+/* Event slots of moe_handle.events (per-kernel timing). */
+#define MOE_EV_DISPATCH_BEGIN 0
+#define MOE_EV_ROUTING_END 1   /* after the three routing kernels                         */
+#define MOE_EV_DISPATCH_END 2  /* after the row scatter                                   */
+#define MOE_EV_FFN_BEGIN 3
+#define MOE_EV_GATHER_END 4    /* RANK_MAJOR / FLAT: after gathering the picks' rows       */
+#define MOE_EV_GEMM1_END 5     /* after GEMM1 + SwiGLU                                    */
+#define MOE_EV_GEMM2_END 6     /* after GEMM2                                             */
+#define MOE_EV_FFN_END 7       /* after the RANK_MAJOR / FLAT local-pick reduction        */
+#define MOE_EV_COMBINE_BEGIN 8
+#define MOE_EV_COMBINE_END 9
+#define MOE_EV_COUNT 10
+
+#define MOE_MAX_TOPK 32
+#define MOE_MAX_WORLD 64
+#define MOE_MAX_EXPERTS 2048
+#define MOE_MAX_HIDDEN 65536
+
+/* EP geometry, the analogue of FleetParams [FI-3 table; section 1] plus the FFN size. */
+typedef struct {
+    int32_t world;        /* W: logical ranks                                              */
+    int32_t max_tok;      /* Tr: num_max_dispatch_tokens_per_rank [MC-EP]                  */
+    int32_t num_tokens;   /* T <= W*Tr; token t belongs to logical rank t / Tr             */
+    int32_t hidden;       /* H, multiple of 128                                            */
+    int32_t num_experts;  /* E, multiple of W; expert e lives on rank e / (E/W)            */
+    int32_t top_k;        /* k                                                             */
+    int32_t intermediate; /* I: SwiGLU FFN width, multiple of 128                          */
+    int32_t layout;       /* moe_layout                                                    */
+    int32_t algorithm;    /* moe_algorithm                                                 */
+} moe_geom;
+
+/*
+ * Dispatch handle: the analogue of Mooncake's (packed_recv_src_info,
+ * packed_recv_layout_range, max_tok, hidden, num_experts) tuple [MC-EP].  moe_dispatch
+ * fills it with device pointers into the caller's workspace; it stays valid until the
+ * workspace is reused by another moe_dispatch, and must only be passed to the
+ * moe_expert_ffn / moe_combine of the same dispatch ([MC-EP]: a handle is never reused
+ * across unrelated dispatch/combine pairs).  cap = W*Tr below; R = offsets[E].
+ */
+typedef struct {
+    moe_geom geom;
+    void *recv_x;              /* bf16. EM: [E, cap, H]; RM: [W(dst), W(src)*Tr, H];
+                                  FLAT: [W(dst), cap, H].  Rows past the counts are
+                                  unspecified and never read.                            */
+    int32_t *counts;           /* [E] rows of expert e (packed_recv_count)               */
+    int32_t *offsets;          /* [E+1] exclusive prefix of counts: the expert-grouped
+                                  pick list of the FFN                                   */
+    int32_t *pick_pos;         /* [T*k] position of pick (t,j) in the pick list, or -1   */
+    int32_t *pick_src;         /* [T*k] first R entries: t*k+j of each pick-list entry
+                                  (packed_recv_src_info, in compact form)               */
+    int32_t *slot;             /* EM: [T*k] recv row e*cap + rank of pick in expert e,
+                                  or -1.  Unused (untouched) for RM/FLAT.                */
+    int32_t *layout_range;     /* EM: [E][W][2] (begin, count) of each source rank's rows
+                                  inside expert e's region (packed_recv_layout_range)    */
+    int32_t *recv_row;         /* RM/FLAT: [T][W] row of token t in destination d's
+                                  region, or -1 if t has no pick on d                    */
+    int32_t *recv_count;       /* RM/FLAT: [W(dst)][W(src)] tokens received per pair     */
+    int32_t *num_recv;         /* RM/FLAT: [W] tokens received per destination           */
+    int32_t *recv_src;         /* RM/FLAT: [W][cap] token of each received row           */
+    int32_t *recv_topk_idx;    /* RM/FLAT: [W][cap][k] LOCAL expert id, -1 = non-local
+                                  pick [FI-3], int32                                     */
+    float *recv_topk_weights;  /* RM/FLAT: [W][cap][k] topk weight, 0 for non-local      */
+    int32_t *status;           /* device status word (MOE_STATUS_* bits)                 */
+    void *workspace;           /* base of the workspace the handle lives in              */
+    size_t workspace_bytes;
+    /* Optional per-kernel timing, the analogue of FlashInfer's enable_timing stage events
+       (section 2): when `events` is non-NULL, every call records the cudaEvent_t
+       events[slot] (slots MOE_EV_*, slot < num_events, NULL entries skipped) on its stream
+       between its kernels.  Caller-owned events; moe_dispatch keeps these two fields of the
+       handle it is given and fills the rest. */
+    void **events;
+    int32_t num_events;
+    uint64_t magic;            /* set by moe_dispatch                                    */
+} moe_handle;
+
+/*
+ * moe_workspace_size - bytes of device workspace one dispatch/ffn/combine cycle needs
+ * for geometry *g: receive buffer, routing metadata, FFN intermediates and scratch.
+ * The analogue of Buffer.get_ep_buffer_size_hint [MC-EP]: size it for the peak
+ * num_tokens (max_tok per rank), not the mean.  Writes the size to *bytes.
+ * Errors: the geometry checks listed under moe_error.
+ */
+int moe_workspace_size(const moe_geom *g, size_t *bytes);
+
+/*
+ * moe_expert_out_size - bytes of the float32 expert_out buffer moe_expert_ffn writes:
+ * EM [E, cap, H]; RM/FLAT [W, cap, H] (the receive layout, float32).
+ */
+int moe_expert_out_size(const moe_geom *g, size_t *bytes);
+
+/*
+ * moe_dispatch - route and scatter one token batch [MC-EP Buffer.dispatch; FI-3].
+ *   x_dev           bf16 [T, H], 16-byte aligned, row-major contiguous
+ *   topk_ids_dev    [T, k] int32 or int64 (ids_dtype), global expert ids, -1 = masked
+ *                   pick [MC-EP]; an id outside [-1, E) sets MOE_STATUS_BAD_EXPERT_ID
+ *                   and that pick is dropped
+ *   topk_weights_dev float32 [T, k]: copied into recv_topk_weights for RM/FLAT (the
+ *                   received routing); unused for EM (may be NULL there)
+ *   workspace_dev   >= moe_workspace_size bytes, 256-byte aligned; overwritten
+ *   h               host struct filled on success
+ * Computes (deterministically; atomics decide no position): per-expert counts and
+ * offsets, the position of every pick in its expert's rows in ascending (token, pick)
+ * order, the EM slots and layout ranges or the RM/FLAT per-destination rows, local
+ * ids and weights, then copies each token row to every place it is received.
+ */
+int moe_dispatch(const moe_geom *g, const void *x_dev, const void *topk_ids_dev,
+                 int ids_dtype, const float *topk_weights_dev, void *workspace_dev,
+                 size_t workspace_bytes, moe_handle *h, void *stream);
+
+/*
+ * moe_prepare_weights - one-time re-layout of w1 [E, 2I, H] (gate rows [0, I), up rows
+ * [I, 2I) per expert [FI-4]) into w1_prepared_dev of the same size: inside each expert,
+ * blocks of 128 gate rows and the matching 128 up rows alternate, so one 256-column GEMM
+ * tile holds both halves of the SwiGLU for 128 output columns.  Both bf16, 16-byte
+ * aligned, distinct buffers.
+ */
+int moe_prepare_weights(const moe_geom *g, const void *w1_dev, void *w1_prepared_dev,
+                        void *stream);
+
+/*
+ * moe_expert_ffn - per-expert grouped SwiGLU FFN on the received rows [FI-2; FI-3]:
+ * for each expert e and each of its rows x: h = x W1[e]^T (fp32 accumulate),
+ * act = bf16(silu(h[:I]) * h[I:]), y = act W2[e]^T (fp32).
+ *   EM:      expert_out[e*cap + r] = y of row r (top_k = 1 per dispatched row)
+ *   RM/FLAT: expert_out[d*cap + r] = sum over the row's LOCAL picks j (ascending) of
+ *            recv_topk_weights[d][r][j] * y_j; non-local picks are masked to weight 0
+ *   w1_prepared_dev bf16 from moe_prepare_weights; w2_dev bf16 [E, H, I]
+ *   expert_out_dev  float32, moe_expert_out_size bytes, 16-byte aligned
+ * Runs on tcgen05 tensor cores (bf16 x bf16 -> fp32 in tensor memory).
+ */
+int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void *w2_dev,
+                   float *expert_out_dev, void *stream);
+
+/*
+ * moe_combine - return expert outputs to token order [MC-EP Buffer.combine; FI-3]:
+ *   EM:      out[t] = bf16( sum over kept picks j ascending of
+ *                           topk_weights[t, j] * expert_out[slot[t, j]] )
+ *   RM/FLAT: out[t] = bf16( sum over destinations d ascending that received t of
+ *                           expert_out[d*cap + recv_row[t, d]] )   (unweighted)
+ *   topk_weights_dev float32 [T, k] (EM; ignored and may be NULL for RM/FLAT)
+ *   out_dev          bf16 [T, H], 16-byte aligned
+ * fp32 accumulation, one round-to-nearest-even to bf16.  Tokens without any kept
+ * pick get zeros.
+ */
+int moe_combine(const moe_handle *h, const float *expert_out_dev,
+                const float *topk_weights_dev, void *out_dev, void *stream);
+
+/*
+ * moe_forward_host - the whole layer end to end from HOST buffers, on one stream:
+ * copy x_host / topk_ids_host / topk_weights_host into the caller's device buffers
+ * (x_dev, topk_ids_dev, topk_weights_dev, same shapes as in moe_dispatch), then
+ * moe_dispatch -> moe_expert_ffn -> moe_combine into out_dev, then copy out_dev to
+ * out_host (bf16 [T, H]).  Asynchronous like the other calls: out_host is valid once the
+ * stream has been synchronised.  Host buffers should be page-locked for the copies to
+ * overlap; pageable memory works but the copies then synchronise.  Returns the first
+ * error of the sequence.
+ */
+int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids_host,
+                     int ids_dtype, const float *topk_weights_host, void *out_host,
+                     void *x_dev, void *topk_ids_dev, float *topk_weights_dev, void *out_dev,
+                     const void *w1_prepared_dev, const void *w2_dev, float *expert_out_dev,
+                     void *workspace_dev, size_t workspace_bytes, moe_handle *h, void *stream);
+
+/*
+ * moe_get_status - wait for `stream`, then read the handle's device status word
+ * (MOE_STATUS_* bits, 0 = clean) into *status_host.  The only synchronising call.
+ */
+int moe_get_status(const moe_handle *h, int32_t *status_host, void *stream);
+
+/* moe_strerror - static text for a moe_error code. */
+const char *moe_strerror(int err);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* COMBINE_TOPK_IDS_MOE_H */

@@ -1,0 +1,113 @@
+"""Shared checks of the GPU layer against the CPU oracle (used by the -m gpu tests)."""
+import numpy as np
+import torch
+
+import combine_topk_ids_gb300 as moe
+import oracle
+
+# spec tolerance on floating outputs: |d| <= 2e-2 * |ref| + 1e-3, elementwise
+RTOL, ATOL = 2e-2, 1e-3
+
+
+def assert_close(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    bad = ~(np.abs(got - ref) <= RTOL * np.abs(ref) + ATOL)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError("%s: %d/%d elements outside tolerance; first at %s: got %r ref %r"
+                             % (what, bad.sum(), bad.size, tuple(i), got[tuple(i)], ref[tuple(i)]))
+
+
+def bf16_tensor_to_f64(t):
+    return oracle.bf16_bits_to_f64(t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
+
+
+def geom_dict(cfg):
+    return oracle.geom_of(cfg)
+
+
+def run_layer(case, layer=None):
+    cfg = case.cfg
+    if layer is None:
+        layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I,
+                                 cfg.layout, cfg.algo)
+        layer.set_weights(case.w1, case.w2)
+    layer.forward(case.x, case.ids, case.w)
+    torch.cuda.synchronize()
+    return layer
+
+
+def check_routing(layer, rt, cfg):
+    """Bit-exact comparison of every routing output the handle exposes."""
+    T, k, E, W, cap = cfg.tokens, cfg.k, cfg.E, cfg.W, cfg.W * cfg.Tr
+    v = lambda f, shape, dt=torch.int32: layer.view(f, shape, dt).cpu().numpy()  # noqa: E731
+    np.testing.assert_array_equal(v("counts", (E,)), rt["counts"])
+    np.testing.assert_array_equal(v("offsets", (E + 1,)), rt["offsets"])
+    np.testing.assert_array_equal(v("pick_pos", (T, k)), rt["pick_pos"])
+    R = rt["R"]
+    np.testing.assert_array_equal(v("pick_src", (T * k,))[:R], rt["pick_src"])
+    if cfg.layout == "EM":
+        np.testing.assert_array_equal(v("slot", (T, k)), rt["slot"])
+        np.testing.assert_array_equal(v("layout_range", (E, W, 2)), rt["layout_range"])
+    else:
+        np.testing.assert_array_equal(v("recv_row", (T, W)), rt["recv_row"])
+        np.testing.assert_array_equal(v("recv_count", (W, W)), rt["recv_count"])
+        np.testing.assert_array_equal(v("num_recv", (W,)), rt["num_recv"])
+        used = rt["recv_src"] >= 0             # rows that hold a token
+        np.testing.assert_array_equal(v("recv_src", (W, cap))[used], rt["recv_src"][used])
+        np.testing.assert_array_equal(v("recv_topk_idx", (W, cap, k))[used], rt["recv_topk_idx"][used])
+        np.testing.assert_array_equal(v("recv_topk_weights", (W, cap, k), torch.float32)[used],
+                                      rt["recv_topk_w"][used])
+
+
+def check_dispatch_rows(layer, rt, case):
+    """Every received row equals its token's x row, bit for bit (checked on the device)."""
+    cfg = case.cfg
+    rows, toks = oracle.dispatch_rows(geom_dict(cfg), rt)
+    nrows = (cfg.E if cfg.layout == "EM" else cfg.W) * cfg.W * cfg.Tr
+    recv = layer.view("recv_x", (nrows, cfg.H), torch.int16)
+    x = case.x.view(torch.int16)
+    dev = case.x.device
+    r_t = torch.from_numpy(np.asarray(rows, np.int64)).to(dev)
+    t_t = torch.from_numpy(np.asarray(toks, np.int64)).to(dev)
+    for s in range(0, len(rows), 1 << 16):
+        assert torch.equal(recv[r_t[s:s + (1 << 16)]], x[t_t[s:s + (1 << 16)]]), "dispatch rows differ"
+
+
+def check_expert_out(layer, rt, case, picks_or_rows=None, max_rows=None):
+    """expert_out against the oracle: per pick (EM) or per received row (RM/FLAT)."""
+    cfg = case.cfg
+    g = geom_dict(cfg)
+    k, H, cap = cfg.k, cfg.H, cfg.W * cfg.Tr
+    eo = layer.expert_out.view(-1, H)
+    if cfg.layout == "EM":
+        picks = np.nonzero(rt["pick_pos"].reshape(-1) >= 0)[0] if picks_or_rows is None else picks_or_rows
+        if max_rows is not None:
+            picks = picks[:max_rows]
+        ys = oracle.pick_outputs(g, rt, case.x_bits, case.w1_host, case.w2_host, picks=picks)
+        slots = rt["slot"].reshape(-1)[picks]
+        got = eo[torch.from_numpy(slots).to(eo.device)].cpu().numpy()
+        assert_close(got, np.array([ys[i] for i in picks]), "expert_out (EM)")
+    else:
+        rows = picks_or_rows
+        if rows is None:
+            rows = [(d, r) for d in range(cfg.W) for r in range(cap) if rt["recv_src"][d, r] >= 0]
+        if max_rows is not None:
+            rows = rows[:max_rows]
+        need = sorted({int(rt["recv_src"][d, r]) * k + j for d, r in rows for j in range(k)
+                       if rt["recv_topk_idx"][d, r, j] >= 0})
+        ys = oracle.pick_outputs(g, rt, case.x_bits, case.w1_host, case.w2_host, picks=need)
+        ref = oracle.ffn_ranks(g, rt, case.w_np, ys.__getitem__, rows)
+        idx = torch.tensor([d * cap + r for d, r in rows], dtype=torch.int64, device=eo.device)
+        assert_close(eo[idx].cpu().numpy(), ref, "expert_out (%s)" % cfg.layout)
+
+
+def check_out(layer, case, tokens=None):
+    cfg = case.cfg
+    _, ref = oracle.layer(geom_dict(cfg), case.x_bits, case.ids_np, case.w_np, case.w1_host,
+                          case.w2_host, tokens=tokens)
+    got = bf16_tensor_to_f64(layer.out if tokens is None else layer.out[torch.as_tensor(tokens)])
+    assert_close(got, ref, "out (%s)" % cfg.name)
+    return ref

@@ -1,0 +1,97 @@
+"""The C-ABI library builds, loads and exports every declared entry point; host-side
+validation returns the documented error codes.  CPU only: no call here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import combine_topk_ids_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(moe.LIB_PATH):
+        moe.build()
+    return moe.lib()
+
+
+def _declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for f in ("moe_workspace_size", "moe_expert_out_size", "moe_dispatch", "moe_prepare_weights",
+              "moe_expert_ffn", "moe_combine", "moe_get_status", "moe_strerror"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for f in _declared_functions():
+        assert hasattr(lib, f), f
+
+
+def _geom(**kw):
+    base = dict(W=2, Tr=32, T=64, H=256, E=8, k=2, I=512, layout="EM", algo="LL")
+    base.update(kw)
+    return moe.make_geom(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(E=7), -2),                 # num_experts % world
+    (dict(H=200), -3),               # hidden % 128
+    (dict(I=100), -4),               # intermediate % 128
+    (dict(T=65), -5),                # num_tokens > world * max_tok
+    (dict(k=0), -6), (dict(k=33), -6),
+    (dict(W=0), -1), (dict(layout=3), -1), (dict(algo=2), -1),
+    (dict(W=128, E=128, Tr=1, T=1), -13),
+])
+def test_geometry_errors(lib, kw, code):
+    g = _geom(**kw)
+    n = ctypes.c_size_t()
+    assert lib.moe_workspace_size(ctypes.byref(g), ctypes.byref(n)) == code
+    assert moe.strerror(code) != "unknown error"
+
+
+def test_workspace_size_grows_with_capacity(lib):
+    a = moe.moe_workspace_size(_geom())
+    b = moe.moe_workspace_size(_geom(Tr=64))
+    assert 0 < a < b and a % 256 == 0
+    # EXPERT_MAJOR receive buffer alone: E * W*Tr * H bf16
+    assert a >= 8 * 64 * 256 * 2
+    assert moe.moe_expert_out_size(_geom()) == 8 * 64 * 256 * 4
+    assert moe.moe_expert_out_size(_geom(layout="RM")) == 2 * 64 * 256 * 4
+
+
+def test_dispatch_host_errors_before_any_launch(lib):
+    g = _geom()
+    h = moe.MoeHandle()
+    ws = ctypes.c_void_p(1 << 20)   # never dereferenced: every case fails validation first
+    x = ctypes.c_void_p(1 << 21)
+    call = lambda **kw: lib.moe_dispatch(  # noqa: E731
+        ctypes.byref(kw.get("g", g)), kw.get("x", x), kw.get("ids", x), kw.get("dt", 1), None,
+        kw.get("ws", ws), kw.get("wsb", 1 << 40), ctypes.byref(h), None)
+    assert call(dt=5) == -7
+    assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == -9
+    assert call(x=ctypes.c_void_p((1 << 21) + 2)) == -9
+    assert call(wsb=16) == -8
+    assert call(g=_geom(layout="RM")) == -1      # RM/FLAT need topk_weights
+    assert h.magic == 0
+
+
+def test_calls_reject_an_unfilled_handle(lib):
+    h = moe.MoeHandle()
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.moe_expert_ffn(ctypes.byref(h), p, p, p, None) == -10
+    assert lib.moe_combine(ctypes.byref(h), p, p, p, None) == -10
+    v = ctypes.c_int32()
+    assert lib.moe_get_status(ctypes.byref(h), ctypes.byref(v), None) == -10

@@ -1,0 +1,51 @@
+"""The five workloads at full size, in the launch configuration bench.py times:
+routing and every permuted row bit-exact against the oracle, expert_out and the combined
+output on sampled rows / tokens that the oracle evaluates one by one."""
+import numpy as np
+import pytest
+import torch
+
+import combine_topk_ids_gb300 as moe
+import gen
+import oracle
+from gen.device import make_case
+from parity_util import check_dispatch_rows, check_expert_out, check_out, check_routing, geom_dict, run_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.build()
+
+
+def _sample(n_total, n, seed):
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(n_total, size=min(n, n_total), replace=False).tolist())
+    pick |= {0, n_total - 1}
+    return np.array(sorted(pick))
+
+
+@pytest.mark.parametrize("name", list(gen.CONFIGS))
+def test_full_size(name):
+    cfg = gen.CONFIGS[name]
+    case = make_case(cfg, "cuda")
+    layer = run_layer(case)
+    assert layer.status() == 0
+    g = geom_dict(cfg)
+    rt = oracle.route(g, case.ids_np, case.w_np)
+    check_routing(layer, rt, cfg)
+    check_dispatch_rows(layer, rt, case)
+    ntok = 64 if cfg.E * cfg.H * cfg.I <= (1 << 30) else 6
+    toks = _sample(cfg.tokens, ntok, 1)
+    if cfg.layout == "EM":
+        picks = np.array([t * cfg.k + j for t in toks for j in range(cfg.k) if rt["pick_pos"][t, j] >= 0])
+        check_expert_out(layer, rt, case, picks_or_rows=picks)
+    else:
+        rows = [(d, int(rt["recv_row"][t, d])) for t in toks for d in range(cfg.W) if rt["recv_row"][t, d] >= 0]
+        check_expert_out(layer, rt, case, picks_or_rows=rows)
+    check_out(layer, case, tokens=toks)
+    del layer, case
+    torch.cuda.empty_cache()

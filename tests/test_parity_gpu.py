@@ -1,0 +1,163 @@
+"""GPU layer vs the CPU oracle through the C ABI: routing and permuted rows bit-exact,
+expert_out and the combined output within |d| <= 2e-2*|ref| + 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import combine_topk_ids_gb300 as moe
+import gen
+import oracle
+from gen.device import make_case
+from parity_util import (assert_close, bf16_tensor_to_f64, check_dispatch_rows, check_expert_out,
+                         check_out, check_routing, geom_dict, run_layer)
+
+pytestmark = pytest.mark.gpu
+
+SMALL_CASES = {
+    "tiny_ll_em": gen.CONFIGS["tiny_ll_em"],
+    "small_em": gen.SMALL["small_em"],
+    "small_rm": gen.SMALL["small_rm"],
+    "small_flat": gen.SMALL["small_flat"],
+    "small_em_masked_i32": gen.SMALL["small_em"].with_(mask_frac=0.3, ids_dtype="int32", seed=3),
+    "small_rm_masked": gen.SMALL["small_rm"].with_(mask_frac=0.3, seed=4),
+    "small_flat_i32": gen.SMALL["small_flat"].with_(ids_dtype="int32", seed=5),
+    "small_em_h384": gen.SMALL["small_em"].with_(H=384, seed=6),          # 128-wide GEMM2 tiles
+    "small_flat_w1": gen.SMALL["small_flat"].with_(W=1, Tr=350, seed=7),  # one logical rank
+    "small_rm_w8": gen.SMALL["small_rm"].with_(W=8, Tr=48, T=380, E=16, seed=8),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.build()
+
+
+@pytest.mark.parametrize("name", list(SMALL_CASES))
+def test_layer_parity_small(name):
+    cfg = SMALL_CASES[name]
+    case = make_case(cfg, "cuda")
+    layer = run_layer(case)
+    assert layer.status() == 0
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    check_routing(layer, rt, cfg)
+    check_dispatch_rows(layer, rt, case)
+    check_expert_out(layer, rt, case)
+    check_out(layer, case)
+
+
+@pytest.mark.parametrize("name", ["small_em", "small_rm", "small_flat"])
+def test_deterministic(name):
+    cfg = SMALL_CASES[name]
+    case = make_case(cfg, "cuda")
+    layer = run_layer(case)
+    out1, eo1 = layer.out.clone(), layer.expert_out.clone()
+    run_layer(case, layer)
+    assert torch.equal(layer.out.view(torch.int16), out1.view(torch.int16))
+    # expert_out rows that hold data (padding rows are unspecified)
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    H, cap = cfg.H, cfg.W * cfg.Tr
+    if cfg.layout == "EM":
+        rows = rt["slot"].reshape(-1)
+        rows = rows[rows >= 0]
+    else:
+        d, r = np.nonzero(rt["recv_src"] >= 0)
+        rows = d * cap + r
+    idx = torch.from_numpy(np.asarray(rows, np.int64)).cuda()
+    assert torch.equal(layer.expert_out.view(-1, H)[idx], eo1.view(-1, H)[idx])
+
+
+@pytest.mark.parametrize("layout", ["EM", "RM", "FLAT"])
+def test_combine_alone_on_seeded_expert_out(layout):
+    """combine on an expert_out drawn by the generator (not produced by the GPU path)."""
+    cfg = SMALL_CASES["small_" + layout.lower()].with_(seed=11)
+    case = make_case(cfg, "cuda")
+    layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout, cfg.algo)
+    layer.dispatch(case.x, case.ids, case.w)
+    rng = np.random.default_rng(123)
+    eo_np = rng.standard_normal(layer.expert_out.numel()).astype(np.float32)
+    layer.expert_out.copy_(torch.from_numpy(eo_np))
+    out = torch.empty((cfg.tokens, cfg.H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_combine(layer.handle, layer.expert_out, case.w, out)
+    torch.cuda.synchronize()
+    g = geom_dict(cfg)
+    rt = oracle.route(g, case.ids_np, case.w_np)
+    eo = eo_np.reshape(-1, cfg.H).astype(np.float64)
+    cap = cfg.W * cfg.Tr
+    toks = np.arange(cfg.tokens)
+    if layout == "EM":
+        ref = oracle.combine_em(g, rt, case.w_np, lambda i: eo[rt["slot"].reshape(-1)[i]], toks)
+    else:
+        ref = oracle.combine_ranks(g, rt, lambda d, r: eo[d * cap + r], toks)
+    got = bf16_tensor_to_f64(out)
+    # fp32 sum vs float64 sum, both rounded once to bf16: at most one bf16 step apart
+    np.testing.assert_allclose(got, ref, rtol=2 ** -7, atol=1e-30)
+
+
+def test_identity_expert_via_recv_buffer():
+    """expert_out := fp32(recv): EM combine equals bf16(x * sum of kept weights)."""
+    cfg = SMALL_CASES["small_em"].with_(mask_frac=0.2, seed=12)
+    case = make_case(cfg, "cuda")
+    layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout, cfg.algo)
+    layer.dispatch(case.x, case.ids, case.w)
+    nrows = cfg.E * cfg.W * cfg.Tr
+    recv = layer.view("recv_x", (nrows, cfg.H), torch.bfloat16)
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    rows = torch.from_numpy(np.asarray(oracle.dispatch_rows(geom_dict(cfg), rt)[0], np.int64)).cuda()
+    eo = layer.expert_out.view(nrows, cfg.H)
+    eo[rows] = recv[rows].float()
+    layer.combine(case.w)
+    torch.cuda.synchronize()
+    ws = np.where(case.ids_np >= 0, case.w_np.astype(np.float64), 0.0).sum(axis=1)
+    ref = oracle.round_bf16(oracle.bf16_bits_to_f64(case.x_bits) * ws[:, None])
+    np.testing.assert_allclose(bf16_tensor_to_f64(layer.out), ref, rtol=2 ** -7, atol=1e-30)
+
+
+# ----------------------------------------------------------------------- edge cases
+def test_empty_batch():
+    cfg = SMALL_CASES["small_rm"].with_(T=0)
+    case = make_case(cfg, "cuda")
+    layer = run_layer(case)
+    assert layer.status() == 0
+    assert layer.view("counts", (cfg.E,), torch.int32).sum().item() == 0
+    assert layer.out.numel() == 0
+
+
+@pytest.mark.parametrize("layout", ["EM", "FLAT"])
+def test_all_picks_masked(layout):
+    cfg = SMALL_CASES["small_" + layout.lower()]
+    ids = np.full((cfg.tokens, cfg.k), -1, np.int64)
+    case = make_case(cfg, "cuda", ids_override=ids)
+    layer = run_layer(case)
+    assert layer.status() == 0
+    assert torch.count_nonzero(layer.out.float()).item() == 0
+
+
+def test_bad_ids_are_flagged_and_dropped():
+    cfg = SMALL_CASES["small_rm"].with_(seed=13)
+    ids, _ = gen.gen_routing(cfg)
+    ids[5, 1] = cfg.E + 3
+    ids[17, 0] = -7
+    case = make_case(cfg, "cuda", ids_override=ids)
+    layer = run_layer(case)
+    assert layer.status() == moe.STATUS_BAD_EXPERT_ID
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    assert rt["n_bad"] == 2
+    check_routing(layer, rt, cfg)
+    check_out(layer, case)
+
+
+def test_expert_major_region_overflow():
+    """A token naming one expert twice can overflow the W*Tr-row EM region: the extra picks
+    are dropped and flagged, the rest matches the oracle."""
+    cfg = gen.MoeConfig("ovf", W=1, Tr=6, H=256, E=2, k=3, I=128, layout="EM", algo="LL",
+                        routing="uniform")
+    ids = np.array([[0, 0, 1], [0, 1, 0], [1, 1, 1], [0, 0, 0], [1, 0, -1], [0, 1, 1]])
+    case = make_case(cfg, "cuda", ids_override=ids)
+    layer = run_layer(case)
+    assert layer.status() == moe.STATUS_EM_OVERFLOW
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    assert rt["n_over"] > 0
+    check_routing(layer, rt, cfg)
+    check_out(layer, case)
