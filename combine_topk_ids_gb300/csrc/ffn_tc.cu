@@ -4,12 +4,16 @@
 // per-expert grouped GEMM with no routing; section 4 step 1: w1 [E, 2I, H], w2 [E, H, I]):
 // for every expert e and each of its n_e rows x,
 //     GEMM1   h   = x W1[e]^T            [n_e, 2I], fp32 accumulate in tensor memory
-//     SwiGLU  act = bf16(silu(h[:, :I]) * h[:, I:])      (fused into GEMM1's epilogue)
-//     GEMM2   y   = act W2[e]^T          [n_e, H],  fp32, written as fp32
+//     SwiGLU  act = silu(h[:, :I]) * h[:, I:]   fp32 (fused into GEMM1's epilogue), stored
+//                   as a pair of bf16 arrays act_hi = bf16(act), act_lo = bf16(act - act_hi)
+//     GEMM2   y   = act_hi W2[e]^T + act_lo W2[e]^T   [n_e, H], one fp32 accumulator
+// The pair carries act to about 16 significant bits, so GEMM2 sees the fp32 activation
+// rather than a bf16 re-quantisation of it.  (A single bf16 act is a rounding decision
+// taken on tensor-core-accumulated values; its flips move y by up to |W2| * ulp(act).)
 //
 // One persistent kernel per GEMM, one CTA per SM, 256 threads:
-//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage (SWIZZLE_128B),
-//               a 4-stage mbarrier ring
+//   warp 0      TMA producer: 128x64 A tile(s) + 256x64 B tile per stage (SWIZZLE_128B),
+//               a 4-stage (GEMM1) or 3-stage (GEMM2: A_hi, A_lo, B) mbarrier ring
 //   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16, M=128,
 //               N=256, K=16, bf16 x bf16 -> fp32 into one of two 256-column TMEM
 //               accumulators, tcgen05.commit frees smem stages and hands tiles over
@@ -32,13 +36,17 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;   // BN: widest n-tile (GEMM2 may use 128)
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int THREADS = 256;
 constexpr int TMEM_COLS = 2 * BN;               // two fp32 accumulators of 128 x 256
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+// Pipeline shape: HILO = the A operand is a bf16 pair (two A tiles per stage).
+template <bool HILO> struct Pipe {
+    static constexpr int kATiles = HILO ? 2 : 1;
+    static constexpr int kStageBytes = kATiles * A_BYTES + B_BYTES;   // 48 or 64 KB
+    static constexpr int kStages = HILO ? 3 : 4;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+};
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A bf16
@@ -58,8 +66,9 @@ struct FfnArgs {
     int a_mode;    // 0: A row = e*a_cap + m; 1: A row = offsets[e] + m
     int64_t a_cap;
     int64_t b_rows;   // rows of B per expert (N)
-    int mode;      // 0: SwiGLU epilogue -> bf16 act; 1: fp32 store
-    void *out;
+    int mode;      // 0: SwiGLU epilogue -> act as a bf16 (hi, lo) pair; 1: fp32 store
+    void *out;     // mode 0: act_hi; mode 1: fp32 rows
+    void *out2;    // mode 0: act_lo
     int64_t out_ld;   // elements per output row
     int out_mode;  // 0: row = e*out_cap + m; 1: row = offsets[e] + m
     int64_t out_cap;
@@ -208,15 +217,18 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return g / (1.0f + __expf(-g)) * u;
 }
 
+template <bool HILO>
 __global__ void __launch_bounds__(THREADS, 1)
-    ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    FfnArgs a) {
+    ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                    const __grid_constant__ CUtensorMap tmB, FfnArgs a) {
+    using P = Pipe<HILO>;
+    constexpr int STAGES = P::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint8_t *sA = smem;                                   // [STAGES][kATiles] A tiles
+    uint8_t *sB = smem + STAGES * P::kATiles * A_BYTES;   // [STAGES] B tiles
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * P::kStageBytes);
     // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -237,6 +249,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        if (HILO)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA2)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
     }
     if (warp == 2) {
@@ -263,12 +277,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int64_t arow = (a.a_mode == 0 ? (int64_t)e * a.a_cap : (int64_t)__ldg(a.offsets + e)) +
                                  (int64_t)mb * BM;
             const int64_t brow = (int64_t)e * a.b_rows + (int64_t)nbk * a.bn;
-            const uint32_t tx = (uint32_t)(A_BYTES + a.bn * BK * 2);
+            const uint32_t tx = (uint32_t)(P::kATiles * A_BYTES + a.bn * BK * 2);
             for (int kb = 0; kb < a.kb; ++kb) {
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, a.status)) { ok = false; break; }
                 const uint32_t fb = full0 + 8 * stage;
                 mbar_expect_tx(fb, tx);
-                tma_load_2d(smem_u32(sA + stage * A_BYTES), &tmA, kb * BK, (int)arow, fb);
+                uint8_t *sa = sA + stage * P::kATiles * A_BYTES;
+                tma_load_2d(smem_u32(sa), &tmA, kb * BK, (int)arow, fb);
+                if (HILO) tma_load_2d(smem_u32(sa + A_BYTES), &tmA2, kb * BK, (int)arow, fb);
                 tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmB, kb * BK, (int)brow, fb);
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
@@ -288,12 +304,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int kb = 0; kb < a.kb; ++kb) {
                 if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
+                const uint32_t a0 = smem_u32(sA + stage * P::kATiles * A_BYTES);
                 const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
-                             (kb | kk) != 0 ? 1u : 0u);
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t bd = sw128_desc(b0 + kk * 32);
+                    mma_bf16(d_tmem, sw128_desc(a0 + kk * 32), bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    if (HILO) mma_bf16(d_tmem, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc, 1u);
+                }
                 mma_commit(empty0 + 8 * stage);   // stage reusable once these MMAs finish
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
@@ -318,8 +336,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
             if (a.mode == 0) {
                 // columns [0,128) gate, [128,256) up of act columns nbk*128 .. +128
-                __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) + orow * a.out_ld +
-                                     (int64_t)nbk * (BN / 2);
+                const int64_t o0 = orow * a.out_ld + (int64_t)nbk * (BN / 2);
+                __nv_bfloat16 *out_hi = reinterpret_cast<__nv_bfloat16 *>(a.out) + o0;
+                __nv_bfloat16 *out_lo = reinterpret_cast<__nv_bfloat16 *>(a.out2) + o0;
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
                     uint32_t g[32], u[32];
@@ -327,19 +346,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld32(tbase + BN / 2 + c, u);
                     tmem_wait_ld();
                     if (row < valid) {
-                        uint4 *o = reinterpret_cast<uint4 *>(out + c);
+                        uint4 *oh = reinterpret_cast<uint4 *>(out_hi + c);
+                        uint4 *ol = reinterpret_cast<uint4 *>(out_lo + c);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
-                            uint32_t w[4];
+                            uint32_t wh[4], wl[4];
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
                                 const int i = v * 8 + h * 2;
-                                __nv_bfloat162 p = __floats2bfloat162_rn(
-                                    silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i])),
-                                    silu_mul(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1])));
-                                w[h] = *reinterpret_cast<uint32_t *>(&p);
+                                const float a0 = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]));
+                                const float a1 = silu_mul(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1]));
+                                __nv_bfloat162 hi = __floats2bfloat162_rn(a0, a1);
+                                __nv_bfloat162 lo = __floats2bfloat162_rn(a0 - __low2float(hi),
+                                                                          a1 - __high2float(hi));
+                                wh[h] = *reinterpret_cast<uint32_t *>(&hi);
+                                wl[h] = *reinterpret_cast<uint32_t *>(&lo);
                             }
-                            o[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                            oh[v] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                            ol[v] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                         }
                     }
                 }
@@ -414,19 +438,21 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int launch_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const FfnArgs &args, int64_t max_tiles,
-                cudaStream_t s) {
+template <bool HILO>
+int launch_gemm(const CUtensorMap &ma, const CUtensorMap &ma2, const CUtensorMap &mb,
+                const FfnArgs &args, int64_t max_tiles, cudaStream_t s) {
     if (max_tiles <= 0) return MOE_OK;
+    constexpr int smem = Pipe<HILO>::kSmemBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(ffn_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        SMEM_BYTES);
+        attr_err = cudaFuncSetAttribute(ffn_gemm_kernel<HILO>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
     int grid = num_sms();
     if ((int64_t)grid > max_tiles) grid = (int)max_tiles;
-    ffn_gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, args);
+    ffn_gemm_kernel<HILO><<<grid, THREADS, smem, s>>>(ma, ma2, mb, args);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -457,8 +483,8 @@ int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s) {
     FfnArgs g = base_args(r);
     g.bn = BN; g.nb = (int)(2 * p.I / BN); g.kb = (int)(p.H / BK);
     g.a_mode = em ? 0 : 1; g.a_cap = p.cap; g.b_rows = 2 * p.I;
-    g.mode = 0; g.out = r.act; g.out_ld = p.I; g.out_mode = 1; g.out_cap = 0;
-    return launch_gemm(mA, mB, g, max_mblocks(p) * g.nb, s);
+    g.mode = 0; g.out = r.act; g.out2 = r.act_lo; g.out_ld = p.I; g.out_mode = 1; g.out_cap = 0;
+    return launch_gemm<false>(mA, mA, mB, g, max_mblocks(p) * g.nb, s);
 }
 
 int launch_gemm2(const Routing &r, const uint16_t *w2, float *expert_out, cudaStream_t s) {
@@ -466,15 +492,16 @@ int launch_gemm2(const Routing &r, const uint16_t *w2, float *expert_out, cudaSt
     if (p.P == 0) return MOE_OK;
     const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
     const int bn = (p.H % 256 == 0) ? 256 : 128;
-    CUtensorMap mA, mB;
-    if (!make_map(&mA, r.act, p.P, p.I, BM) || !make_map(&mB, w2, p.E * p.H, p.I, bn))
+    CUtensorMap mA, mA2, mB;
+    if (!make_map(&mA, r.act, p.P, p.I, BM) || !make_map(&mA2, r.act_lo, p.P, p.I, BM) ||
+        !make_map(&mB, w2, p.E * p.H, p.I, bn))
         return MOE_ERR_CUDA;
     FfnArgs g = base_args(r);
     g.bn = bn; g.nb = (int)(p.H / bn); g.kb = (int)(p.I / BK);
     g.a_mode = 1; g.a_cap = 0; g.b_rows = p.H; g.mode = 1; g.out_ld = p.H;
     if (em) { g.out = expert_out; g.out_mode = 0; g.out_cap = p.cap; }
     else { g.out = r.ypick; g.out_mode = 1; g.out_cap = 0; }
-    return launch_gemm(mA, mB, g, max_mblocks(p) * g.nb, s);
+    return launch_gemm<true>(mA, mA2, mB, g, max_mblocks(p) * g.nb, s);
 }
 
 }  // namespace moe

@@ -106,6 +106,7 @@ int make_plan(const moe_geom &g, Plan *p) {
     q.blk_dbase = take(4 * W * nb);
     q.recv_x = take(2 * (em ? E : W) * cap * H);
     q.act = take(2 * P * I);
+    q.act_lo = take(2 * P * I);
     q.apick = take(em ? 0 : 2 * P * H);
     q.ypick = take(em ? 0 : 4 * P * H);
     q.total = off;
@@ -127,6 +128,7 @@ Routing carve(const Plan &p, void *ws) {
     r.recv_topk_w = reinterpret_cast<float *>(b + p.recv_topk_w);
     r.recv_x = reinterpret_cast<uint16_t *>(b + p.recv_x);
     r.act = reinterpret_cast<uint16_t *>(b + p.act);
+    r.act_lo = reinterpret_cast<uint16_t *>(b + p.act_lo);
     r.apick = reinterpret_cast<uint16_t *>(b + p.apick);
     r.ypick = reinterpret_cast<float *>(b + p.ypick);
     return r;

@@ -24,7 +24,7 @@ struct Plan {
     int nb;         // routing blocks in total (W * nbpr)
     size_t status, counts, offsets, mprefix, pick_pos, pick_src, slot, layout_range,
         blk_hist, blk_base, recv_row, recv_count, num_recv, recv_src, recv_topk_idx,
-        recv_topk_w, blk_dhist, blk_dbase, recv_x, act, apick, ypick, total;
+        recv_topk_w, blk_dhist, blk_dbase, recv_x, act, act_lo, apick, ypick, total;
 };
 
 // Returns MOE_OK or a moe_error for an invalid geometry.
@@ -37,7 +37,7 @@ struct Routing {
         *blk_hist, *blk_base, *recv_row, *recv_count, *num_recv, *recv_src, *recv_topk_idx,
         *blk_dhist, *blk_dbase;
     float *recv_topk_w;
-    uint16_t *recv_x, *act, *apick;
+    uint16_t *recv_x, *act, *act_lo, *apick;   // act / act_lo: SwiGLU output as a bf16 pair
     float *ypick;
 };
 

@@ -5,8 +5,8 @@ CPU-baseline leg (bench.py --impl reference / cpu_baseline) may import this pack
 The product library never calls it and shares no code with it.
 
 Plain and slow on purpose: routing is the literal (t, j)-ordered loop in moe_oracle.c;
-the FFN and combine are numpy in float64, one expert at a time; bf16 rounding happens
-exactly where the layer stores bf16 values.
+the FFN and combine are numpy in float64, one expert at a time; the only rounding is the
+final output's to bf16.
 
 Sources (page title, section):
   * FlashInfer "MoE-EP implementation & usage", section 2 "Call stack": dispatch ->
@@ -22,8 +22,9 @@ Sources (page title, section):
 Readings where the pages are silent (each listed in the design notes):
   * gate = rows [0, I) of w1[e], up = rows [I, 2I); SwiGLU act = silu(gate) * up with
     silu(g) = g / (1 + exp(-g))  (parity unpinned by the pages: a fixed convention);
-  * act is rounded to bf16 (it is the bf16 operand of the second grouped GEMM);
-    expert_out stays float (float64 here); the final output is rounded to bf16;
+  * the expert FFN is evaluated in full precision from the bf16 weights and inputs: no
+    re-quantisation of the SwiGLU activation or of expert_out (float64 here); the final
+    combined output is rounded to bf16 (round-to-nearest-even);
   * RANK_MAJOR / FLAT apply topk_weights in the FFN stage's reduction over the local
     picks of a received row (ascending j), and combine sums over destinations without
     weights (ascending d).
@@ -153,12 +154,12 @@ def dispatch_rows(geom, rt):
 
 def swiglu_expert(xrows, w1e, w2e):
     """One expert's FFN on the rows xrows [n, H] (float64 values of bf16 inputs):
-    h = x W1e^T, act = bf16(silu(h[:, :I]) * h[:, I:]), y = act W2e^T (float64)."""
+    h = x W1e^T, act = silu(h[:, :I]) * h[:, I:], y = act W2e^T, all float64."""
     I = w2e.shape[1]
     h = xrows @ w1e.T
     g, u = h[:, :I], h[:, I:]
     with np.errstate(over="ignore"):
-        act = round_bf16(g / (1.0 + np.exp(-g)) * u)
+        act = g / (1.0 + np.exp(-g)) * u
     return act @ w2e.T
 
 
