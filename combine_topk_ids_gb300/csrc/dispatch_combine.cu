@@ -1,7 +1,7 @@
 // Data-movement kernels of the layer: the dispatch row scatter, the RANK_MAJOR / FLAT
 // pick gather and weighted local-pick reduction, the combine gather-reduce, and the
 // one-time gate/up interleave of w1.  All are HBM-bound copies or reductions: one warp per
-// row, 16-byte vector loads and stores, several loads in flight per lane.
+// (row, column chunk), 16-byte vector loads and stores, several loads in flight per lane.
 //
 // Sources: Mooncake EP guide, "Buffer.dispatch(...)" / "Buffer.combine(...)" (send each
 // token row to the owners of its experts; return expert outputs by routing weight to the
@@ -35,20 +35,27 @@ __device__ __forceinline__ float4 ld_nc_f4(const float *p) {
 }
 
 // ---------------------------------------------------------------- dispatch row scatter
-// One warp per token: x[t] is read once and written to each of its receive rows
+// x[t] is read once and written to each of its receive rows
 // (EM: the slot of every kept pick; RM/FLAT: the row in every destination that got it).
+// Rows are split into chunks of 32 lanes x kCopyU 16-byte vectors (1024 bf16 or 512 fp32
+// columns); one warp handles one (row, chunk) so that even a 1024-token batch keeps
+// thousands of warps and many loads in flight.
+constexpr int kCopyU = 4;
+
 struct CopyArgs {
     const uint16_t *x;
     uint16_t *recv;
     const int32_t *slot, *recv_row;
-    int T, k, W, H, layout;
+    int T, k, W, H, layout, nchunk;
     int64_t cap;
 };
 
 __global__ void __launch_bounds__(kCopyThreads) dispatch_copy_kernel(CopyArgs a) {
     __shared__ int64_t dst[kWarpsPerBlock][MOE_MAX_WORLD > MOE_MAX_TOPK ? MOE_MAX_WORLD : MOE_MAX_TOPK];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t t = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (token, chunk)
+    const int64_t t = gw / a.nchunk;
+    const int chunk = (int)(gw - t * a.nchunk);
     if (t >= a.T) return;
     const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
     const int n = em ? a.k : a.W;
@@ -58,8 +65,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_copy_kernel(CopyArgs a)
         int64_t row = -1;
         if (q < n) {
             if (em) {
-                int s = a.slot[t * a.k + q];
-                row = s;
+                row = a.slot[t * a.k + q];
             } else {
                 int r = a.recv_row[t * a.W + q];
                 row = r >= 0 ? (int64_t)q * a.cap + r : -1;
@@ -71,19 +77,17 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_copy_kernel(CopyArgs a)
     }
     __syncwarp();
     const int nv = a.H / 8;   // uint4 per row
+    const int c0 = chunk * 32 * kCopyU + lane;
     const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * a.H);
-    constexpr int U = 4;
-    for (int c0 = lane; c0 < nv; c0 += 32 * U) {
-        uint4 v[U];
+    uint4 v[kCopyU];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (c0 + 32 * u < nv) v[u] = ld_nc_v4(src + c0 + 32 * u);
-        for (int d = 0; d < nd; ++d) {
-            uint4 *o = reinterpret_cast<uint4 *>(a.recv + dst[warp][d] * a.H);
+    for (int u = 0; u < kCopyU; ++u)
+        if (c0 + 32 * u < nv) v[u] = ld_nc_v4(src + c0 + 32 * u);
+    for (int d = 0; d < nd; ++d) {
+        uint4 *o = reinterpret_cast<uint4 *>(a.recv + dst[warp][d] * a.H);
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (c0 + 32 * u < nv) o[c0 + 32 * u] = v[u];
-        }
+        for (int u = 0; u < kCopyU; ++u)
+            if (c0 + 32 * u < nv) o[c0 + 32 * u] = v[u];
     }
 }
 
@@ -94,7 +98,7 @@ struct GatherArgs {
     const uint16_t *recv;
     uint16_t *apick;
     const int32_t *offsets, *pick_src, *recv_row;
-    int E, Le, k, W, H;
+    int E, Le, k, W, H, nchunk;
     int64_t P, cap;
 };
 
@@ -110,7 +114,9 @@ __device__ __forceinline__ int expert_of_pick(const int32_t *offsets, int E, int
 
 __global__ void __launch_bounds__(kCopyThreads) gather_picks_kernel(GatherArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t p = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (pick, chunk)
+    const int64_t p = gw / a.nchunk;
+    const int chunk = (int)(gw - p * a.nchunk);
     if (p >= a.P || p >= a.offsets[a.E]) return;
     const int e = expert_of_pick(a.offsets, a.E, (int)p);
     const int i = a.pick_src[p];
@@ -119,16 +125,14 @@ __global__ void __launch_bounds__(kCopyThreads) gather_picks_kernel(GatherArgs a
     const uint4 *src = reinterpret_cast<const uint4 *>(a.recv + row * a.H);
     uint4 *dst = reinterpret_cast<uint4 *>(a.apick + p * a.H);
     const int nv = a.H / 8;
-    constexpr int U = 4;
-    for (int c0 = lane; c0 < nv; c0 += 32 * U) {
-        uint4 v[U];
+    const int c0 = chunk * 32 * kCopyU + lane;
+    uint4 v[kCopyU];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (c0 + 32 * u < nv) v[u] = ld_nc_v4(src + c0 + 32 * u);
+    for (int u = 0; u < kCopyU; ++u)
+        if (c0 + 32 * u < nv) v[u] = ld_nc_v4(src + c0 + 32 * u);
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (c0 + 32 * u < nv) dst[c0 + 32 * u] = v[u];
-    }
+    for (int u = 0; u < kCopyU; ++u)
+        if (c0 + 32 * u < nv) dst[c0 + 32 * u] = v[u];
 }
 
 // ------------------------- RANK_MAJOR / FLAT: weighted reduction over a row's local picks
@@ -139,7 +143,7 @@ struct ReduceArgs {
     float *out;
     const int32_t *recv_count, *num_recv, *recv_src, *recv_topk_idx, *pick_pos;
     const float *recv_topk_w;
-    int W, Tr, k, H, layout;
+    int W, Tr, k, H, layout, nchunk;
     int64_t cap;
 };
 
@@ -147,7 +151,9 @@ __global__ void __launch_bounds__(kCopyThreads) reduce_ranks_kernel(ReduceArgs a
     __shared__ int64_t src[kWarpsPerBlock][MOE_MAX_TOPK];
     __shared__ float wt[kWarpsPerBlock][MOE_MAX_TOPK];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t gr = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // d*cap + r
+    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (row, chunk)
+    const int64_t gr = gw / a.nchunk;                                 // d*cap + r
+    const int chunk = (int)(gw - gr * a.nchunk);
     if (gr >= (int64_t)a.W * a.cap) return;
     const int d = (int)(gr / a.cap);
     const int r = (int)(gr % a.cap);
@@ -175,19 +181,29 @@ __global__ void __launch_bounds__(kCopyThreads) reduce_ranks_kernel(ReduceArgs a
     }
     __syncwarp();
     const int nv = a.H / 4;
-    float4 *o = reinterpret_cast<float4 *>(a.out + gr * a.H);
-    for (int c = lane; c < nv; c += 32) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < n; ++q) {
-            float4 y = ld_nc_f4(a.ypick + src[warp][q] * a.H + 4 * c);
-            float w = wt[warp][q];
-            acc.x = fmaf(w, y.x, acc.x);
-            acc.y = fmaf(w, y.y, acc.y);
-            acc.z = fmaf(w, y.z, acc.z);
-            acc.w = fmaf(w, y.w, acc.w);
+    const int c0 = chunk * 32 * kCopyU + lane;
+    float4 acc[kCopyU];
+#pragma unroll
+    for (int u = 0; u < kCopyU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < n; ++q) {
+        const float *row = a.ypick + src[warp][q] * a.H;
+        const float w = wt[warp][q];
+        float4 y[kCopyU];
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u)
+            if (c0 + 32 * u < nv) y[u] = ld_nc_f4(row + 4 * (c0 + 32 * u));
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u) {
+            acc[u].x = fmaf(w, y[u].x, acc[u].x);
+            acc[u].y = fmaf(w, y[u].y, acc[u].y);
+            acc[u].z = fmaf(w, y[u].z, acc[u].z);
+            acc[u].w = fmaf(w, y[u].w, acc[u].w);
         }
-        o[c] = acc;
     }
+    float4 *o = reinterpret_cast<float4 *>(a.out + gr * a.H);
+#pragma unroll
+    for (int u = 0; u < kCopyU; ++u)
+        if (c0 + 32 * u < nv) o[c0 + 32 * u] = acc[u];
 }
 
 // ----------------------------------------------------------------------------- combine
@@ -198,7 +214,7 @@ struct CombineArgs {
     const float *topk_w;
     const int32_t *slot, *recv_row;
     uint16_t *out;
-    int T, k, W, H, layout;
+    int T, k, W, H, layout, nchunk;
     int64_t cap;
 };
 
@@ -206,7 +222,9 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
     __shared__ int64_t src[kWarpsPerBlock][MOE_MAX_WORLD > MOE_MAX_TOPK ? MOE_MAX_WORLD : MOE_MAX_TOPK];
     __shared__ float wt[kWarpsPerBlock][MOE_MAX_WORLD > MOE_MAX_TOPK ? MOE_MAX_WORLD : MOE_MAX_TOPK];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t t = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (token, chunk)
+    const int64_t t = gw / a.nchunk;
+    const int chunk = (int)(gw - t * a.nchunk);
     if (t >= a.T) return;
     const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
     const int n = em ? a.k : a.W;
@@ -233,31 +251,43 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
         ns += __popc(bal);
     }
     __syncwarp();
-    const int nv = a.H / 4;
-    uint2 *o = reinterpret_cast<uint2 *>(a.out + t * a.H);
-    for (int c = lane; c < nv; c += 32) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < ns; ++q) {
-            float4 y = ld_nc_f4(a.eo + src[warp][q] * a.H + 4 * c);
+    const int nv = a.H / 4;   // float4 per row
+    const int c0 = chunk * 32 * kCopyU + lane;
+    float4 acc[kCopyU];
+#pragma unroll
+    for (int u = 0; u < kCopyU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < ns; ++q) {
+        const float *row = a.eo + src[warp][q] * a.H;
+        const float w = wt[warp][q];
+        float4 y[kCopyU];
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u)
+            if (c0 + 32 * u < nv) y[u] = ld_nc_f4(row + 4 * (c0 + 32 * u));
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u) {
             if (em) {
-                float w = wt[warp][q];
-                acc.x = fmaf(w, y.x, acc.x);
-                acc.y = fmaf(w, y.y, acc.y);
-                acc.z = fmaf(w, y.z, acc.z);
-                acc.w = fmaf(w, y.w, acc.w);
+                acc[u].x = fmaf(w, y[u].x, acc[u].x);
+                acc[u].y = fmaf(w, y[u].y, acc[u].y);
+                acc[u].z = fmaf(w, y[u].z, acc[u].z);
+                acc[u].w = fmaf(w, y[u].w, acc[u].w);
             } else {
-                acc.x += y.x;
-                acc.y += y.y;
-                acc.z += y.z;
-                acc.w += y.w;
+                acc[u].x += y[u].x;
+                acc[u].y += y[u].y;
+                acc[u].z += y[u].z;
+                acc[u].w += y[u].w;
             }
         }
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    }
+    uint2 *o = reinterpret_cast<uint2 *>(a.out + t * a.H);
+#pragma unroll
+    for (int u = 0; u < kCopyU; ++u) {
+        if (c0 + 32 * u >= nv) continue;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[u].z, acc[u].w);
         uint2 v;
         v.x = *reinterpret_cast<uint32_t *>(&lo);
         v.y = *reinterpret_cast<uint32_t *>(&hi);
-        o[c] = v;
+        o[c0 + 32 * u] = v;
     }
 }
 
@@ -287,28 +317,31 @@ inline unsigned blocks_for(int64_t warps) {
 cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.T == 0) return cudaSuccess;
+    const int nchunk = (int)((p.H / 8 + 32 * kCopyU - 1) / (32 * kCopyU));
     CopyArgs a{x, r.recv_x, r.slot, r.recv_row, (int)p.T, (int)p.k, (int)p.W, (int)p.H,
-               p.layout, p.cap};
-    dispatch_copy_kernel<<<blocks_for(p.T), kCopyThreads, 0, s>>>(a);
+               p.layout, nchunk, p.cap};
+    dispatch_copy_kernel<<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather_picks(const Routing &r, cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.P == 0) return cudaSuccess;
+    const int nchunk = (int)((p.H / 8 + 32 * kCopyU - 1) / (32 * kCopyU));
     GatherArgs a{r.recv_x, r.apick, r.offsets, r.pick_src, r.recv_row,
-                 (int)p.E, (int)(p.E / p.W), (int)p.k, (int)p.W, (int)p.H, p.P, p.cap};
-    gather_picks_kernel<<<blocks_for(p.P), kCopyThreads, 0, s>>>(a);
+                 (int)p.E, (int)(p.E / p.W), (int)p.k, (int)p.W, (int)p.H, nchunk, p.P, p.cap};
+    gather_picks_kernel<<<blocks_for(p.P * nchunk), kCopyThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_reduce_ranks(const Routing &r, float *expert_out, cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.T == 0) return cudaSuccess;
+    const int nchunk = (int)((p.H / 4 + 32 * kCopyU - 1) / (32 * kCopyU));
     ReduceArgs a{r.ypick, expert_out, r.recv_count, r.num_recv, r.recv_src, r.recv_topk_idx,
                  r.pick_pos, r.recv_topk_w, (int)p.W, (int)p.Tr, (int)p.k, (int)p.H, p.layout,
-                 p.cap};
-    reduce_ranks_kernel<<<blocks_for(p.W * p.cap), kCopyThreads, 0, s>>>(a);
+                 nchunk, p.cap};
+    reduce_ranks_kernel<<<blocks_for(p.W * p.cap * nchunk), kCopyThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -316,9 +349,10 @@ cudaError_t launch_combine(const Routing &r, const float *expert_out, const floa
                            uint16_t *out, cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.T == 0) return cudaSuccess;
+    const int nchunk = (int)((p.H / 4 + 32 * kCopyU - 1) / (32 * kCopyU));
     CombineArgs a{expert_out, topk_w, r.slot, r.recv_row, out, (int)p.T, (int)p.k, (int)p.W,
-                  (int)p.H, p.layout, p.cap};
-    combine_kernel<<<blocks_for(p.T), kCopyThreads, 0, s>>>(a);
+                  (int)p.H, p.layout, nchunk, p.cap};
+    combine_kernel<<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

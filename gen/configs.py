@@ -77,7 +77,7 @@ ALL = {**CONFIGS, **SMALL}
 # A smaller EXPERT_MAJOR case for detailed (multi-pass) profiler captures of the same
 # kernels: 4 experts, weights 0.7 GB (larger than L2), about 1.3 GB on the device.
 PROFILE = {
-    "ncu_em_small": MoeConfig("ncu_em_small", W=8, Tr=128, H=4096, E=4, k=2, I=7168,
+    "ncu_em_small": MoeConfig("ncu_em_small", W=4, Tr=256, H=4096, E=4, k=2, I=7168,
                               layout="EM", algo="LL", routing="uniform"),
     "ncu_flat_small": MoeConfig("ncu_flat_small", W=8, Tr=512, H=7168, E=32, k=8, I=2048,
                                 layout="FLAT", algo="HT", routing="uniform"),
