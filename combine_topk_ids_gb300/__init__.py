@@ -71,6 +71,8 @@ def lib():
         L.moe_get_status.argtypes = [H, ctypes.POINTER(ctypes.c_int32), _P]
         L.moe_forward_host.argtypes = [G, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                        _P, ctypes.c_size_t, H, _P]
+        L.moe_route_noalloc.argtypes = [G, _P, ctypes.c_int] + [_P] * 8
+        L.moe_route_noalloc.restype = ctypes.c_int
         L.moe_strerror.argtypes = [ctypes.c_int]
         L.moe_strerror.restype = ctypes.c_char_p
         for f in ("moe_workspace_size", "moe_expert_out_size", "moe_dispatch",
@@ -155,6 +157,16 @@ def moe_forward_host(g, x_host, ids_host, w_host, out_host, x_dev, ids_dev, w_de
         _ptr(out_host), _ptr(x_dev), _ptr(ids_dev), _ptr(w_dev), _ptr(out_dev), _ptr(w1_prepared),
         _ptr(w2), _ptr(expert_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
         ctypes.byref(handle), _stream(stream)), "moe_forward_host")
+
+
+def moe_route_noalloc(g, topk_ids, counts, offsets, pick_pos, pick_src, slot, layout_range, status,
+                      stream=None):
+    """EXPERT_MAJOR routing into caller buffers with no workspace and no allocation, for
+    callers that can only pass inputs and outputs (see include/moe.h)."""
+    _check(lib().moe_route_noalloc(ctypes.byref(g), _ptr(topk_ids), _ids_dtype(topk_ids), _ptr(counts),
+                                   _ptr(offsets), _ptr(pick_pos), _ptr(pick_src), _ptr(slot),
+                                   _ptr(layout_range), _ptr(status), _stream(stream)),
+           "moe_route_noalloc")
 
 
 def moe_get_status(h, stream=None) -> int:

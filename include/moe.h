@@ -248,6 +248,35 @@ int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids
  */
 int moe_get_status(const moe_handle *h, int32_t *status_host, void *stream);
 
+/*
+ * moe_route_noalloc - EXPERT_MAJOR routing that allocates nothing and needs no workspace.
+ * The pages have no counterpart of this call; it exists for callers that can only pass
+ * input and output buffers (plugin hosts and engines that own all device memory and
+ * plan it ahead of time) and so can neither give moe_dispatch a workspace nor let the
+ * library call cudaMalloc.
+ *   Computes exactly the routing outputs moe_dispatch produces for an EXPERT_MAJOR
+ *   geometry, into caller buffers: counts_dev [E], offsets_dev [E+1], pick_pos_dev
+ *   [T*k], pick_src_dev [T*k], slot_dev [T*k], layout_range_dev [E][W][2] (all int32,
+ *   same meaning as the moe_handle fields) and status_dev (one int32, MOE_STATUS_* bits,
+ *   cleared by the call).  No rows are copied.
+ *   Scratch: a static device array of MOE_NOALLOC_SCRATCH_BYTES compiled into the library
+ *   (held by every GPU that loads it until the process exits).  The routing needs
+ *   (2 * E * nb + E + 1) * 4 bytes of it, nb being the routing chunk count of the geometry
+ *   (about 256 for large batches); a larger geometry returns MOE_ERR_LIMIT.
+ *   The first call on each device looks the array's address up (cudaGetSymbolAddress)
+ *   with that device current; make that first call before any stream capture.
+ *   Every call shares the one array, so calls that overlap on the GPU (issued on different
+ *   streams of one device without ordering between them) race on it and corrupt each
+ *   other's results: order them on one stream.
+ *   Errors: MOE_ERR_INVALID_ARGUMENT for a non-EXPERT_MAJOR geometry or a NULL buffer,
+ *   the geometry errors of moe_workspace_size, MOE_ERR_LIMIT beyond the scratch size.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+int moe_route_noalloc(const moe_geom *g, const void *topk_ids_dev, int ids_dtype,
+                      int32_t *counts_dev, int32_t *offsets_dev, int32_t *pick_pos_dev,
+                      int32_t *pick_src_dev, int32_t *slot_dev, int32_t *layout_range_dev,
+                      int32_t *status_dev, void *stream);
+
 /* moe_strerror - static text for a moe_error code. */
 const char *moe_strerror(int err);
 
