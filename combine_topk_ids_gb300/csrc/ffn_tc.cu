@@ -40,25 +40,31 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int THREADS = 256;
 constexpr int TMEM_COLS = 2 * BN;               // two fp32 accumulators of 128 x 256
-// Pipeline shape: HILO = the A operand is a bf16 pair (two A tiles per stage).
-template <bool HILO> struct Pipe {
-    static constexpr int kATiles = HILO ? 2 : 1;
-    static constexpr int kStageBytes = kATiles * A_BYTES + B_BYTES;   // 48 or 64 KB
-    static constexpr int kStages = HILO ? 3 : 4;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
-};
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
+
+// Pipeline shape.  HILO: the A operand is a bf16 pair (two A tiles per stage).  PAIR: a
+// cluster of two CTAs on two SMs computes a 256-row tile with tcgen05.mma.cta_group::2;
+// each CTA stages its own 128 rows of A and half of the B tile.
+template <bool HILO, bool PAIR> struct Pipe {
+    static constexpr int kATiles = HILO ? 2 : 1;
+    static constexpr int kBBytes = PAIR ? B_BYTES / 2 : B_BYTES;
+    static constexpr int kStageBytes = kATiles * A_BYTES + kBBytes;     // 32..64 KB
+    static constexpr int kStages = (192 * 1024) / kStageBytes;          // 3..6
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int kMRows = PAIR ? 2 * BM : BM;                   // rows of one tile
+};
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A bf16
 // (bits 7-9 = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15/16 = 0),
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc(int n) {
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(BM >> 4) << 24);
+           ((uint32_t)(m >> 4) << 24);
 }
 
 struct FfnArgs {
-    const int32_t *counts, *offsets, *mprefix;
+    const int32_t *counts, *offsets;
+    const int32_t *mprefix;   // prefix over experts of ceil(rows / tile rows)
     int E;
     int bn;        // n-tile width: 256 or 128
     int nb;        // n-blocks per expert (N / bn)
@@ -154,6 +160,64 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
+// --- two-SM (cluster of two CTAs) variants
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t num_clusters_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+// TMA load into this CTA's shared memory, completing on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// Arrive once on the mbarrier at `bar` in both CTAs of the pair when this thread's
+// earlier tcgen05 operations complete.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t acc) {
     asm volatile(
@@ -217,17 +281,17 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return g / (1.0f + __expf(-g)) * u;
 }
 
-template <bool HILO>
+template <bool HILO, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB, FfnArgs a) {
-    using P = Pipe<HILO>;
+    using P = Pipe<HILO, PAIR>;
     constexpr int STAGES = P::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;                                   // [STAGES][kATiles] A tiles
-    uint8_t *sB = smem + STAGES * P::kATiles * A_BYTES;   // [STAGES] B tiles
+    uint8_t *sB = smem + STAGES * P::kATiles * A_BYTES;   // [STAGES] B tiles (or halves)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * P::kStageBytes);
     // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
@@ -236,6 +300,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
     const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+    // PAIR: rank 0 (the leader) issues the MMAs for both CTAs and owns the barriers they
+    // wait on; rank 1 stages rows 128..255 of A and the second half of B.
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+    const bool leader = rank == 0;
+    const int first_tile = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int tile_step = PAIR ? (int)num_clusters_x() : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -244,7 +314,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(tfull0 + 8 * s, 1);
-            mbar_init(tempty0 + 8 * s, 128);
+            mbar_init(tempty0 + 8 * s, PAIR ? 8 : 4);   // one arrival per epilogue warp
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -254,14 +324,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
     }
     if (warp == 2) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();   // the peer's barriers exist before anyone signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = __ldg(a.mprefix + a.E) * a.nb;
@@ -271,33 +350,44 @@ __global__ void __launch_bounds__(THREADS, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const int b_rows_cta = PAIR ? a.bn / 2 : a.bn;
+        const uint32_t tx_cta = (uint32_t)(P::kATiles * A_BYTES + b_rows_cta * BK * 2);
+        const uint32_t tx = PAIR ? 2 * tx_cta : tx_cta;   // the leader's barrier sees both CTAs
+        for (int tile = first_tile; tile < total && ok; tile += tile_step) {
             int e, mb, nbk;
             decode_tile(a, tile, e, mb, nbk);
             const int64_t arow = (a.a_mode == 0 ? (int64_t)e * a.a_cap : (int64_t)__ldg(a.offsets + e)) +
-                                 (int64_t)mb * BM;
-            const int64_t brow = (int64_t)e * a.b_rows + (int64_t)nbk * a.bn;
-            const uint32_t tx = (uint32_t)(P::kATiles * A_BYTES + a.bn * BK * 2);
+                                 (int64_t)mb * P::kMRows + (int64_t)rank * BM;
+            const int64_t brow = (int64_t)e * a.b_rows + (int64_t)nbk * a.bn + (int64_t)rank * b_rows_cta;
             for (int kb = 0; kb < a.kb; ++kb) {
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, a.status)) { ok = false; break; }
                 const uint32_t fb = full0 + 8 * stage;
-                mbar_expect_tx(fb, tx);
                 uint8_t *sa = sA + stage * P::kATiles * A_BYTES;
-                tma_load_2d(smem_u32(sa), &tmA, kb * BK, (int)arow, fb);
-                if (HILO) tma_load_2d(smem_u32(sa + A_BYTES), &tmA2, kb * BK, (int)arow, fb);
-                tma_load_2d(smem_u32(sB + stage * B_BYTES), &tmB, kb * BK, (int)brow, fb);
+                const uint32_t sb = smem_u32(sB + stage * P::kBBytes);
+                if (PAIR) {
+                    if (leader) mbar_expect_tx(fb, tx);
+                    const uint32_t fbl = map_to_rank(fb, 0);
+                    tma_load_2d_pair(smem_u32(sa), &tmA, kb * BK, (int)arow, fbl);
+                    if (HILO) tma_load_2d_pair(smem_u32(sa + A_BYTES), &tmA2, kb * BK, (int)arow, fbl);
+                    tma_load_2d_pair(sb, &tmB, kb * BK, (int)brow, fbl);
+                } else {
+                    mbar_expect_tx(fb, tx);
+                    tma_load_2d(smem_u32(sa), &tmA, kb * BK, (int)arow, fb);
+                    if (HILO) tma_load_2d(smem_u32(sa + A_BYTES), &tmA2, kb * BK, (int)arow, fb);
+                    tma_load_2d(sb, &tmB, kb * BK, (int)brow, fb);
+                }
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && leader) {
         // ---------------------------------------------------------------- MMA issuer
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        const uint32_t idesc = make_idesc(a.bn);
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const uint32_t idesc = make_idesc(P::kMRows, a.bn);
+        for (int tile = first_tile; tile < total && ok; tile += tile_step) {
             if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -305,32 +395,43 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(sA + stage * P::kATiles * A_BYTES);
-                const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+                const uint32_t b0 = smem_u32(sB + stage * P::kBBytes);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     const uint64_t bd = sw128_desc(b0 + kk * 32);
-                    mma_bf16(d_tmem, sw128_desc(a0 + kk * 32), bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                    if (HILO) mma_bf16(d_tmem, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc, 1u);
+                    const uint64_t ad = sw128_desc(a0 + kk * 32);
+                    const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+                    if (PAIR) {
+                        mma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+                        if (HILO) mma_bf16_pair(d_tmem, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc, 1u);
+                    } else {
+                        mma_bf16(d_tmem, ad, bd, idesc, accum);
+                        if (HILO) mma_bf16(d_tmem, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc, 1u);
+                    }
                 }
-                mma_commit(empty0 + 8 * stage);   // stage reusable once these MMAs finish
+                // the stage is reusable (in both CTAs) once these MMAs finish
+                if (PAIR) mma_commit_pair(empty0 + 8 * stage);
+                else mma_commit(empty0 + 8 * stage);
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
-            mma_commit(tfull0 + 8 * acc);          // accumulator ready for the epilogue
+            if (PAIR) mma_commit_pair(tfull0 + 8 * acc);   // accumulators ready in both CTAs
+            else mma_commit(tfull0 + 8 * acc);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------------ epilogue
         const int quad = warp & 3;                 // TMEM lanes 32*quad .. 32*quad+31
-        const int row = quad * 32 + lane;
+        const int row = quad * 32 + lane;          // row inside this CTA's 128 rows
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        for (int tile = first_tile; tile < total; tile += tile_step) {
             int e, mb, nbk;
             decode_tile(a, tile, e, mb, nbk);
-            const int valid = min(BM, __ldg(a.counts + e) - mb * BM);
+            const int m0 = mb * P::kMRows + (int)rank * BM;   // first row of this CTA's half
+            const int valid = min(BM, __ldg(a.counts + e) - m0);
             const int64_t orow = (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) +
-                                 (int64_t)mb * BM + row;
+                                 (int64_t)m0 + row;
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
@@ -384,12 +485,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(tempty0 + 8 * acc);
+            __syncwarp();
+            if (lane == 0) {   // this warp is done with the accumulator
+                if (PAIR) mbar_arrive_cluster(map_to_rank(tempty0 + 8 * acc, 0));
+                else mbar_arrive(tempty0 + 8 * acc);
+            }
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
     }
 
     __syncthreads();
+    if (PAIR) cluster_sync();   // no signal from the peer can still be on its way here
     if (*abort_flag) {
         // Give in-flight TMA copies and MMAs time to land before the memory is released.
         unsigned long long t0 = globaltimer();
@@ -397,9 +503,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (warp == 2) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(TMEM_COLS)
-                     : "memory");
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(TMEM_COLS)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(TMEM_COLS)
+                         : "memory");
     }
 }
 
@@ -438,70 +549,121 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool HILO>
+template <bool HILO, bool PAIR>
 int launch_gemm(const CUtensorMap &ma, const CUtensorMap &ma2, const CUtensorMap &mb,
                 const FfnArgs &args, int64_t max_tiles, cudaStream_t s) {
     if (max_tiles <= 0) return MOE_OK;
-    constexpr int smem = Pipe<HILO>::kSmemBytes;
+    constexpr int smem = Pipe<HILO, PAIR>::kSmemBytes;
+    auto kernel = ffn_gemm_kernel<HILO, PAIR>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(ffn_gemm_kernel<HILO>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static int max_clusters = 0;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (attr_err == cudaSuccess && PAIR) {
+            attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+            cudaLaunchConfig_t q = {};
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            q.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+            q.blockDim = dim3(THREADS, 1, 1);
+            q.dynamicSmemBytes = smem;
+            q.attrs = at;
+            q.numAttrs = 1;
+            if (attr_err == cudaSuccess)
+                attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &q);
+        }
     });
     if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
-    int grid = num_sms();
-    if ((int64_t)grid > max_tiles) grid = (int)max_tiles;
-    ffn_gemm_kernel<HILO><<<grid, THREADS, smem, s>>>(ma, ma2, mb, args);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    if (!PAIR) {
+        int grid = num_sms();
+        if ((int64_t)grid > max_tiles) grid = (int)max_tiles;
+        kernel<<<grid, THREADS, smem, s>>>(ma, ma2, mb, args);
+        return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
+    // persistent clusters of two CTAs: never more than can be resident at once
+    int clusters = max_clusters > 0 ? max_clusters : num_sms() / 2;
+    if ((int64_t)clusters > max_tiles) clusters = (int)max_tiles;
+    if (clusters < 1) return MOE_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, ma, ma2, mb, args) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-}  // namespace
+// Two-SM tiles (256 rows per tile).  Measured on GB300 (same box, same build, A/B): the
+// cta_group::2 MMA spends ~24% more tensor-pipe cycles per FLOP than two cta_group::1
+// MMAs here, and halving the per-SM B tile only pays that back on small per-expert GEMMs
+// (K <= 2048 and N <= 2048: ragged 16384-token workload, GEMM1 -6%, GEMM2 -3%); on the
+// Mixtral-like (K 4096 / 14336) and DeepSeek-like prefill (K 7168) shapes it was 2-30%
+// slower.  It also needs many rows per expert, or most of a 256-row tile is padding.
+// Decided from the geometry alone (the counts live on the device).
+bool use_pair(const Plan &p, int64_t K, int64_t N) {
+    return p.P >= 192 * p.E && K <= 2048 && N <= 2048;
+}
 
-namespace {
-// upper bound of the m-blocks over all experts: sum ceil(n_e/128) <= P/128 + E
-int64_t max_mblocks(const Plan &p) { return p.P / BM + p.E; }
+// upper bound of the row blocks over all experts: sum ceil(n_e/rows) <= P/rows + E
+int64_t max_mblocks(const Plan &p, int rows) { return p.P / rows + p.E; }
 
-FfnArgs base_args(const Routing &r) {
+FfnArgs base_args(const Routing &r, bool pair) {
     const Plan &p = *r.p;
     FfnArgs g{};
-    g.counts = r.counts; g.offsets = r.offsets; g.mprefix = r.mprefix; g.E = (int)p.E;
+    g.counts = r.counts; g.offsets = r.offsets; g.mprefix = pair ? r.mprefix2 : r.mprefix;
+    g.E = (int)p.E;
     g.status = r.status;
     return g;
 }
+
 }  // namespace
 
 int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.P == 0) return MOE_OK;
     const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    const bool pair = use_pair(p, p.H, 2 * p.I);
     CUtensorMap mA, mB;
     const void *a1 = em ? (const void *)r.recv_x : (const void *)r.apick;
     const int64_t a1_rows = em ? p.E * p.cap : p.P;
-    if (!make_map(&mA, a1, a1_rows, p.H, BM) || !make_map(&mB, w1p, p.E * 2 * p.I, p.H, BN))
+    if (!make_map(&mA, a1, a1_rows, p.H, BM) ||
+        !make_map(&mB, w1p, p.E * 2 * p.I, p.H, pair ? BN / 2 : BN))
         return MOE_ERR_CUDA;
-    FfnArgs g = base_args(r);
+    FfnArgs g = base_args(r, pair);
     g.bn = BN; g.nb = (int)(2 * p.I / BN); g.kb = (int)(p.H / BK);
     g.a_mode = em ? 0 : 1; g.a_cap = p.cap; g.b_rows = 2 * p.I;
     g.mode = 0; g.out = r.act; g.out2 = r.act_lo; g.out_ld = p.I; g.out_mode = 1; g.out_cap = 0;
-    return launch_gemm<false>(mA, mA, mB, g, max_mblocks(p) * g.nb, s);
+    if (pair) return launch_gemm<false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
+    return launch_gemm<false, false>(mA, mA, mB, g, max_mblocks(p, BM) * g.nb, s);
 }
 
 int launch_gemm2(const Routing &r, const uint16_t *w2, float *expert_out, cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.P == 0) return MOE_OK;
     const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    const bool pair = use_pair(p, p.I, p.H);
     const int bn = (p.H % 256 == 0) ? 256 : 128;
     CUtensorMap mA, mA2, mB;
     if (!make_map(&mA, r.act, p.P, p.I, BM) || !make_map(&mA2, r.act_lo, p.P, p.I, BM) ||
-        !make_map(&mB, w2, p.E * p.H, p.I, bn))
+        !make_map(&mB, w2, p.E * p.H, p.I, pair ? bn / 2 : bn))
         return MOE_ERR_CUDA;
-    FfnArgs g = base_args(r);
+    FfnArgs g = base_args(r, pair);
     g.bn = bn; g.nb = (int)(p.H / bn); g.kb = (int)(p.I / BK);
     g.a_mode = 1; g.a_cap = 0; g.b_rows = p.H; g.mode = 1; g.out_ld = p.H;
     if (em) { g.out = expert_out; g.out_mode = 0; g.out_cap = p.cap; }
     else { g.out = r.ypick; g.out_mode = 1; g.out_cap = 0; }
-    return launch_gemm<true>(mA, mA2, mB, g, max_mblocks(p) * g.nb, s);
+    if (pair) return launch_gemm<true, true>(mA, mA2, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
+    return launch_gemm<true, false>(mA, mA2, mB, g, max_mblocks(p, BM) * g.nb, s);
 }
 
 }  // namespace moe

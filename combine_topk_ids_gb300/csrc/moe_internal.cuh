@@ -22,7 +22,7 @@ struct Plan {
     int tb;         // tokens per routing block
     int nbpr;       // routing blocks per logical rank
     int nb;         // routing blocks in total (W * nbpr)
-    size_t status, counts, offsets, mprefix, pick_pos, pick_src, slot, layout_range,
+    size_t status, counts, offsets, mprefix, mprefix2, pick_pos, pick_src, slot, layout_range,
         blk_hist, blk_base, recv_row, recv_count, num_recv, recv_src, recv_topk_idx,
         recv_topk_w, blk_dhist, blk_dbase, recv_x, act, act_lo, apick, ypick, total;
 };
@@ -33,7 +33,7 @@ int make_plan(const moe_geom &g, Plan *p);
 // Workspace pointers of one dispatch.
 struct Routing {
     const Plan *p;
-    int32_t *status, *counts, *offsets, *mprefix, *pick_pos, *pick_src, *slot, *layout_range,
+    int32_t *status, *counts, *offsets, *mprefix, *mprefix2, *pick_pos, *pick_src, *slot, *layout_range,
         *blk_hist, *blk_base, *recv_row, *recv_count, *num_recv, *recv_src, *recv_topk_idx,
         *blk_dhist, *blk_dbase;
     float *recv_topk_w;

@@ -14,9 +14,9 @@
 namespace moe {
 namespace {
 
-// Per-chunk expert histograms and their exclusive bases ([E][nb] int32 each) plus the
-// m-block prefix ([E+1]): 2*E*nb + E + 1 ints must fit.  Every GPU that loads the library
-// holds this array until the process exits.
+// Per-chunk expert histograms and their exclusive bases ([E][nb] int32 each) plus the two
+// GEMM row-block prefixes ([E+1] each): 2*E*nb + 2*(E+1) ints must fit.  Every GPU that
+// loads the library holds this array until the process exits.
 constexpr size_t kScratchBytes = MOE_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) int32_t g_route_scratch[kScratchBytes / sizeof(int32_t)];
 
@@ -60,9 +60,9 @@ extern "C" int moe_route_noalloc(const moe_geom *g, const void *topk_ids_dev, in
     if (rc != MOE_OK) return rc;
     if (p.T > 0 && (!topk_ids_dev || !pick_pos_dev || !pick_src_dev || !slot_dev))
         return MOE_ERR_INVALID_ARGUMENT;
-    // scratch: blk_hist [E*nb], blk_base [E*nb], mprefix [E+1]
+    // scratch: blk_hist [E*nb], blk_base [E*nb], mprefix [E+1], mprefix2 [E+1]
     const size_t hist_ints = (size_t)p.E * p.nb;
-    const size_t need = 2 * hist_ints + (size_t)p.E + 1;
+    const size_t need = 2 * hist_ints + 2 * ((size_t)p.E + 1);
     if (need * sizeof(int32_t) > kScratchBytes) return MOE_ERR_LIMIT;
 
     int err = MOE_OK;
@@ -81,6 +81,7 @@ extern "C" int moe_route_noalloc(const moe_geom *g, const void *topk_ids_dev, in
     r.blk_hist = scratch;
     r.blk_base = scratch + hist_ints;
     r.mprefix = scratch + 2 * hist_ints;
+    r.mprefix2 = r.mprefix + p.E + 1;
     // every scratch entry the kernels read is written earlier in the same call, so the
     // previous call's contents never need clearing; only the status output starts at 0
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -29,7 +29,7 @@ struct RouteArgs {
     const float *topk_w;
     int T, W, Tr, E, k, Le, layout, tb, nbpr, nb;
     int64_t cap;
-    int32_t *status, *counts, *offsets, *mprefix, *pick_pos, *pick_src, *slot, *layout_range;
+    int32_t *status, *counts, *offsets, *mprefix, *mprefix2, *pick_pos, *pick_src, *slot, *layout_range;
     int32_t *blk_hist, *blk_base;   // [E][nb]
     int32_t *recv_row, *recv_count, *num_recv, *recv_src, *recv_topk_idx;
     int32_t *blk_dhist, *blk_dbase; // [W][nb]
@@ -137,8 +137,8 @@ __device__ __forceinline__ int scan_row(const RouteArgs &a, const int32_t *hist,
 }
 
 __global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
-    __shared__ int wsum[2][32];
-    __shared__ int carry[2];
+    __shared__ int wsum[3][32];
+    __shared__ int carry[3];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
     // (1) per expert: chunk bases, layout ranges, counts (EM clamps to the region size)
@@ -173,37 +173,44 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
         }
     }
     __syncthreads();
-    // (2) expert offsets and m-block (128-row GEMM tile) prefix over experts
-    if (threadIdx.x == 0) carry[0] = carry[1] = 0;
+    // (2) expert offsets and the prefixes of GEMM row blocks (128-row tiles of one SM,
+    //     256-row tiles of an SM pair) over experts
+    if (threadIdx.x == 0) carry[0] = carry[1] = carry[2] = 0;
     __syncthreads();
     for (int e0 = 0; e0 < a.E; e0 += blockDim.x) {
         int e = e0 + threadIdx.x;
-        int c = e < a.E ? a.counts[e] : 0;
-        int m = (c + kTileM - 1) / kTileM;
-        int ic = warp_incl_scan(c), im = warp_incl_scan(m);
-        if (lane == 31) { wsum[0][warp] = ic; wsum[1][warp] = im; }
+        int v[3];
+        v[0] = e < a.E ? a.counts[e] : 0;
+        v[1] = (v[0] + kTileM - 1) / kTileM;
+        v[2] = (v[0] + 2 * kTileM - 1) / (2 * kTileM);
+        int inc[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) inc[q] = warp_incl_scan(v[q]);
+        if (lane == 31)
+            for (int q = 0; q < 3; ++q) wsum[q][warp] = inc[q];
         __syncthreads();
         if (warp == 0) {
-            int v0 = lane < nwarps ? wsum[0][lane] : 0, v1 = lane < nwarps ? wsum[1][lane] : 0;
-            int s0 = warp_incl_scan(v0), s1 = warp_incl_scan(v1);
-            wsum[0][lane] = s0 - v0;
-            wsum[1][lane] = s1 - v1;
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+                int w = lane < nwarps ? wsum[q][lane] : 0;
+                wsum[q][lane] = warp_incl_scan(w) - w;
+            }
         }
         __syncthreads();
         if (e < a.E) {
-            a.offsets[e] = carry[0] + wsum[0][warp] + ic - c;
-            a.mprefix[e] = carry[1] + wsum[1][warp] + im - m;
+            a.offsets[e] = carry[0] + wsum[0][warp] + inc[0] - v[0];
+            a.mprefix[e] = carry[1] + wsum[1][warp] + inc[1] - v[1];
+            a.mprefix2[e] = carry[2] + wsum[2][warp] + inc[2] - v[2];
         }
         __syncthreads();
-        if (threadIdx.x == blockDim.x - 1) {
-            carry[0] += wsum[0][warp] + ic;
-            carry[1] += wsum[1][warp] + im;
-        }
+        if (threadIdx.x == blockDim.x - 1)
+            for (int q = 0; q < 3; ++q) carry[q] += wsum[q][warp] + inc[q];
         __syncthreads();
     }
     if (threadIdx.x == 0) {
         a.offsets[a.E] = carry[0];
         a.mprefix[a.E] = carry[1];
+        a.mprefix2[a.E] = carry[2];
     }
 }
 
@@ -322,6 +329,211 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(RouteArgs a
     }
 }
 
+
+// ---------------------------------------------------------------------------------------
+// Small batches: the three steps above in one CTA of 32 warps, everything in shared memory
+// (one launch instead of three; decode-sized batches are launch-latency bound).  Same
+// deterministic scheme: each warp owns a contiguous run of picks (and of tokens), counts
+// it, takes an exclusive prefix over the warps, then ranks its run 32 at a time.  Per
+// (expert, source rank) and (destination, source rank) counts come from shared-memory
+// atomics (counts only).  RANK_MAJOR rows are derived from the token's rank among all
+// tokens received by the destination minus those of earlier source ranks.
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedWarps = kFusedThreads / 32;
+
+// Exclusive scan of three values per thread across a 1024-thread block.
+__device__ __forceinline__ void block_excl_scan3(const int (&v)[3], int (&ex)[3], int (*wsum)[32]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) inc[q] = warp_incl_scan(v[q]);
+    if (lane == 31)
+        for (int q = 0; q < 3; ++q) wsum[q][warp] = inc[q];
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            int w = wsum[q][lane];
+            wsum[q][lane] = warp_incl_scan(w) - w;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 3; ++q) ex[q] = wsum[q][warp] + inc[q] - v[q];
+}
+
+__global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a) {
+    extern __shared__ int sm[];
+    __shared__ int wsum[3][32];
+    const int E = a.E, W = a.W;
+    int *cur = sm;                          // [warps][E]
+    int *dcur = cur + kFusedWarps * E;      // [warps][W]
+    int *ew = dcur + kFusedWarps * W;       // [E][W]  kept picks per (expert, source rank)
+    int *dw = ew + E * W;                   // [W][W]  tokens per (destination, source rank)
+    int *off = dw + W * W;                  // [E]     expert offsets
+    int *cnt = off + E;                     // [E]     kept counts
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    const int total_sm = kFusedWarps * (E + W) + E * W + W * W + 2 * E;
+    for (int i = threadIdx.x; i < total_sm; i += blockDim.x) sm[i] = 0;
+    const int64_t P = (int64_t)a.T * a.k;
+    const int64_t ppw = (P + kFusedWarps * 32 - 1) / (kFusedWarps * 32) * 32;
+    const int64_t wp0 = min(warp * ppw, P), wp1 = min(wp0 + ppw, P);
+    const int tpw = (a.T + kFusedWarps * 32 - 1) / (kFusedWarps * 32) * 32;
+    const int wt0 = min(warp * tpw, a.T), wt1 = min(wt0 + tpw, a.T);
+    __syncthreads();
+    // pass 1: counts
+    bool bad = false;
+    for (int64_t i0 = wp0; i0 < wp1; i0 += 32) {
+        int64_t i = i0 + lane;
+        int e = i < wp1 ? load_id(a, i) : -1;
+        if (e == -2) bad = true;
+        int key = e >= 0 ? e : -1;
+        unsigned peers = __match_any_sync(kFull, key);
+        if (key >= 0 && lane == __ffs(peers) - 1) cur[warp * E + key] += __popc(peers);
+        __syncwarp();
+    }
+    if (bad) atomicOr(a.status, MOE_STATUS_BAD_EXPERT_ID);
+    if (!em) {
+        for (int tt = wt0; tt < wt1; tt += 32) {
+            int t = tt + lane;
+            unsigned long long m = t < wt1 ? dest_mask(a, t) : 0ull;
+            for (int d = 0; d < W; ++d) {
+                bool has = (m >> d) & 1ull;
+                unsigned bal = __ballot_sync(kFull, has);
+                if (lane == 0) dcur[warp * W + d] += __popc(bal);
+                if (has) atomicAdd(&dw[d * W + t / a.Tr], 1);
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // per expert: exclusive prefix over warps; kept count (EM clamps to the region)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < kFusedWarps; ++w) {
+            int c = cur[w * E + e];
+            cur[w * E + e] = run;
+            run += c;
+        }
+        int kept = (em && run > a.cap) ? (int)a.cap : run;
+        cnt[e] = kept;
+        a.counts[e] = kept;
+    }
+    // per destination: exclusive prefix over warps (rank among all tokens it receives),
+    // received counts per source rank, and their exclusive prefix over source ranks
+    if (!em) {
+        for (int d = threadIdx.x; d < W; d += blockDim.x) {
+            int run = 0;
+            for (int w = 0; w < kFusedWarps; ++w) {
+                int c = dcur[w * W + d];
+                dcur[w * W + d] = run;
+                run += c;
+            }
+            a.num_recv[d] = run;
+            int b = 0;
+            for (int s2 = 0; s2 < W; ++s2) {
+                int c = dw[d * W + s2];
+                a.recv_count[d * W + s2] = c;
+                dw[d * W + s2] = b;
+                b += c;
+            }
+        }
+    }
+    __syncthreads();
+    // expert offsets and the 128 / 256-row block prefixes (E <= blockDim.x here)
+    {
+        int e = threadIdx.x;
+        int v[3], ex[3];
+        v[0] = e < E ? cnt[e] : 0;
+        v[1] = (v[0] + kTileM - 1) / kTileM;
+        v[2] = (v[0] + 2 * kTileM - 1) / (2 * kTileM);
+        block_excl_scan3(v, ex, wsum);
+        if (e < E) {
+            off[e] = ex[0];
+            a.offsets[e] = ex[0];
+            a.mprefix[e] = ex[1];
+            a.mprefix2[e] = ex[2];
+        }
+        if (threadIdx.x == blockDim.x - 1) {
+            a.offsets[E] = ex[0] + v[0];
+            a.mprefix[E] = ex[1] + v[1];
+            a.mprefix2[E] = ex[2] + v[2];
+        }
+    }
+    __syncthreads();
+    // pass 2: positions of the picks
+    bool overflow = false;
+    for (int64_t i0 = wp0; i0 < wp1; i0 += 32) {
+        int64_t i = i0 + lane;
+        int e = i < wp1 ? load_id(a, i) : -1;
+        int key = e >= 0 ? e : -1;
+        unsigned peers = __match_any_sync(kFull, key);
+        int pos = key >= 0 ? cur[warp * E + key] + __popc(peers & lanemask_lt()) : 0;
+        __syncwarp();
+        if (key >= 0 && lane == __ffs(peers) - 1) cur[warp * E + key] += __popc(peers);
+        __syncwarp();
+        if (i < wp1) {
+            int pp = -1, sl = -1;
+            if (key >= 0) {
+                if (pos < cnt[key]) {
+                    pp = off[key] + pos;
+                    sl = (int)((int64_t)key * a.cap + pos);
+                    a.pick_src[pp] = (int)i;
+                    atomicAdd(&ew[key * W + (int)(i / a.k) / a.Tr], 1);
+                } else {
+                    overflow = true;
+                }
+            }
+            a.pick_pos[i] = pp;
+            if (em) a.slot[i] = sl;
+        }
+    }
+    if (overflow) atomicOr(a.status, MOE_STATUS_EM_OVERFLOW);
+    // layout ranges of the kept picks
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int b = 0;
+        for (int r = 0; r < W; ++r) {
+            int c = ew[e * W + r];
+            a.layout_range[((int64_t)e * W + r) * 2 + 0] = b;
+            a.layout_range[((int64_t)e * W + r) * 2 + 1] = c;
+            b += c;
+        }
+    }
+    if (em) return;
+    // destinations: rows, source tokens, local ids and weights
+    for (int tt = wt0; tt < wt1; tt += 32) {
+        int t = tt + lane;
+        bool valid = t < wt1;
+        unsigned long long m = valid ? dest_mask(a, t) : 0ull;
+        for (int d = 0; d < W; ++d) {
+            bool has = (m >> d) & 1ull;
+            unsigned bal = __ballot_sync(kFull, has);
+            int flat = dcur[warp * W + d] + __popc(bal & lanemask_lt());
+            __syncwarp();
+            if (lane == 0) dcur[warp * W + d] += __popc(bal);
+            __syncwarp();
+            if (!valid) continue;
+            if (!has) {
+                a.recv_row[(int64_t)t * W + d] = -1;
+                continue;
+            }
+            const int s2 = t / a.Tr;
+            const int row = a.layout == MOE_LAYOUT_RANK_MAJOR ? s2 * a.Tr + flat - dw[d * W + s2] : flat;
+            a.recv_row[(int64_t)t * W + d] = row;
+            int64_t o = (int64_t)d * a.cap + row;
+            a.recv_src[o] = t;
+            for (int j = 0; j < a.k; ++j) {
+                int ej = load_id(a, (int64_t)t * a.k + j);
+                bool local = ej >= 0 && ej / a.Le == d;
+                a.recv_topk_idx[o * a.k + j] = local ? ej - d * a.Le : -1;
+                a.recv_topk_w[o * a.k + j] = local ? a.topk_w[(int64_t)t * a.k + j] : 0.0f;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const float *topk_w,
@@ -337,11 +549,25 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
     a.tb = p.tb; a.nbpr = p.nbpr; a.nb = p.nb;
     a.cap = p.cap;
     a.status = r.status; a.counts = r.counts; a.offsets = r.offsets; a.mprefix = r.mprefix;
+    a.mprefix2 = r.mprefix2;
     a.pick_pos = r.pick_pos; a.pick_src = r.pick_src; a.slot = r.slot;
     a.layout_range = r.layout_range; a.blk_hist = r.blk_hist; a.blk_base = r.blk_base;
     a.recv_row = r.recv_row; a.recv_count = r.recv_count; a.num_recv = r.num_recv;
     a.recv_src = r.recv_src; a.recv_topk_idx = r.recv_topk_idx; a.recv_topk_w = r.recv_topk_w;
     a.blk_dhist = r.blk_dhist; a.blk_dbase = r.blk_dbase;
+
+    // one fused CTA for small batches (bounded shared memory: E <= 512, E*W <= 4096)
+    if (p.P <= 16384 && a.E <= 512 && a.E * a.W <= 4096) {
+        const size_t smf = (size_t)(kFusedWarps * (a.E + a.W) + a.E * a.W + a.W * a.W + 2 * a.E) *
+                           sizeof(int);
+        if (smf > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(route_fused_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf);
+            if (e != cudaSuccess) return e;
+        }
+        route_fused_kernel<<<1, kFusedThreads, smf, s>>>(a);
+        return cudaGetLastError();
+    }
 
     size_t sm1 = (size_t)(a.E + a.W) * sizeof(int);
     route_count_kernel<<<a.nb, kRouteThreads, sm1, s>>>(a);

@@ -72,6 +72,28 @@ SMALL = {
                             layout="FLAT", algo="HT", routing="uniform", T=350),
 }
 
+# Shapes with many rows per expert (>= 192 on average), which take the two-SM GEMM tiles
+# (256 rows per tile), still small enough for the oracle; ragged tails in every expert.
+SMALL.update({
+    "pair_em": MoeConfig("pair_em", W=2, Tr=384, H=512, E=4, k=2, I=384,
+                         layout="EM", algo="LL", routing="uniform", T=700),
+    "pair_rm": MoeConfig("pair_rm", W=2, Tr=384, H=384, E=4, k=2, I=256,
+                         layout="RM", algo="LL", routing="zipf", T=700),
+    "pair_flat": MoeConfig("pair_flat", W=2, Tr=384, H=512, E=4, k=3, I=384,
+                           layout="FLAT", algo="HT", routing="uniform", T=700),
+})
+
+# Batches above the single-CTA routing limit (16384 picks), which take the three-kernel
+# multi-block routing path; narrow H and I keep the oracle fast.
+SMALL.update({
+    "blocks_em": MoeConfig("blocks_em", W=4, Tr=1100, H=256, E=16, k=4, I=128,
+                           layout="EM", algo="HT", routing="dirichlet", T=4300),
+    "blocks_rm": MoeConfig("blocks_rm", W=4, Tr=1100, H=256, E=16, k=4, I=128,
+                           layout="RM", algo="LL", routing="zipf", T=4300),
+    "blocks_flat": MoeConfig("blocks_flat", W=4, Tr=1100, H=256, E=16, k=4, I=128,
+                             layout="FLAT", algo="HT", routing="uniform", T=4300, mask_frac=0.1),
+})
+
 ALL = {**CONFIGS, **SMALL}
 
 # A smaller EXPERT_MAJOR case for detailed (multi-pass) profiler captures of the same

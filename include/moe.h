@@ -261,7 +261,7 @@ int moe_get_status(const moe_handle *h, int32_t *status_host, void *stream);
  *   cleared by the call).  No rows are copied.
  *   Scratch: a static device array of MOE_NOALLOC_SCRATCH_BYTES compiled into the library
  *   (held by every GPU that loads it until the process exits).  The routing needs
- *   (2 * E * nb + E + 1) * 4 bytes of it, nb being the routing chunk count of the geometry
+ *   (2 * E * nb + 2 * E + 2) * 4 bytes of it, nb being the routing chunk count of the geometry
  *   (about 256 for large batches); a larger geometry returns MOE_ERR_LIMIT.
  *   The first call on each device looks the array's address up (cudaGetSymbolAddress)
  *   with that device current; make that first call before any stream capture.

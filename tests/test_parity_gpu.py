@@ -24,6 +24,15 @@ SMALL_CASES = {
     "small_em_h384": gen.SMALL["small_em"].with_(H=384, seed=6),          # 128-wide GEMM2 tiles
     "small_flat_w1": gen.SMALL["small_flat"].with_(W=1, Tr=350, seed=7),  # one logical rank
     "small_rm_w8": gen.SMALL["small_rm"].with_(W=8, Tr=48, T=380, E=16, seed=8),
+    # two-SM GEMM tiles (many rows per expert)
+    "pair_em": gen.SMALL["pair_em"],
+    "pair_rm_h384": gen.SMALL["pair_rm"],
+    "pair_flat": gen.SMALL["pair_flat"],
+    "pair_em_masked_i32": gen.SMALL["pair_em"].with_(mask_frac=0.2, ids_dtype="int32", seed=9),
+    # multi-block routing (more than 16384 picks)
+    "blocks_em": gen.SMALL["blocks_em"],
+    "blocks_rm": gen.SMALL["blocks_rm"],
+    "blocks_flat": gen.SMALL["blocks_flat"],
 }
 
 
@@ -47,7 +56,7 @@ def test_layer_parity_small(name):
     check_out(layer, case)
 
 
-@pytest.mark.parametrize("name", ["small_em", "small_rm", "small_flat"])
+@pytest.mark.parametrize("name", ["small_em", "small_rm", "small_flat", "pair_em", "pair_flat"])
 def test_deterministic(name):
     cfg = SMALL_CASES[name]
     case = make_case(cfg, "cuda")
