@@ -343,7 +343,7 @@ def run_ours(args, cfg, rank, world, dist):
                "sample": "first %d of %d tokens (full routing; FFN + combine of the sample), best of %d"
                          % (n, cfg.tokens, reps)}
 
-    per_step = 7 if cfg.layout == "EM" else 9
+    per_step = moe.moe_launches_per_layer(layer.geom)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "ours",

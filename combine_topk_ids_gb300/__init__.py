@@ -71,6 +71,8 @@ def lib():
         L.moe_get_status.argtypes = [H, ctypes.POINTER(ctypes.c_int32), _P]
         L.moe_forward_host.argtypes = [G, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                        _P, ctypes.c_size_t, H, _P]
+        L.moe_launches_per_layer.argtypes = [G, ctypes.POINTER(ctypes.c_int32)]
+        L.moe_launches_per_layer.restype = ctypes.c_int
         L.moe_route_noalloc.argtypes = [G, _P, ctypes.c_int] + [_P] * 8
         L.moe_route_noalloc.restype = ctypes.c_int
         L.moe_strerror.argtypes = [ctypes.c_int]
@@ -167,6 +169,12 @@ def moe_route_noalloc(g, topk_ids, counts, offsets, pick_pos, pick_src, slot, la
                                    _ptr(offsets), _ptr(pick_pos), _ptr(pick_src), _ptr(slot),
                                    _ptr(layout_range), _ptr(status), _stream(stream)),
            "moe_route_noalloc")
+
+
+def moe_launches_per_layer(g) -> int:
+    n = ctypes.c_int32()
+    _check(lib().moe_launches_per_layer(ctypes.byref(g), ctypes.byref(n)), "moe_launches_per_layer")
+    return n.value
 
 
 def moe_get_status(h, stream=None) -> int:

@@ -341,6 +341,22 @@ int moe_get_status(const moe_handle *h, int32_t *status_host, void *stream) {
     return MOE_OK;
 }
 
+int moe_launches_per_layer(const moe_geom *g, int32_t *n) {
+    if (!g || !n) return MOE_ERR_INVALID_ARGUMENT;
+    Plan p;
+    int rc = make_plan(*g, &p);
+    if (rc != MOE_OK) return rc;
+    if (p.T == 0) {
+        *n = routing_launches(p);
+        return MOE_OK;
+    }
+    const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    // routing, row scatter, (RM/FLAT pick gather), GEMM1, GEMM2, (RM/FLAT local-pick
+    // reduction), combine
+    *n = routing_launches(p) + 1 + (em ? 0 : 1) + 2 + (em ? 0 : 1) + 1;
+    return MOE_OK;
+}
+
 const char *moe_strerror(int err) {
     switch (err) {
     case MOE_OK: return "ok";

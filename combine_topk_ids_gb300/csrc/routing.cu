@@ -536,6 +536,10 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a)
 
 }  // namespace
 
+int routing_launches(const Plan &p) {
+    return (p.P <= 16384 && p.E <= 512 && p.E * p.W <= 4096) ? 1 : 3;
+}
+
 cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const float *topk_w,
                            cudaStream_t s) {
     const Plan &p = *r.p;
@@ -557,7 +561,7 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
     a.blk_dhist = r.blk_dhist; a.blk_dbase = r.blk_dbase;
 
     // one fused CTA for small batches (bounded shared memory: E <= 512, E*W <= 4096)
-    if (p.P <= 16384 && a.E <= 512 && a.E * a.W <= 4096) {
+    if (routing_launches(p) == 1) {
         const size_t smf = (size_t)(kFusedWarps * (a.E + a.W) + a.E * a.W + a.W * a.W + 2 * a.E) *
                            sizeof(int);
         if (smf > 48 * 1024) {

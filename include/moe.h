@@ -277,6 +277,14 @@ int moe_route_noalloc(const moe_geom *g, const void *topk_ids_dev, int ids_dtype
                       int32_t *pick_src_dev, int32_t *slot_dev, int32_t *layout_range_dev,
                       int32_t *status_dev, void *stream);
 
+/*
+ * moe_launches_per_layer - number of kernels one moe_dispatch + moe_expert_ffn +
+ * moe_combine of geometry *g queues (routing is one kernel for batches of at most 16384
+ * picks and three above; RANK_MAJOR / FLAT add the pick-row gather and the local-pick
+ * reduction).  Written to *n.
+ */
+int moe_launches_per_layer(const moe_geom *g, int32_t *n);
+
 /* moe_strerror - static text for a moe_error code. */
 const char *moe_strerror(int err);
 
