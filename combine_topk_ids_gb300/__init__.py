@@ -17,7 +17,7 @@ from .build import LIB_PATH, build  # noqa: F401
 LAYOUT = {"EM": 0, "RM": 1, "FLAT": 2}
 ALGO = {"LL": 0, "HT": 1}
 IDS_INT32, IDS_INT64 = 0, 1
-STATUS_BAD_EXPERT_ID, STATUS_EM_OVERFLOW, STATUS_TIMEOUT = 0x1, 0x2, 0x4
+STATUS_BAD_EXPERT_ID, STATUS_EM_OVERFLOW, STATUS_TIMEOUT, STATUS_INACTIVE_RANK = 0x1, 0x2, 0x4, 0x8
 
 
 class MoeGeom(ctypes.Structure):
@@ -64,7 +64,7 @@ def lib():
         sz = ctypes.POINTER(ctypes.c_size_t)
         L.moe_workspace_size.argtypes = [G, sz]
         L.moe_expert_out_size.argtypes = [G, sz]
-        L.moe_dispatch.argtypes = [G, _P, _P, ctypes.c_int, _P, _P, ctypes.c_size_t, H, _P]
+        L.moe_dispatch.argtypes = [G, _P, _P, ctypes.c_int, _P, _P, _P, ctypes.c_size_t, H, _P]
         L.moe_prepare_weights.argtypes = [G, _P, _P, _P]
         L.moe_expert_ffn.argtypes = [H, _P, _P, _P, _P]
         L.moe_combine.argtypes = [H, _P, _P, _P, _P]
@@ -126,12 +126,15 @@ def _ids_dtype(t):
     return {torch.int64: IDS_INT64, torch.int32: IDS_INT32}.get(t.dtype, 99)
 
 
-def moe_dispatch(g, x, topk_ids, topk_weights, workspace, stream=None, handle=None) -> MoeHandle:
-    """handle: optional MoeHandle to fill (its events fields are kept)."""
+def moe_dispatch(g, x, topk_ids, topk_weights, workspace, stream=None, handle=None,
+                 active_ranks=None) -> MoeHandle:
+    """handle: optional MoeHandle to fill (its events fields are kept).  active_ranks: optional
+    int32 [W] device tensor, 0 = failed logical rank."""
     h = MoeHandle() if handle is None else handle
     ids_dtype = _ids_dtype(topk_ids)
     _check(lib().moe_dispatch(ctypes.byref(g), _ptr(x), _ptr(topk_ids), ids_dtype,
-                              _ptr(topk_weights), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _ptr(topk_weights), _ptr(active_ranks), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(),
                               ctypes.byref(h), _stream(stream)), "moe_dispatch")
     return h
 
@@ -253,8 +256,9 @@ class MoELayer1GPU:
         moe_prepare_weights(self.geom, w1, self.w1p)
         self.w2 = w2
 
-    def dispatch(self, x, topk_ids, topk_weights):
-        moe_dispatch(self.geom, x, topk_ids, topk_weights, self.workspace, handle=self.handle)
+    def dispatch(self, x, topk_ids, topk_weights, active_ranks=None):
+        moe_dispatch(self.geom, x, topk_ids, topk_weights, self.workspace, handle=self.handle,
+                     active_ranks=active_ranks)
         return self.handle
 
     def expert_ffn(self):
@@ -265,8 +269,8 @@ class MoELayer1GPU:
         moe_combine(self.handle, self.expert_out, topk_weights, self.out)
         return self.out
 
-    def forward(self, x, topk_ids, topk_weights):
-        self.dispatch(x, topk_ids, topk_weights)
+    def forward(self, x, topk_ids, topk_weights, active_ranks=None):
+        self.dispatch(x, topk_ids, topk_weights, active_ranks)
         self.expert_ffn()
         return self.combine(topk_weights)
 

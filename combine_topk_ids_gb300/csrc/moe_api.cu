@@ -176,8 +176,8 @@ int moe_expert_out_size(const moe_geom *g, size_t *bytes) {
 }
 
 int moe_dispatch(const moe_geom *g, const void *x_dev, const void *topk_ids_dev, int ids_dtype,
-                 const float *topk_weights_dev, void *workspace_dev, size_t workspace_bytes,
-                 moe_handle *h, void *stream) {
+                 const float *topk_weights_dev, const int32_t *active_ranks_dev, void *workspace_dev,
+                 size_t workspace_bytes, moe_handle *h, void *stream) {
     if (!g || !h || !workspace_dev) return MOE_ERR_INVALID_ARGUMENT;
     if (ids_dtype != MOE_IDS_INT32 && ids_dtype != MOE_IDS_INT64) return MOE_ERR_IDS_DTYPE;
     Plan p;
@@ -188,7 +188,8 @@ int moe_dispatch(const moe_geom *g, const void *x_dev, const void *topk_ids_dev,
         return MOE_ERR_INVALID_ARGUMENT;
     if (!aligned(workspace_dev, 256) || (x_dev && !aligned(x_dev, 16)) ||
         (topk_ids_dev && !aligned(topk_ids_dev, ids_dtype == MOE_IDS_INT64 ? 8 : 4)) ||
-        (topk_weights_dev && !aligned(topk_weights_dev, 4)))
+        (topk_weights_dev && !aligned(topk_weights_dev, 4)) ||
+        (active_ranks_dev && !aligned(active_ranks_dev, 4)))
         return MOE_ERR_MISALIGNED;
     if (workspace_bytes < p.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if ((rc = check_device()) != MOE_OK) return rc;
@@ -222,8 +223,8 @@ int moe_dispatch(const moe_geom *g, const void *x_dev, const void *topk_ids_dev,
 
     record(h, MOE_EV_DISPATCH_BEGIN, s);
     if (cudaMemsetAsync(r.status, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_routing(r, topk_ids_dev, ids_dtype == MOE_IDS_INT64, topk_weights_dev, s) !=
-        cudaSuccess)
+    if (launch_routing(r, topk_ids_dev, ids_dtype == MOE_IDS_INT64, topk_weights_dev,
+                       active_ranks_dev, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     record(h, MOE_EV_ROUTING_END, s);
     if (launch_dispatch_copy(r, static_cast<const uint16_t *>(x_dev), s) != cudaSuccess)
@@ -317,8 +318,8 @@ int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids
                 cudaSuccess)
             return MOE_ERR_CUDA;
     }
-    if ((rc = moe_dispatch(g, x_dev, topk_ids_dev, ids_dtype, topk_weights_dev, workspace_dev,
-                           workspace_bytes, h, stream)) != MOE_OK)
+    if ((rc = moe_dispatch(g, x_dev, topk_ids_dev, ids_dtype, topk_weights_dev, nullptr,
+                           workspace_dev, workspace_bytes, h, stream)) != MOE_OK)
         return rc;
     if ((rc = moe_expert_ffn(h, w1_prepared_dev, w2_dev, expert_out_dev, stream)) != MOE_OK) return rc;
     if ((rc = moe_combine(h, expert_out_dev, topk_weights_dev, out_dev, stream)) != MOE_OK) return rc;

@@ -45,7 +45,7 @@ Routing carve(const Plan &p, void *ws);
 
 // ---- launchers (return cudaGetLastError of the launch) -------------------------------
 cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const float *topk_w,
-                           cudaStream_t s);
+                           const int32_t *active, cudaStream_t s);
 int routing_launches(const Plan &p);   // kernels launch_routing queues for this geometry
 cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream_t s);
 cudaError_t launch_gather_picks(const Routing &r, cudaStream_t s);

@@ -86,7 +86,8 @@ extern "C" int moe_route_noalloc(const moe_geom *g, const void *topk_ids_dev, in
     // previous call's contents never need clearing; only the status output starts at 0
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(status_dev, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
-    return launch_routing(r, topk_ids_dev, ids_dtype == MOE_IDS_INT64, nullptr, s) == cudaSuccess
+    return launch_routing(r, topk_ids_dev, ids_dtype == MOE_IDS_INT64, nullptr, nullptr, s) ==
+                   cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
 }

@@ -27,6 +27,7 @@ struct RouteArgs {
     const void *ids;
     int ids64;
     const float *topk_w;
+    const int32_t *active;          // EP rank-health mask [W] (NULL: all ranks active)
     int T, W, Tr, E, k, Le, layout, tb, nbpr, nb;
     int64_t cap;
     int32_t *status, *counts, *offsets, *mprefix, *mprefix2, *pick_pos, *pick_src, *slot, *layout_range;
@@ -36,20 +37,33 @@ struct RouteArgs {
     float *recv_topk_w;
 };
 
-// Expert id of pick i: [0, E) valid, -1 masked, -2 outside [-1, E).
-__device__ __forceinline__ int load_id(const RouteArgs &a, int64_t i) {
+// Bit r set iff logical rank r is active (Mooncake EP active_ranks: 0 = failed rank).
+// Read once per block into shared memory by the caller.
+__device__ __forceinline__ unsigned long long load_active_mask(const RouteArgs &a) {
+    unsigned long long m = 0;
+    for (int r = 0; r < a.W; ++r)
+        if (!a.active || a.active[r] != 0) m |= 1ull << r;
+    return m;
+}
+
+// Expert id of pick i: [0, E) valid, -1 masked, -2 outside [-1, E), -3 dropped because its
+// expert's rank or its token's source rank is inactive.
+__device__ __forceinline__ int load_id(const RouteArgs &a, int64_t i, unsigned long long act) {
     long long v = a.ids64 ? reinterpret_cast<const long long *>(a.ids)[i]
                           : (long long)reinterpret_cast<const int *>(a.ids)[i];
     if (v == -1) return -1;
     if (v < -1 || v >= a.E) return -2;
+    const int src = (int)(i / a.k) / a.Tr;
+    if (!((act >> ((int)v / a.Le)) & 1ull) || !((act >> src) & 1ull)) return -3;
     return (int)v;
 }
 
 // Bit d set iff token t has a valid pick on destination rank d.
-__device__ __forceinline__ unsigned long long dest_mask(const RouteArgs &a, int t) {
+__device__ __forceinline__ unsigned long long dest_mask(const RouteArgs &a, int t,
+                                                        unsigned long long act) {
     unsigned long long m = 0;
     for (int j = 0; j < a.k; ++j) {
-        int e = load_id(a, (int64_t)t * a.k + j);
+        int e = load_id(a, (int64_t)t * a.k + j, act);
         if (e >= 0) m |= 1ull << (e / a.Le);
     }
     return m;
@@ -83,19 +97,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_count_kernel(RouteArgs a)
     extern __shared__ int sm[];
     int *hist = sm;          // [E]
     int *dhist = sm + a.E;   // [W]
+    __shared__ unsigned long long s_act;
+    if (threadIdx.x == 0) s_act = load_active_mask(a);
     for (int i = threadIdx.x; i < a.E + a.W; i += blockDim.x) sm[i] = 0;
     __syncthreads();
+    const unsigned long long act = s_act;
     int t0, t1;
     block_tokens(a, blockIdx.x, t0, t1);
-    bool bad = false;
+    bool bad = false, inactive = false;
     for (int64_t i = (int64_t)t0 * a.k + threadIdx.x; i < (int64_t)t1 * a.k; i += blockDim.x) {
-        int e = load_id(a, i);
+        int e = load_id(a, i, act);
         if (e >= 0) atomicAdd(&hist[e], 1);   // counts only; positions come later
         else if (e == -2) bad = true;
+        else if (e == -3) inactive = true;
     }
     if (a.layout != MOE_LAYOUT_EXPERT_MAJOR) {
         for (int t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
-            unsigned long long m = dest_mask(a, t);
+            unsigned long long m = dest_mask(a, t, act);
             while (m) {
                 int d = __ffsll((long long)m) - 1;
                 m &= m - 1;
@@ -104,6 +122,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_count_kernel(RouteArgs a)
         }
     }
     if (bad) atomicOr(a.status, MOE_STATUS_BAD_EXPERT_ID);
+    if (inactive) atomicOr(a.status, MOE_STATUS_INACTIVE_RANK);
     __syncthreads();
     for (int e = threadIdx.x; e < a.E; e += blockDim.x)
         a.blk_hist[(int64_t)e * a.nb + blockIdx.x] = hist[e];
@@ -218,6 +237,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(RouteArgs a
     extern __shared__ int sm[];
     int *cur = sm;                          // [warps][E] running position inside expert
     int *dcur = sm + kRouteWarps * a.E;     // [warps][W] running row inside destination
+    __shared__ unsigned long long s_act;
+    if (threadIdx.x == 0) s_act = load_active_mask(a);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, b = blockIdx.x;
     const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
     for (int i = threadIdx.x; i < kRouteWarps * (a.E + a.W); i += blockDim.x) sm[i] = 0;
@@ -230,10 +251,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(RouteArgs a
     const int tpw = ((t1 - t0) + kRouteWarps * 32 - 1) / (kRouteWarps * 32) * 32;
     const int wt0 = min(t0 + warp * tpw, t1), wt1 = min(wt0 + tpw, t1);
     __syncthreads();
+    const unsigned long long act = s_act;
     // pass 1: per-warp counts
     for (int64_t i0 = wp0; i0 < wp1; i0 += 32) {
         int64_t i = i0 + lane;
-        int e = i < wp1 ? load_id(a, i) : -1;
+        int e = i < wp1 ? load_id(a, i, act) : -1;
         int key = e >= 0 ? e : -1;
         unsigned peers = __match_any_sync(kFull, key);
         if (key >= 0 && lane == __ffs(peers) - 1) cur[warp * a.E + key] += __popc(peers);
@@ -242,7 +264,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(RouteArgs a
     if (!em) {
         for (int tt = wt0; tt < wt1; tt += 32) {
             int t = tt + lane;
-            unsigned long long m = t < wt1 ? dest_mask(a, t) : 0ull;
+            unsigned long long m = t < wt1 ? dest_mask(a, t, act) : 0ull;
             for (int d = 0; d < a.W; ++d) {
                 unsigned bal = __ballot_sync(kFull, (m >> d) & 1ull);
                 if (lane == 0) dcur[warp * a.W + d] += __popc(bal);
@@ -275,7 +297,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(RouteArgs a
     bool overflow = false;
     for (int64_t i0 = wp0; i0 < wp1; i0 += 32) {
         int64_t i = i0 + lane;
-        int e = i < wp1 ? load_id(a, i) : -1;
+        int e = i < wp1 ? load_id(a, i, act) : -1;
         int key = e >= 0 ? e : -1;
         unsigned peers = __match_any_sync(kFull, key);
         int pos = key >= 0 ? cur[warp * a.E + key] + __popc(peers & lanemask_lt()) : 0;
@@ -303,7 +325,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(RouteArgs a
     for (int tt = wt0; tt < wt1; tt += 32) {
         int t = tt + lane;
         bool valid = t < wt1;
-        unsigned long long m = valid ? dest_mask(a, t) : 0ull;
+        unsigned long long m = valid ? dest_mask(a, t, act) : 0ull;
         for (int d = 0; d < a.W; ++d) {
             bool has = (m >> d) & 1ull;
             unsigned bal = __ballot_sync(kFull, has);
@@ -320,7 +342,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(RouteArgs a
             int64_t o = (int64_t)d * a.cap + row;
             a.recv_src[o] = t;
             for (int j = 0; j < a.k; ++j) {
-                int ej = load_id(a, (int64_t)t * a.k + j);
+                int ej = load_id(a, (int64_t)t * a.k + j, act);
                 bool local = ej >= 0 && ej / a.Le == d;
                 a.recv_topk_idx[o * a.k + j] = local ? ej - d * a.Le : -1;
                 a.recv_topk_w[o * a.k + j] = local ? a.topk_w[(int64_t)t * a.k + j] : 0.0f;
@@ -372,6 +394,8 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a)
     int *dw = ew + E * W;                   // [W][W]  tokens per (destination, source rank)
     int *off = dw + W * W;                  // [E]     expert offsets
     int *cnt = off + E;                     // [E]     kept counts
+    __shared__ unsigned long long s_act;
+    if (threadIdx.x == 0) s_act = load_active_mask(a);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
     const int total_sm = kFusedWarps * (E + W) + E * W + W * W + 2 * E;
@@ -382,22 +406,25 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a)
     const int tpw = (a.T + kFusedWarps * 32 - 1) / (kFusedWarps * 32) * 32;
     const int wt0 = min(warp * tpw, a.T), wt1 = min(wt0 + tpw, a.T);
     __syncthreads();
+    const unsigned long long act = s_act;
     // pass 1: counts
-    bool bad = false;
+    bool bad = false, inactive = false;
     for (int64_t i0 = wp0; i0 < wp1; i0 += 32) {
         int64_t i = i0 + lane;
-        int e = i < wp1 ? load_id(a, i) : -1;
+        int e = i < wp1 ? load_id(a, i, act) : -1;
         if (e == -2) bad = true;
+        if (e == -3) inactive = true;
         int key = e >= 0 ? e : -1;
         unsigned peers = __match_any_sync(kFull, key);
         if (key >= 0 && lane == __ffs(peers) - 1) cur[warp * E + key] += __popc(peers);
         __syncwarp();
     }
     if (bad) atomicOr(a.status, MOE_STATUS_BAD_EXPERT_ID);
+    if (inactive) atomicOr(a.status, MOE_STATUS_INACTIVE_RANK);
     if (!em) {
         for (int tt = wt0; tt < wt1; tt += 32) {
             int t = tt + lane;
-            unsigned long long m = t < wt1 ? dest_mask(a, t) : 0ull;
+            unsigned long long m = t < wt1 ? dest_mask(a, t, act) : 0ull;
             for (int d = 0; d < W; ++d) {
                 bool has = (m >> d) & 1ull;
                 unsigned bal = __ballot_sync(kFull, has);
@@ -466,7 +493,7 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a)
     bool overflow = false;
     for (int64_t i0 = wp0; i0 < wp1; i0 += 32) {
         int64_t i = i0 + lane;
-        int e = i < wp1 ? load_id(a, i) : -1;
+        int e = i < wp1 ? load_id(a, i, act) : -1;
         int key = e >= 0 ? e : -1;
         unsigned peers = __match_any_sync(kFull, key);
         int pos = key >= 0 ? cur[warp * E + key] + __popc(peers & lanemask_lt()) : 0;
@@ -506,7 +533,7 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a)
     for (int tt = wt0; tt < wt1; tt += 32) {
         int t = tt + lane;
         bool valid = t < wt1;
-        unsigned long long m = valid ? dest_mask(a, t) : 0ull;
+        unsigned long long m = valid ? dest_mask(a, t, act) : 0ull;
         for (int d = 0; d < W; ++d) {
             bool has = (m >> d) & 1ull;
             unsigned bal = __ballot_sync(kFull, has);
@@ -525,7 +552,7 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a)
             int64_t o = (int64_t)d * a.cap + row;
             a.recv_src[o] = t;
             for (int j = 0; j < a.k; ++j) {
-                int ej = load_id(a, (int64_t)t * a.k + j);
+                int ej = load_id(a, (int64_t)t * a.k + j, act);
                 bool local = ej >= 0 && ej / a.Le == d;
                 a.recv_topk_idx[o * a.k + j] = local ? ej - d * a.Le : -1;
                 a.recv_topk_w[o * a.k + j] = local ? a.topk_w[(int64_t)t * a.k + j] : 0.0f;
@@ -541,12 +568,13 @@ int routing_launches(const Plan &p) {
 }
 
 cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const float *topk_w,
-                           cudaStream_t s) {
+                           const int32_t *active, cudaStream_t s) {
     const Plan &p = *r.p;
     RouteArgs a;
     a.ids = ids;
     a.ids64 = ids64;
     a.topk_w = topk_w;
+    a.active = active;
     a.T = (int)p.T; a.W = (int)p.W; a.Tr = (int)p.Tr; a.E = (int)p.E; a.k = (int)p.k;
     a.Le = (int)(p.E / p.W);
     a.layout = p.layout;

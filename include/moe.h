@@ -78,6 +78,8 @@ typedef enum {
 #define MOE_STATUS_EM_OVERFLOW 0x2    /* EXPERT_MAJOR region full (a token named one expert
                                          twice): the later picks were dropped                 */
 #define MOE_STATUS_TIMEOUT 0x4        /* a bounded device wait gave up; outputs are invalid    */
+#define MOE_STATUS_INACTIVE_RANK 0x8  /* picks were dropped by the active_ranks mask
+                                         (informational)                                      */
 
 /* Event slots of moe_handle.events (per-kernel timing). */
 #define MOE_EV_DISPATCH_BEGIN 0
@@ -177,6 +179,11 @@ int moe_expert_out_size(const moe_geom *g, size_t *bytes);
  *                   and that pick is dropped
  *   topk_weights_dev float32 [T, k]: copied into recv_topk_weights for RM/FLAT (the
  *                   received routing); unused for EM (may be NULL there)
+ *   active_ranks_dev int32 [W] EP rank-health mask [MC-EP Buffer.dispatch active_ranks],
+ *                   or NULL (all active).  A rank with 0 has failed: picks whose expert lives
+ *                   on it and all picks of the tokens it owns are dropped (not dispatched,
+ *                   computed or combined; such tokens combine to zero) and
+ *                   MOE_STATUS_INACTIVE_RANK is set.  Read by the kernels at dispatch time.
  *   workspace_dev   >= moe_workspace_size bytes, 256-byte aligned; overwritten
  *   h               host struct filled on success
  * Computes (deterministically; atomics decide no position): per-expert counts and
@@ -185,8 +192,8 @@ int moe_expert_out_size(const moe_geom *g, size_t *bytes);
  * ids and weights, then copies each token row to every place it is received.
  */
 int moe_dispatch(const moe_geom *g, const void *x_dev, const void *topk_ids_dev,
-                 int ids_dtype, const float *topk_weights_dev, void *workspace_dev,
-                 size_t workspace_bytes, moe_handle *h, void *stream);
+                 int ids_dtype, const float *topk_weights_dev, const int32_t *active_ranks_dev,
+                 void *workspace_dev, size_t workspace_bytes, moe_handle *h, void *stream);
 
 /*
  * moe_prepare_weights - one-time re-layout of w1 [E, 2I, H] (gate rows [0, I), up rows
@@ -230,7 +237,7 @@ int moe_combine(const moe_handle *h, const float *expert_out_dev,
  * moe_forward_host - the whole layer end to end from HOST buffers, on one stream:
  * copy x_host / topk_ids_host / topk_weights_host into the caller's device buffers
  * (x_dev, topk_ids_dev, topk_weights_dev, same shapes as in moe_dispatch), then
- * moe_dispatch -> moe_expert_ffn -> moe_combine into out_dev, then copy out_dev to
+ * moe_dispatch (all ranks active) -> moe_expert_ffn -> moe_combine into out_dev, then copy out_dev to
  * out_host (bf16 [T, H]).  Asynchronous like the other calls: out_host is valid once the
  * stream has been synchronised.  Host buffers should be page-locked for the copies to
  * overlap; pageable memory works but the copies then synchronise.  Returns the first

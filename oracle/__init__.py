@@ -53,10 +53,10 @@ def _c():
         i64p = np.ctypeslib.ndpointer(np.int64, flags="C_CONTIGUOUS")
         f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
         ci = ctypes.c_int
-        _lib.oracle_route_experts.argtypes = [ci, ci, ci, ci, ci, ctypes.c_int64, i64p, i32p, i32p,
-                                              i32p, i32p, i32p, i32p]
+        _lib.oracle_route_experts.argtypes = [ci, ci, ci, ci, ci, ctypes.c_int64, i64p, ctypes.c_void_p,
+                                              i32p, i32p, i32p, i32p, i32p, i32p, i32p]
         _lib.oracle_route_experts.restype = ci
-        _lib.oracle_route_ranks.argtypes = [ci, ci, ci, ci, ci, ci, i64p, f32p,
+        _lib.oracle_route_ranks.argtypes = [ci, ci, ci, ci, ci, ci, i64p, ctypes.c_void_p, f32p,
                                             i32p, i32p, i32p, i32p, i32p, f32p]
         _lib.oracle_route_ranks.restype = None
     return _lib
@@ -80,9 +80,11 @@ def bf16_bits_to_f64(bits):
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def route(geom, ids, topk_w):
+def route(geom, ids, topk_w, active=None):
     """All routing metadata of one dispatch (Mooncake EP "Buffer.dispatch" outputs and the
     FlashInfer layout contracts).  geom: dict with W, Tr, T, E, k, layout ("EM"|"RM"|"FLAT").
+    active: optional EP rank-health mask [W] (0 = failed rank): picks whose expert or whose
+    token's source rank is inactive are dropped.
 
     Returns a dict of int32 arrays: counts, offsets, pick_pos, pick_src (first R entries),
     layout_range [E, W, 2], slot (EM recv row per pick or -1), and for RM/FLAT recv_row
@@ -103,14 +105,17 @@ def route(geom, ids, topk_w):
     pick_src = np.full(max(T * k, 1), -1, np.int32)
     lrange = np.zeros(E * W * 2, np.int32)
     n_over = np.zeros(1, np.int32)
+    n_inact = np.zeros(1, np.int32)
     cap = W * Tr
+    act = None if active is None else np.ascontiguousarray(np.asarray(active), dtype=np.int32)
+    act_p = None if act is None else act.ctypes.data_as(ctypes.c_void_p)
     # only the EXPERT_MAJOR region has a per-expert row capacity (W*Tr rows)
-    n_bad = lib.oracle_route_experts(T, k, E, W, Tr, cap if lay == 0 else -1, ids64, counts,
-                                     offsets, pick_pos, pick_src, lrange, n_over)
+    n_bad = lib.oracle_route_experts(T, k, E, W, Tr, cap if lay == 0 else -1, ids64, act_p, counts,
+                                     offsets, pick_pos, pick_src, lrange, n_over, n_inact)
     R = int(offsets[E])
     out = dict(ids=ids64, counts=counts, offsets=offsets, pick_pos=pick_pos.reshape(T, k),
                pick_src=pick_src[:R], layout_range=lrange.reshape(E, W, 2), n_bad=n_bad,
-               n_over=int(n_over[0]), R=R)
+               n_over=int(n_over[0]), n_inactive=int(n_inact[0]), R=R, active=act)
     # EXPERT_MAJOR receive row: expert e's region starts at e*cap, packed from its row 0.
     slot = np.full(T * k, -1, np.int64)
     valid = (pick_pos >= 0) & (lay == 0)
@@ -124,7 +129,7 @@ def route(geom, ids, topk_w):
         recv_src = np.full(W * cap, -1, np.int32)
         rti = np.full(W * cap * k, -1, np.int32)
         rtw = np.zeros(W * cap * k, np.float32)
-        lib.oracle_route_ranks(T, k, E, W, Tr, lay, ids64, w32, recv_row, recv_count,
+        lib.oracle_route_ranks(T, k, E, W, Tr, lay, ids64, act_p, w32, recv_row, recv_count,
                                num_recv, recv_src, rti, rtw)
         out.update(recv_row=recv_row.reshape(T, W), recv_count=recv_count.reshape(W, W),
                    num_recv=num_recv, recv_src=recv_src.reshape(W, cap),
@@ -250,12 +255,12 @@ def combine_ranks(geom, rt, expert_out_of, tokens):
     return round_bf16(np.array(res))
 
 
-def layer(geom, x_bits, ids, topk_w, w1, w2, tokens=None, expert_fn=None):
+def layer(geom, x_bits, ids, topk_w, w1, w2, tokens=None, expert_fn=None, active=None):
     """The whole layer for `tokens` (default all): route -> dispatch -> expert FFN ->
     combine, returning (route metadata, out [len(tokens), H] float64 holding bf16 values).
-    Only the picks of the requested tokens are evaluated."""
+    Only the picks of the requested tokens are evaluated.  active: EP rank-health mask."""
     T, k = geom["T"], geom["k"]
-    rt = route(geom, ids, topk_w)
+    rt = route(geom, ids, topk_w, active)
     tokens = np.arange(T) if tokens is None else np.asarray(tokens)
     picks = [t * k + j for t in tokens for j in range(k) if rt["pick_pos"][t, j] >= 0]
     ys = pick_outputs(geom, rt, x_bits, w1, w2, picks=picks, expert_fn=expert_fn)

@@ -18,9 +18,21 @@
  * Readings where the pages are silent (stated once, used throughout):
  *   - order inside an expert region / a receive region is ascending (token, pick);
  *   - a token is received by destination rank d once if any of its valid picks lives on d;
- *   - an id outside [-1, E) is an error: it is counted and the pick is dropped.
+ *   - an id outside [-1, E) is an error: it is counted and the pick is dropped;
+ *   - EP rank-health mask (Mooncake EP guide, Buffer.dispatch `active_ranks`, int32
+ *     [num_ranks], 0 = failed rank; "Active-rank tensors: PG vs EP"): a pick is dropped
+ *     when its expert lives on an inactive rank or its token belongs to an inactive source
+ *     rank (`active` NULL = all ranks active).
  */
+
 #include <stdint.h>
+
+/* 1 iff pick (t, e) survives the rank-health mask. */
+static int rank_ok(const int32_t *active, int Le, int Tr, int t, int64_t e)
+{
+    if (!active) return 1;
+    return active[e / Le] != 0 && active[t / Tr] != 0;
+}
 
 /* Expert-grouped pick list (shared by all three layouts).
  *   cap          capacity of one expert's region in rows, or -1 for no limit.  The
@@ -38,11 +50,14 @@
  * Returns the number of ids outside [-1, E).
  */
 int oracle_route_experts(int T, int k, int E, int W, int Tr, int64_t cap, const int64_t *ids,
-                         int32_t *counts, int32_t *offsets, int32_t *pick_pos,
-                         int32_t *pick_src, int32_t *layout_range, int32_t *n_over)
+                         const int32_t *active, int32_t *counts, int32_t *offsets,
+                         int32_t *pick_pos, int32_t *pick_src, int32_t *layout_range,
+                         int32_t *n_over, int32_t *n_inactive)
 {
     int bad = 0;
+    int Le = E / W;
     *n_over = 0;
+    *n_inactive = 0;
     for (int e = 0; e < E; ++e) counts[e] = 0;
     for (int i = 0; i < E * W * 2; ++i) layout_range[i] = 0;
     for (int t = 0; t < T; ++t)
@@ -50,6 +65,7 @@ int oracle_route_experts(int T, int k, int E, int W, int Tr, int64_t cap, const 
             int64_t e = ids[(int64_t)t * k + j];
             if (e == -1) continue;
             if (e < -1 || e >= E) { ++bad; continue; }
+            if (!rank_ok(active, Le, Tr, t, e)) { *n_inactive += 1; continue; }
             if (cap >= 0 && counts[e] >= cap) { *n_over += 1; continue; }
             counts[e] += 1;
             layout_range[(e * W + t / Tr) * 2 + 1] += 1;
@@ -70,7 +86,10 @@ int oracle_route_experts(int T, int k, int E, int W, int Tr, int64_t cap, const 
         for (int j = 0; j < k; ++j) {
             int64_t i = (int64_t)t * k + j;
             int64_t e = ids[i];
-            if (e < 0 || e >= E || next[e] == offsets[e + 1]) { pick_pos[i] = -1; continue; }
+            if (e < 0 || e >= E || !rank_ok(active, Le, Tr, t, e) || next[e] == offsets[e + 1]) {
+                pick_pos[i] = -1;
+                continue;
+            }
             int p = next[e]++;
             pick_pos[i] = p;
             pick_src[p] = (int32_t)i;
@@ -90,7 +109,7 @@ int oracle_route_experts(int T, int k, int E, int W, int Tr, int64_t cap, const 
  *   recv_topk_w[(d*cap+row)*k + j]   topk_weights[t, j] if pick j lives on d, else 0
  */
 void oracle_route_ranks(int T, int k, int E, int W, int Tr, int layout,
-                        const int64_t *ids, const float *topk_w,
+                        const int64_t *ids, const int32_t *active, const float *topk_w,
                         int32_t *recv_row, int32_t *recv_count, int32_t *num_recv,
                         int32_t *recv_src, int32_t *recv_topk_idx, float *recv_topk_w)
 {
@@ -104,7 +123,7 @@ void oracle_route_ranks(int T, int k, int E, int W, int Tr, int layout,
             int on_d = 0;
             for (int j = 0; j < k; ++j) {
                 int64_t e = ids[(int64_t)t * k + j];
-                if (e >= 0 && e < E && e / Le == d) on_d = 1;
+                if (e >= 0 && e < E && e / Le == d && rank_ok(active, Le, Tr, t, e)) on_d = 1;
             }
             if (!on_d) { recv_row[(int64_t)t * W + d] = -1; continue; }
             int row = (layout == 1) ? s * Tr + recv_count[d * W + s] : num_recv[d];
@@ -115,7 +134,7 @@ void oracle_route_ranks(int T, int k, int E, int W, int Tr, int layout,
             for (int j = 0; j < k; ++j) {
                 int64_t e = ids[(int64_t)t * k + j];
                 int64_t o = (d * cap + row) * k + j;
-                if (e >= 0 && e < E && e / Le == d) {
+                if (e >= 0 && e < E && e / Le == d && rank_ok(active, Le, Tr, t, e)) {
                     recv_topk_idx[o] = (int32_t)(e - (int64_t)d * Le);
                     recv_topk_w[o] = topk_w[(int64_t)t * k + j];
                 } else {

@@ -28,13 +28,14 @@ def geom_dict(cfg):
     return oracle.geom_of(cfg)
 
 
-def run_layer(case, layer=None):
+def run_layer(case, layer=None, active=None):
     cfg = case.cfg
     if layer is None:
         layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I,
                                  cfg.layout, cfg.algo)
         layer.set_weights(case.w1, case.w2)
-    layer.forward(case.x, case.ids, case.w)
+    act = None if active is None else torch.as_tensor(active, dtype=torch.int32, device=case.x.device)
+    layer.forward(case.x, case.ids, case.w, act)
     torch.cuda.synchronize()
     return layer
 
@@ -104,10 +105,10 @@ def check_expert_out(layer, rt, case, picks_or_rows=None, max_rows=None):
         assert_close(eo[idx].cpu().numpy(), ref, "expert_out (%s)" % cfg.layout)
 
 
-def check_out(layer, case, tokens=None):
+def check_out(layer, case, tokens=None, active=None):
     cfg = case.cfg
     _, ref = oracle.layer(geom_dict(cfg), case.x_bits, case.ids_np, case.w_np, case.w1_host,
-                          case.w2_host, tokens=tokens)
+                          case.w2_host, tokens=tokens, active=active)
     got = bf16_tensor_to_f64(layer.out if tokens is None else layer.out[torch.as_tensor(tokens)])
     assert_close(got, ref, "out (%s)" % cfg.name)
     return ref

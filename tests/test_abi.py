@@ -79,11 +79,12 @@ def test_dispatch_host_errors_before_any_launch(lib):
     x = ctypes.c_void_p(1 << 21)
     call = lambda **kw: lib.moe_dispatch(  # noqa: E731
         ctypes.byref(kw.get("g", g)), kw.get("x", x), kw.get("ids", x), kw.get("dt", 1), None,
-        kw.get("ws", ws), kw.get("wsb", 1 << 40), ctypes.byref(h), None)
+        kw.get("act", None), kw.get("ws", ws), kw.get("wsb", 1 << 40), ctypes.byref(h), None)
     assert call(dt=5) == -7
     assert call(ws=ctypes.c_void_p((1 << 20) + 16)) == -9
     assert call(x=ctypes.c_void_p((1 << 21) + 2)) == -9
     assert call(wsb=16) == -8
+    assert call(act=ctypes.c_void_p((1 << 21) + 2)) == -9
     assert call(g=_geom(layout="RM")) == -1      # RM/FLAT need topk_weights
     assert h.magic == 0
 

@@ -23,13 +23,16 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 # ----------------------------------------------------------------------------- routing
-def brute_route(W, Tr, T, E, k, ids, w, cap=None):
+def brute_route(W, Tr, T, E, k, ids, w, cap=None, active=None):
     """Enumeration: every quantity counted directly from its definition, O(n^2).
-    cap: EXPERT_MAJOR region rows; a pick with that many earlier picks of its expert is dropped."""
+    cap: EXPERT_MAJOR region rows; a pick with that many earlier picks of its expert is dropped.
+    active: rank-health mask; picks of an inactive expert rank or source rank are dropped."""
     ids = np.asarray(ids).reshape(T, k)
     Le = E // W
     picks = [(t, j) for t in range(T) for j in range(k)]
-    in_range = lambda t, j: 0 <= ids[t, j] < E  # noqa: E731
+    alive = (lambda t, j: True) if active is None else (  # noqa: E731
+        lambda t, j: active[ids[t, j] // Le] != 0 and active[t // Tr] != 0)
+    in_range = lambda t, j: 0 <= ids[t, j] < E and alive(t, j)  # noqa: E731
     earlier = lambda t, j: sum(1 for (a, b) in picks  # noqa: E731
                                if (a, b) < (t, j) and in_range(a, b) and ids[a, b] == ids[t, j])
     valid = lambda t, j: in_range(t, j) and (cap is None or earlier(t, j) < cap)  # noqa: E731
@@ -83,6 +86,43 @@ def test_route_matches_brute_force(seed):
         np.testing.assert_array_equal(rt["layout_range"], b["lr"])
         if layout != "EM":
             np.testing.assert_array_equal(rt["recv_row"], b["rm"] if layout == "RM" else b["fl"])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_route_with_rank_mask_matches_brute_force(seed):
+    W, Tr, T, E, k, ids, w = _rand_case(200 + seed)
+    rng = np.random.default_rng(seed)
+    active = (rng.random(W) < 0.6).astype(np.int32)
+    for layout in ("EM", "RM", "FLAT"):
+        b = brute_route(W, Tr, T, E, k, ids, w, cap=W * Tr if layout == "EM" else None, active=active)
+        rt = oracle.route(dict(W=W, Tr=Tr, T=T, E=E, k=k, layout=layout), ids, w, active)
+        assert list(rt["counts"]) == b["counts"]
+        np.testing.assert_array_equal(rt["pick_pos"], b["pos"])
+        np.testing.assert_array_equal(rt["layout_range"], b["lr"])
+        if layout != "EM":
+            np.testing.assert_array_equal(rt["recv_row"], b["rm"] if layout == "RM" else b["fl"])
+
+
+@pytest.mark.parametrize("layout", ["EM", "RM", "FLAT"])
+def test_rank_mask_equals_masked_ids(layout):
+    """A failed rank is equivalent to masking (-1) every pick on it and every pick of the
+    tokens it owns (Mooncake EP: active_ranks = 0 marks a failed rank)."""
+    c = _tiny_cfg(layout)
+    x, ids, w, w1, w2 = _inputs(c)
+    active = np.array([1, 0], np.int32)
+    Le, Tr = c.E // c.W, c.Tr
+    ids_m = ids.copy()
+    for t in range(c.tokens):
+        for j in range(c.k):
+            if ids[t, j] >= 0 and (active[ids[t, j] // Le] == 0 or active[t // Tr] == 0):
+                ids_m[t, j] = -1
+    g = oracle.geom_of(c)
+    rt_a, out_a = oracle.layer(g, x, ids, w, w1, w2, active=active)
+    rt_b, out_b = oracle.layer(g, x, ids_m, w, w1, w2)
+    np.testing.assert_array_equal(out_a, out_b)
+    np.testing.assert_array_equal(rt_a["pick_pos"], rt_b["pick_pos"])
+    assert rt_a["n_inactive"] == int(((ids >= 0) & (ids_m == -1)).sum())
+    assert np.all(out_a[Tr:] == 0)   # tokens of the failed source rank combine to zero
 
 
 @pytest.mark.parametrize("seed", range(10))

@@ -157,6 +157,22 @@ def test_bad_ids_are_flagged_and_dropped():
     check_out(layer, case)
 
 
+@pytest.mark.parametrize("name", ["small_em", "small_rm", "small_flat", "blocks_rm", "pair_flat"])
+def test_inactive_ranks_are_masked(name):
+    """EP rank-health mask: picks on a failed rank and tokens owned by it are dropped."""
+    cfg = SMALL_CASES[name].with_(seed=31)
+    active = np.ones(cfg.W, np.int32)
+    active[1] = 0
+    case = make_case(cfg, "cuda")
+    layer = run_layer(case, active=active)
+    assert layer.status() == moe.STATUS_INACTIVE_RANK
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np, active)
+    assert rt["n_inactive"] > 0
+    check_routing(layer, rt, cfg)
+    check_dispatch_rows(layer, rt, case)
+    check_out(layer, case, active=active)
+
+
 def test_expert_major_region_overflow():
     """A token naming one expert twice can overflow the W*Tr-row EM region: the extra picks
     are dropped and flagged, the rest matches the oracle."""
