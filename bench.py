@@ -173,6 +173,22 @@ def oracle_sample_time(cfg, case, n_tokens):
     return time.perf_counter() - t0
 
 
+def max_over_ranks(x, dist, device="cpu"):
+    """Max of a per-rank float over all ranks (identity without torch.distributed)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_step, steps, world, max_seconds):
+    """Whole-job throughput: every replica processes tokens_per_step per step; time is the
+    slowest rank's."""
+    return tokens_per_step * steps * world / max_seconds
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -259,12 +275,8 @@ def run_ours(args, cfg, rank, world, dist):
     if status != 0:
         raise RuntimeError("device status %d after the timed steps" % status)
 
-    total_s = sum(steps_ms) / 1e3
-    if dist is not None:
-        t = torch.tensor([total_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
-    value = cfg.tokens * args.steps * world / total_s
+    total_s = max_over_ranks(sum(steps_ms) / 1e3, dist, dev)
+    value = job_tokens_per_s(cfg.tokens, args.steps, world, total_s)
     kmean = {k: statistics.mean(d[k] for d in ktimes) for k in ktimes[0]}
 
     # batch statistics for the algorithmic work (read once, outside the timed region)
@@ -325,12 +337,8 @@ def run_ours(args, cfg, rank, world, dist):
             raise RuntimeError("device status after e2e steps")
         if not torch.equal(out_h.view(torch.int16), layer.out.cpu().view(torch.int16)):
             raise RuntimeError("host-buffer output differs from the device output")
-        e2e_s = sum(e2e_ms) / 1e3
-        if dist is not None:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": cfg.tokens * args.steps * world / e2e_s, "unit": "tokens/s",
+        e2e_s = max_over_ranks(sum(e2e_ms) / 1e3, dist, dev)
+        e2e = {"value": job_tokens_per_s(cfg.tokens, args.steps, world, e2e_s), "unit": "tokens/s",
                "h2d_bytes_per_step": x_h.numel() * 2 + ids_h.numel() * ids_h.element_size() + w_h.numel() * 4,
                "d2h_bytes_per_step": out_h.numel() * 2}
 
