@@ -39,7 +39,7 @@ ORACLE_SAMPLE_TOKENS = {"tiny_ll_em": 64, "mixtral_ll_em": 4, "dsv3_ll_rm": 4, "
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -83,7 +83,9 @@ def algorithmic_work(cfg, rt):
 
 
 class ClockSampler:
-    """nvidia-smi SM clock / throttle-reason samples (every 200 ms) during the timed region."""
+    """nvidia-smi SM clock / throttle-reason samples (every 50 ms) taken while the timed
+    steps run.  start() returns once the sampler has written its first row, so that the
+    rows counted between begin() and end() fall inside the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -93,16 +95,34 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.out = None
+        self.span = [0, None]
+
+    def _rows(self):
+        with open(self.out.name) as f:
+            return [p for p in ([x.strip() for x in line.split(",")] for line in f) if len(p) >= 9]
 
     def start(self):
         try:
-            self.out = open(os.devnull if False else "/tmp/_bench_clocks_%d.csv" % os.getpid(), "w")
+            self.out = open("/tmp/_bench_clocks_%d.csv" % os.getpid(), "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.out,
                 stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5 and self.proc.poll() is None and not self._rows():
+            time.sleep(0.02)
+
+    def begin(self):
+        if self.proc is not None:
+            self.span[0] = len(self._rows())
+
+    def end(self):
+        if self.proc is not None:
+            time.sleep(0.06)            # one more row, taken as the last step ends
+            self.span[1] = len(self._rows())
 
     def stop(self):
         if self.proc is None:
@@ -113,13 +133,11 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.close()
-        rows = []
-        with open(self.out.name) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+        rows = self._rows()
         os.unlink(self.out.name)
+        # the rows written while the timed steps ran; the last row before them if none
+        a, b = self.span[0], self.span[1] if self.span[1] is not None else len(rows)
+        rows = rows[a:b] or rows[max(a - 1, 0):a]
         if not rows:
             return None
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -258,6 +276,7 @@ def run_ours(args, cfg, rank, world, dist):
     torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
+    clocks.begin()
     steps_ms, ktimes = [], []
     for _ in range(args.steps):
         flush.zero_()
@@ -267,6 +286,7 @@ def run_ours(args, cfg, rank, world, dist):
         ev1.synchronize()
         steps_ms.append(ev0.elapsed_time(ev1))
         ktimes.append(layer.kernel_times_ms())
+    clocks.end()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()

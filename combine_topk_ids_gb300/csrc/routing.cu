@@ -53,7 +53,7 @@ __device__ __forceinline__ int load_id(const RouteArgs &a, int64_t i, unsigned l
                           : (long long)reinterpret_cast<const int *>(a.ids)[i];
     if (v == -1) return -1;
     if (v < -1 || v >= a.E) return -2;
-    const int src = (int)(i / a.k) / a.Tr;
+    const int src = ((int)i / a.k) / a.Tr;   // picks fit in int32 (checked on the host)
     if (!((act >> ((int)v / a.Le)) & 1ull) || !((act >> src) & 1ull)) return -3;
     return (int)v;
 }
@@ -131,26 +131,45 @@ __global__ void __launch_bounds__(kRouteThreads) route_count_kernel(RouteArgs a)
             a.blk_dhist[(int64_t)d * a.nb + blockIdx.x] = dhist[d];
 }
 
-// Exclusive scan of one row hist[0..nb) (blocks grouped by logical rank) into base[],
-// warp-cooperative.  RANK_MAJOR destinations restart each rank at s*Tr.  Lane 0 gets the
-// per-rank sums through the callback.
+// Exclusive scan of one row hist[0..nb) (blocks grouped by logical rank, nbpr per rank)
+// into base[], warp-cooperative, in one pass over the row.  RANK_MAJOR destinations restart
+// each source rank at row s*Tr.  on_rank(s, begin, count) is then called by lane s % 32 for
+// every rank s (begin/count of the plain, non-restarted scan).  Returns the row total.
 template <typename RankFn>
 __device__ __forceinline__ int scan_row(const RouteArgs &a, const int32_t *hist, int32_t *base,
                                         bool restart_per_rank, RankFn on_rank) {
-    int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31;
     int run = 0;
-    for (int s = 0; s < a.W; ++s) {
-        if (restart_per_rank) run = s * a.Tr;
-        int begin = run;
-        int b_end = (s + 1) * a.nbpr;
-        for (int b0 = s * a.nbpr; b0 < b_end; b0 += 32) {
-            int b = b0 + lane;
-            int v = b < b_end ? hist[b] : 0;
-            int incl = warp_incl_scan(v);
-            if (b < b_end) base[b] = run + incl - v;
-            run += __shfl_sync(kFull, incl, 31);
+    for (int b0 = 0; b0 < a.nb; b0 += 32) {
+        const int b = b0 + lane;
+        const int v = b < a.nb ? hist[b] : 0;
+        const int incl = warp_incl_scan(v);
+        if (b < a.nb) base[b] = run + incl - v;
+        run += __shfl_sync(kFull, incl, 31);
+    }
+    __syncwarp();
+    // per-rank begin (= exclusive prefix at the rank's first block) and count
+    int first[2] = {0, 0};   // ranks lane and lane + 32 (W <= 64)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int r = lane + 32 * q;
+        if (r < a.W) {
+            const int beg = base[r * a.nbpr];
+            const int end = r + 1 < a.W ? base[(r + 1) * a.nbpr] : run;
+            first[q] = beg;
+            on_rank(r, beg, end - beg);
         }
-        on_rank(s, begin, run - begin);
+    }
+    if (restart_per_rank) {
+        __syncwarp();
+        for (int b0 = 0; b0 < a.nb; b0 += 32) {
+            const int b = b0 + lane;
+            const int r = (b < a.nb ? b : 0) / a.nbpr;
+            const int f0 = __shfl_sync(kFull, first[0], r & 31);
+            const int f1 = __shfl_sync(kFull, first[1], r & 31);
+            if (b < a.nb) base[b] = r * a.Tr + base[b] - (r < 32 ? f0 : f1);
+        }
+        __syncwarp();
     }
     return run;
 }
@@ -164,14 +183,12 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
     for (int e = warp; e < a.E; e += nwarps) {
         int total = scan_row(a, a.blk_hist + (int64_t)e * a.nb, a.blk_base + (int64_t)e * a.nb,
                              false, [&](int s, int begin, int cnt) {
-                                 if (lane == 0) {
-                                     int64_t lim = em ? a.cap : (int64_t)1 << 40;
-                                     int64_t b = begin < lim ? begin : lim;
-                                     int64_t kept = lim - begin;
-                                     kept = kept < 0 ? 0 : (kept > cnt ? cnt : kept);
-                                     a.layout_range[((int64_t)e * a.W + s) * 2 + 0] = (int)b;
-                                     a.layout_range[((int64_t)e * a.W + s) * 2 + 1] = (int)kept;
-                                 }
+                                 int64_t lim = em ? a.cap : (int64_t)1 << 40;
+                                 int64_t b = begin < lim ? begin : lim;
+                                 int64_t kept = lim - begin;
+                                 kept = kept < 0 ? 0 : (kept > cnt ? cnt : kept);
+                                 a.layout_range[((int64_t)e * a.W + s) * 2 + 0] = (int)b;
+                                 a.layout_range[((int64_t)e * a.W + s) * 2 + 1] = (int)kept;
                              });
         if (lane == 0) a.counts[e] = (em && total > a.cap) ? (int)a.cap : total;
     }
@@ -180,15 +197,9 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
         for (int d = warp; d < a.W; d += nwarps) {
             int total = scan_row(a, a.blk_dhist + (int64_t)d * a.nb, a.blk_dbase + (int64_t)d * a.nb,
                                  a.layout == MOE_LAYOUT_RANK_MAJOR, [&](int s, int, int cnt) {
-                                     if (lane == 0) a.recv_count[d * a.W + s] = cnt;
+                                     a.recv_count[d * a.W + s] = cnt;
                                  });
-            if (lane == 0) {
-                // RANK_MAJOR's running value includes the s*Tr row base of the last rank
-                int n = 0;
-                for (int s = 0; s < a.W; ++s) n += a.recv_count[d * a.W + s];
-                a.num_recv[d] = n;
-                (void)total;
-            }
+            if (lane == 0) a.num_recv[d] = total;
         }
     }
     __syncthreads();
@@ -341,13 +352,20 @@ __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(RouteArgs a
             a.recv_row[(int64_t)t * a.W + d] = row;
             int64_t o = (int64_t)d * a.cap + row;
             a.recv_src[o] = t;
-            for (int j = 0; j < a.k; ++j) {
-                int ej = load_id(a, (int64_t)t * a.k + j, act);
-                bool local = ej >= 0 && ej / a.Le == d;
-                a.recv_topk_idx[o * a.k + j] = local ? ej - d * a.Le : -1;
-                a.recv_topk_w[o * a.k + j] = local ? a.topk_w[(int64_t)t * a.k + j] : 0.0f;
+            for (int j = 0; j < a.k; ++j) {   // non-local until a local pick claims it below
+                a.recv_topk_idx[o * a.k + j] = -1;
+                a.recv_topk_w[o * a.k + j] = 0.0f;
             }
         }
+    }
+    __syncthreads();   // this block's receive rows exist; now place its local picks in them
+    for (int64_t i = p0 + threadIdx.x; i < p0 + np; i += blockDim.x) {
+        const int e = load_id(a, i, act);
+        if (e < 0) continue;
+        const int t = (int)i / a.k, j = (int)i - t * a.k, d = e / a.Le;
+        const int64_t o = (int64_t)d * a.cap + a.recv_row[(int64_t)t * a.W + d];
+        a.recv_topk_idx[o * a.k + j] = e - d * a.Le;
+        a.recv_topk_w[o * a.k + j] = a.topk_w[i];
     }
 }
 
@@ -551,20 +569,33 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a)
             a.recv_row[(int64_t)t * W + d] = row;
             int64_t o = (int64_t)d * a.cap + row;
             a.recv_src[o] = t;
-            for (int j = 0; j < a.k; ++j) {
-                int ej = load_id(a, (int64_t)t * a.k + j, act);
-                bool local = ej >= 0 && ej / a.Le == d;
-                a.recv_topk_idx[o * a.k + j] = local ? ej - d * a.Le : -1;
-                a.recv_topk_w[o * a.k + j] = local ? a.topk_w[(int64_t)t * a.k + j] : 0.0f;
+            for (int j = 0; j < a.k; ++j) {   // non-local until a local pick claims it below
+                a.recv_topk_idx[o * a.k + j] = -1;
+                a.recv_topk_w[o * a.k + j] = 0.0f;
             }
         }
+    }
+    __syncthreads();   // every receive row exists; now place the local picks in them
+    for (int64_t i = threadIdx.x; i < P; i += blockDim.x) {
+        const int e = load_id(a, i, act);
+        if (e < 0) continue;
+        const int t = (int)i / a.k, j = (int)i - t * a.k, d = e / a.Le;
+        const int64_t o = (int64_t)d * a.cap + a.recv_row[(int64_t)t * W + d];
+        a.recv_topk_idx[o * a.k + j] = e - d * a.Le;
+        a.recv_topk_w[o * a.k + j] = a.topk_w[i];
     }
 }
 
 }  // namespace
 
+#ifndef MOE_FUSED_ROUTING_MAX_PICKS
+#define MOE_FUSED_ROUTING_MAX_PICKS 16384
+#endif
+// The single-CTA path wins for few experts (one launch instead of three: 10 vs ~15 us on
+// the 8-expert decode batch) and loses for many (82 vs 36 us with 256 experts, where its
+// per-expert work runs on one SM), so it is kept for E <= 64.
 int routing_launches(const Plan &p) {
-    return (p.P <= 16384 && p.E <= 512 && p.E * p.W <= 4096) ? 1 : 3;
+    return (p.P <= MOE_FUSED_ROUTING_MAX_PICKS && p.E <= 64 && p.E * p.W <= 4096) ? 1 : 3;
 }
 
 cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const float *topk_w,
@@ -588,7 +619,7 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
     a.recv_src = r.recv_src; a.recv_topk_idx = r.recv_topk_idx; a.recv_topk_w = r.recv_topk_w;
     a.blk_dhist = r.blk_dhist; a.blk_dbase = r.blk_dbase;
 
-    // one fused CTA for small batches (bounded shared memory: E <= 512, E*W <= 4096)
+    // one fused CTA for small batches with few experts (bounded shared memory)
     if (routing_launches(p) == 1) {
         const size_t smf = (size_t)(kFusedWarps * (a.E + a.W) + a.E * a.W + a.W * a.W + 2 * a.E) *
                            sizeof(int);
