@@ -150,7 +150,8 @@ class ClockSampler:
 
 
 # sources that define the grouped-GEMM kernels whose ncu counters are committed
-TRAFFIC_SOURCES = ("combine_topk_ids_gb300/csrc/ffn_tc.cu", "combine_topk_ids_gb300/csrc/moe_internal.cuh",
+TRAFFIC_SOURCES = ("combine_topk_ids_gb300/csrc/ffn_tc.cu", "combine_topk_ids_gb300/csrc/tc_common.cuh",
+                   "combine_topk_ids_gb300/csrc/moe_internal.cuh",
                    "combine_topk_ids_gb300/build.py")
 
 

@@ -6,8 +6,9 @@ There is no fallback: if libmoe.so is missing, or the device is not a GB300, the
 raise.
 
 Functions carry the C names: moe_workspace_size, moe_expert_out_size, moe_dispatch,
-moe_prepare_weights, moe_expert_ffn, moe_combine, moe_get_status.  MoELayer1GPU bundles
-them with the buffers of one geometry.
+moe_prepare_weights, moe_expert_ffn, moe_combine, moe_get_status, and for the FP8 variant
+moe_quantize_weights_fp8, moe_prepare_weights_fp8, moe_expert_ffn_fp8.  MoELayer1GPU
+bundles them with the buffers of one geometry.
 """
 import ctypes
 import os
@@ -16,6 +17,7 @@ from .build import LIB_PATH, build  # noqa: F401
 
 LAYOUT = {"EM": 0, "RM": 1, "FLAT": 2}
 ALGO = {"LL": 0, "HT": 1}
+QUANT = {"bf16": 0, "fp8": 1}
 IDS_INT32, IDS_INT64 = 0, 1
 STATUS_BAD_EXPERT_ID, STATUS_EM_OVERFLOW, STATUS_TIMEOUT, STATUS_INACTIVE_RANK = 0x1, 0x2, 0x4, 0x8
 
@@ -23,13 +25,13 @@ STATUS_BAD_EXPERT_ID, STATUS_EM_OVERFLOW, STATUS_TIMEOUT, STATUS_INACTIVE_RANK =
 class MoeGeom(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "world", "max_tok", "num_tokens", "hidden", "num_experts", "top_k", "intermediate",
-        "layout", "algorithm")]
+        "layout", "algorithm", "quant")]
 
 
 _P = ctypes.c_void_p
-_HANDLE_PTRS = ("recv_x", "counts", "offsets", "pick_pos", "pick_src", "slot", "layout_range",
-                "recv_row", "recv_count", "num_recv", "recv_src", "recv_topk_idx",
-                "recv_topk_weights", "status", "workspace")
+_HANDLE_PTRS = ("recv_x", "recv_scales", "counts", "offsets", "pick_pos", "pick_src", "slot",
+                "layout_range", "recv_row", "recv_count", "num_recv", "recv_src", "recv_topk_idx",
+                "recv_topk_weights", "status", "ffn_act", "ffn_act_scales", "workspace")
 
 
 class MoeHandle(ctypes.Structure):
@@ -75,11 +77,15 @@ def lib():
         L.moe_launches_per_layer.restype = ctypes.c_int
         L.moe_route_noalloc.argtypes = [G, _P, ctypes.c_int] + [_P] * 8
         L.moe_route_noalloc.restype = ctypes.c_int
+        L.moe_quantize_weights_fp8.argtypes = [G] + [_P] * 7
+        L.moe_prepare_weights_fp8.argtypes = [G] + [_P] * 5
+        L.moe_expert_ffn_fp8.argtypes = [H] + [_P] * 6
         L.moe_strerror.argtypes = [ctypes.c_int]
         L.moe_strerror.restype = ctypes.c_char_p
         for f in ("moe_workspace_size", "moe_expert_out_size", "moe_dispatch",
                   "moe_prepare_weights", "moe_expert_ffn", "moe_combine", "moe_get_status",
-                  "moe_forward_host"):
+                  "moe_forward_host", "moe_quantize_weights_fp8", "moe_prepare_weights_fp8",
+                  "moe_expert_ffn_fp8"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -94,9 +100,10 @@ def _check(rc, where):
         raise MoeError(rc, where)
 
 
-def make_geom(W, Tr, T, H, E, k, I, layout="EM", algo="LL") -> MoeGeom:
+def make_geom(W, Tr, T, H, E, k, I, layout="EM", algo="LL", quant="bf16") -> MoeGeom:
     return MoeGeom(W, Tr, T, H, E, k, I, LAYOUT[layout] if isinstance(layout, str) else layout,
-                   ALGO[algo] if isinstance(algo, str) else algo)
+                   ALGO[algo] if isinstance(algo, str) else algo,
+                   QUANT[quant] if isinstance(quant, str) else quant)
 
 
 def _ptr(t):
@@ -147,6 +154,22 @@ def moe_prepare_weights(g, w1, w1_prepared, stream=None):
 def moe_expert_ffn(h, w1_prepared, w2, expert_out, stream=None):
     _check(lib().moe_expert_ffn(ctypes.byref(h), _ptr(w1_prepared), _ptr(w2), _ptr(expert_out),
                                 _stream(stream)), "moe_expert_ffn")
+
+
+def moe_quantize_weights_fp8(g, w1, w2, w1q_prepared, w1_scales_prepared, w2q, w2_scales, stream=None):
+    _check(lib().moe_quantize_weights_fp8(ctypes.byref(g), _ptr(w1), _ptr(w2), _ptr(w1q_prepared),
+                                          _ptr(w1_scales_prepared), _ptr(w2q), _ptr(w2_scales),
+                                          _stream(stream)), "moe_quantize_weights_fp8")
+
+
+def moe_prepare_weights_fp8(g, w1q, w1_scales, w1q_prepared, w1_scales_prepared, stream=None):
+    _check(lib().moe_prepare_weights_fp8(ctypes.byref(g), _ptr(w1q), _ptr(w1_scales), _ptr(w1q_prepared),
+                                         _ptr(w1_scales_prepared), _stream(stream)), "moe_prepare_weights_fp8")
+
+
+def moe_expert_ffn_fp8(h, w1q_prepared, w1_scales_prepared, w2q, w2_scales, expert_out, stream=None):
+    _check(lib().moe_expert_ffn_fp8(ctypes.byref(h), _ptr(w1q_prepared), _ptr(w1_scales_prepared), _ptr(w2q),
+                                    _ptr(w2_scales), _ptr(expert_out), _stream(stream)), "moe_expert_ffn_fp8")
 
 
 def moe_combine(h, expert_out, topk_weights, out, stream=None):
@@ -202,12 +225,14 @@ class MoELayer1GPU:
     """One MoE EP layer of a fixed geometry with its buffers on the current CUDA device.
 
     forward(x, topk_ids, topk_weights) = moe_dispatch -> moe_expert_ffn -> moe_combine,
-    all on the current stream, no host synchronisation.
+    all on the current stream, no host synchronisation.  quant="fp8": FP8 dispatch and
+    moe_expert_ffn_fp8 on weights quantised by set_weights.
     """
 
-    def __init__(self, W, Tr, T, H, E, k, I, layout="EM", algo="LL", device="cuda"):
+    def __init__(self, W, Tr, T, H, E, k, I, layout="EM", algo="LL", device="cuda", quant="bf16"):
         import torch
-        self.geom = make_geom(W, Tr, T, H, E, k, I, layout, algo)
+        self.quant = quant
+        self.geom = make_geom(W, Tr, T, H, E, k, I, layout, algo, quant)
         self.device = torch.device(device)
         self.workspace = torch.empty(moe_workspace_size(self.geom), dtype=torch.uint8, device=self.device)
         self.expert_out = torch.empty(moe_expert_out_size(self.geom) // 4, dtype=torch.float32,
@@ -251,7 +276,17 @@ class MoELayer1GPU:
         return d
 
     def set_weights(self, w1, w2):
+        """bf16 w1 [E, 2I, H] and w2 [E, H, I]; prepared (FP8: quantised) once here."""
         import torch
+        if self.quant == "fp8":
+            E, I2, H = w1.shape
+            dev = w1.device
+            self.w1p = torch.empty((E, I2, H), dtype=torch.uint8, device=dev)
+            self.w1s = torch.empty((E, I2 // 128, H // 128), dtype=torch.float32, device=dev)
+            self.w2 = torch.empty(tuple(w2.shape), dtype=torch.uint8, device=dev)
+            self.w2s = torch.empty((E, H // 128, I2 // 256), dtype=torch.float32, device=dev)
+            moe_quantize_weights_fp8(self.geom, w1, w2, self.w1p, self.w1s, self.w2, self.w2s)
+            return
         self.w1p = torch.empty_like(w1)
         moe_prepare_weights(self.geom, w1, self.w1p)
         self.w2 = w2
@@ -262,7 +297,10 @@ class MoELayer1GPU:
         return self.handle
 
     def expert_ffn(self):
-        moe_expert_ffn(self.handle, self.w1p, self.w2, self.expert_out)
+        if self.quant == "fp8":
+            moe_expert_ffn_fp8(self.handle, self.w1p, self.w1s, self.w2, self.w2s, self.expert_out)
+        else:
+            moe_expert_ffn(self.handle, self.w1p, self.w2, self.expert_out)
         return self.expert_out
 
     def combine(self, topk_weights):

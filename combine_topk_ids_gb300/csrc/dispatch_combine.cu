@@ -1,6 +1,7 @@
-// Data-movement kernels of the layer: the dispatch row scatter, the RANK_MAJOR / FLAT
-// pick gather and weighted local-pick reduction, the combine gather-reduce, and the
-// one-time gate/up interleave of w1.  All are HBM-bound copies or reductions: one warp per
+// Data-movement kernels of the layer: the dispatch row scatter (bf16, or quantised to FP8
+// on the way), the RANK_MAJOR / FLAT pick gather and weighted local-pick reduction, the
+// combine gather-reduce, and the one-time weight preparations (gate/up interleave of w1,
+// FP8 block quantisation).  All are HBM-bound copies or reductions: one warp per
 // (row, column chunk), 16-byte vector loads and stores, several loads in flight per lane.
 //
 // Sources: Mooncake EP guide, "Buffer.dispatch(...)" / "Buffer.combine(...)" (send each
@@ -9,6 +10,7 @@
 // layout contracts" (EXPERT_MAJOR reweights per token on combine; RANK_MAJOR / FLAT mask
 // non-local picks to weight 0 and sum without weights across ranks).
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "moe_internal.cuh"
 
@@ -308,6 +310,211 @@ __global__ void __launch_bounds__(kCopyThreads) prepare_w1_kernel(const uint16_t
     for (int c = lane; c < H / 8; c += 32) d[c] = ld_nc_v4(s + c);
 }
 
+// ------------------------------------------------------------------------------- FP8
+// Quantisation rule of a block with largest magnitude amax (float32, IEEE rounding):
+// a = max(amax, 2^-100), scale = a / 448, inv = 448 / a, code = e4m3_rne_satfinite(v * inv).
+__device__ __forceinline__ void fp8_scale(float amax, float &scale, float &inv) {
+    const float a = fmaxf(amax, 0x1p-100f);
+    scale = __fdiv_rn(a, 448.0f);
+    inv = __fdiv_rn(448.0f, a);
+}
+
+// Four e4m3 codes (round to nearest even, saturating) of v0..v3 * inv; v0 in the lowest byte.
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3, float inv) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(v0, inv), __fmul_rn(v1, inv)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(v2, inv), __fmul_rn(v3, inv)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// FP8 dispatch: like dispatch_copy_kernel, but each 128-column block of x[t] is quantised
+// once (16 lanes x 8 columns: the half-warp reduces amax) and the e4m3 codes plus the
+// block scale are written to every receive row of the token.
+struct QuantCopyArgs {
+    const uint16_t *x;
+    uint8_t *recv;          // [nrecv, H] codes
+    float *recv_scales;     // [H/128][nrecv]
+    const int32_t *slot, *recv_row;
+    int T, k, W, H, layout, nchunk;
+    int64_t cap, nrecv;
+};
+
+__global__ void __launch_bounds__(kCopyThreads) dispatch_quant_kernel(QuantCopyArgs a) {
+    __shared__ int64_t dst[kWarpsPerBlock][MOE_MAX_WORLD > MOE_MAX_TOPK ? MOE_MAX_WORLD : MOE_MAX_TOPK];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (token, chunk)
+    const int64_t t = gw / a.nchunk;
+    const int chunk = (int)(gw - t * a.nchunk);
+    if (t >= a.T) return;
+    const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    const int n = em ? a.k : a.W;
+    int nd = 0;
+    for (int q0 = 0; q0 < n; q0 += 32) {
+        int q = q0 + lane;
+        int64_t row = -1;
+        if (q < n) {
+            if (em) {
+                row = a.slot[t * a.k + q];
+            } else {
+                int r = a.recv_row[t * a.W + q];
+                row = r >= 0 ? (int64_t)q * a.cap + r : -1;
+            }
+        }
+        unsigned bal = __ballot_sync(0xffffffffu, row >= 0);
+        if (row >= 0) dst[warp][nd + __popc(bal & ((1u << lane) - 1u))] = row;
+        nd += __popc(bal);
+    }
+    __syncwarp();
+    const int nv = a.H / 8;   // 8-column vectors per row; a 128-column block is 16 of them
+    const int c0 = chunk * 32 * kCopyU + lane;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.x + t * a.H);
+    uint2 q[kCopyU];
+    float sc[kCopyU];
+#pragma unroll
+    for (int u = 0; u < kCopyU; ++u) {
+        const int c = c0 + 32 * u;
+        // c < nv is the same for the 16 lanes of a block (H is a multiple of 128)
+        const uint4 v = c < nv ? ld_nc_v4(src + c) : make_uint4(0, 0, 0, 0);
+        float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float inv;
+        fp8_scale(m, sc[u], inv);
+        q[u].x = e4m3x4(f[0], f[1], f[2], f[3], inv);
+        q[u].y = e4m3x4(f[4], f[5], f[6], f[7], inv);
+    }
+    for (int d = 0; d < nd; ++d) {
+        const int64_t row = dst[warp][d];
+        uint2 *o = reinterpret_cast<uint2 *>(a.recv + row * a.H);
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u) {
+            const int c = c0 + 32 * u;
+            if (c < nv) {
+                o[c] = q[u];
+                if ((lane & 15) == 0) a.recv_scales[(int64_t)(c >> 4) * a.nrecv + row] = sc[u];
+            }
+        }
+    }
+}
+
+// RANK_MAJOR / FLAT, FP8: apick[p] = codes of the pick's receive row, and its scales.
+struct GatherF8Args {
+    const uint8_t *recv;
+    const float *recv_scales;   // [H/128][nrecv]
+    uint8_t *apick;
+    float *apick_scales;        // [H/128][P]
+    const int32_t *offsets, *pick_src, *recv_row;
+    int E, Le, k, W, H, nchunk;
+    int64_t P, cap, nrecv;
+};
+
+__global__ void __launch_bounds__(kCopyThreads) gather_picks_fp8_kernel(GatherF8Args a) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (pick, chunk)
+    const int64_t p = gw / a.nchunk;
+    const int chunk = (int)(gw - p * a.nchunk);
+    if (p >= a.P || p >= a.offsets[a.E]) return;
+    const int e = expert_of_pick(a.offsets, a.E, (int)p);
+    const int i = a.pick_src[p];
+    const int t = i / a.k, d = e / a.Le;
+    const int64_t row = (int64_t)d * a.cap + a.recv_row[(int64_t)t * a.W + d];
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.recv + row * a.H);
+    uint4 *dst = reinterpret_cast<uint4 *>(a.apick + p * a.H);
+    const int nv = a.H / 16;
+    const int c0 = chunk * 32 * kCopyU + lane;
+    uint4 v[kCopyU];
+#pragma unroll
+    for (int u = 0; u < kCopyU; ++u)
+        if (c0 + 32 * u < nv) v[u] = ld_nc_v4(src + c0 + 32 * u);
+#pragma unroll
+    for (int u = 0; u < kCopyU; ++u)
+        if (c0 + 32 * u < nv) dst[c0 + 32 * u] = v[u];
+    if (chunk == 0)
+        for (int b = lane; b < a.H / 128; b += 32)
+            a.apick_scales[(int64_t)b * a.P + p] = a.recv_scales[(int64_t)b * a.nrecv + row];
+}
+
+// 128x128-block quantisation of bf16 weights [E, R, C]: one CTA per block, thread
+// (r, h) = (tid / 2, tid % 2) owns 64 columns of block row r.  With w1_inter = I > 0 the
+// output row blocks are the gate/up interleave of moe_prepare_weights (gate block j ->
+// 2j, up block j -> 2j + 1); scales [E, R/128, C/128] follow the same block order.
+__global__ void __launch_bounds__(256) quantize_blocks_kernel(const uint16_t *w, uint8_t *q, float *sc,
+                                                              int64_t R, int64_t C, int64_t w1_inter) {
+    __shared__ float red[8];
+    const int64_t RB = R / 128, CB = C / 128;
+    const int64_t bid = blockIdx.x;
+    const int64_t e = bid / (RB * CB);
+    const int64_t rem = bid - e * RB * CB;
+    const int64_t rb = rem / CB, cb = rem - (rem / CB) * CB;
+    const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
+    const uint4 *src = reinterpret_cast<const uint4 *>(w + (e * R + rb * 128 + r) * C + cb * 128 + h * 64);
+    float f[64];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 v = ld_nc_v4(src + i);
+        f[8 * i + 0] = bf16_lo(v.x); f[8 * i + 1] = bf16_hi(v.x);
+        f[8 * i + 2] = bf16_lo(v.y); f[8 * i + 3] = bf16_hi(v.y);
+        f[8 * i + 4] = bf16_lo(v.z); f[8 * i + 5] = bf16_hi(v.z);
+        f[8 * i + 6] = bf16_lo(v.w); f[8 * i + 7] = bf16_hi(v.w);
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(f[i]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, red[i]);
+    float scale, inv;
+    fp8_scale(m, scale, inv);
+    int64_t orb = rb;
+    if (w1_inter > 0) {
+        const int64_t IB = w1_inter / 128;
+        orb = rb < IB ? 2 * rb : 2 * (rb - IB) + 1;
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(q + (e * R + orb * 128 + r) * C + cb * 128 + h * 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        dst[i] = make_uint4(e4m3x4(f[16 * i + 0], f[16 * i + 1], f[16 * i + 2], f[16 * i + 3], inv),
+                            e4m3x4(f[16 * i + 4], f[16 * i + 5], f[16 * i + 6], f[16 * i + 7], inv),
+                            e4m3x4(f[16 * i + 8], f[16 * i + 9], f[16 * i + 10], f[16 * i + 11], inv),
+                            e4m3x4(f[16 * i + 12], f[16 * i + 13], f[16 * i + 14], f[16 * i + 15], inv));
+    if (threadIdx.x == 0) sc[(e * RB + orb) * CB + cb] = scale;
+}
+
+// Gate/up interleave of FP8 w1 codes [E, 2I, H] (row permutation of prepare_w1_kernel)
+// and of its block scales [E, 2I/128, H/128].
+__global__ void __launch_bounds__(kCopyThreads) prepare_w1_fp8_kernel(const uint8_t *w1, const float *s1,
+                                                                      uint8_t *w1p, float *s1p,
+                                                                      int64_t rows, int I, int H) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t rp = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
+    if (rp >= rows) return;
+    const int64_t e = rp / (2 * I);
+    const int local = (int)(rp % (2 * I));
+    const int b = local / 256, q = local % 256;
+    const int src_local = q < 128 ? b * 128 + q : I + b * 128 + (q - 128);
+    const uint4 *s = reinterpret_cast<const uint4 *>(w1 + (e * 2 * I + src_local) * (int64_t)H);
+    uint4 *d = reinterpret_cast<uint4 *>(w1p + rp * (int64_t)H);
+    for (int c = lane; c < H / 16; c += 32) d[c] = ld_nc_v4(s + c);
+    if (local % 128 == 0) {   // first row of a 128-row block: move the block's scales
+        const int CB = H / 128;
+        const float *ss = s1 + (e * (2 * I / 128) + src_local / 128) * CB;
+        float *ds = s1p + (e * (2 * I / 128) + local / 128) * CB;
+        for (int c = lane; c < CB; c += 32) ds[c] = ss[c];
+    }
+}
+
 inline unsigned blocks_for(int64_t warps) {
     return (unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
 }
@@ -361,6 +568,45 @@ cudaError_t launch_prepare_w1(const moe_geom &g, const uint16_t *w1, uint16_t *w
     int64_t rows = (int64_t)g.num_experts * 2 * g.intermediate;
     prepare_w1_kernel<<<blocks_for(rows), kCopyThreads, 0, s>>>(w1, w1p, rows, g.intermediate,
                                                                g.hidden);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_quant(const Routing &r, const uint16_t *x, cudaStream_t s) {
+    const Plan &p = *r.p;
+    if (p.T == 0) return cudaSuccess;
+    const int nchunk = (int)((p.H / 8 + 32 * kCopyU - 1) / (32 * kCopyU));
+    QuantCopyArgs a{x, reinterpret_cast<uint8_t *>(r.recv_x), r.recv_scales, r.slot, r.recv_row,
+                    (int)p.T, (int)p.k, (int)p.W, (int)p.H, p.layout, nchunk, p.cap, p.nrecv};
+    dispatch_quant_kernel<<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_picks_fp8(const Routing &r, cudaStream_t s) {
+    const Plan &p = *r.p;
+    if (p.P == 0) return cudaSuccess;
+    const int nchunk = (int)((p.H / 16 + 32 * kCopyU - 1) / (32 * kCopyU));
+    GatherF8Args a{reinterpret_cast<const uint8_t *>(r.recv_x), r.recv_scales,
+                   reinterpret_cast<uint8_t *>(r.apick), r.apick_scales, r.offsets, r.pick_src,
+                   r.recv_row, (int)p.E, (int)(p.E / p.W), (int)p.k, (int)p.W, (int)p.H, nchunk,
+                   p.P, p.cap, p.nrecv};
+    gather_picks_fp8_kernel<<<blocks_for(p.P * nchunk), kCopyThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weights_fp8(const uint16_t *w, int64_t E, int64_t rows, int64_t cols,
+                                        int64_t w1_inter, uint8_t *q, float *sc, cudaStream_t s) {
+    const int64_t blocks = E * (rows / 128) * (cols / 128);
+    if (blocks == 0) return cudaSuccess;
+    if (blocks >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+    quantize_blocks_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, q, sc, rows, cols, w1_inter);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_w1_fp8(const moe_geom &g, const uint8_t *w1q, const float *w1s,
+                                  uint8_t *w1qp, float *w1sp, cudaStream_t s) {
+    int64_t rows = (int64_t)g.num_experts * 2 * g.intermediate;
+    prepare_w1_fp8_kernel<<<blocks_for(rows), kCopyThreads, 0, s>>>(w1q, w1s, w1qp, w1sp, rows,
+                                                                   g.intermediate, g.hidden);
     return cudaGetLastError();
 }
 

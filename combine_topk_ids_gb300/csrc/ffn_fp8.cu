@@ -1,0 +1,425 @@
+// FP8 grouped SwiGLU expert FFN on 5th-generation tensor cores (tcgen05.mma kind::f8f6f4).
+//
+// Operation (Mooncake EP guide, "Buffer.dispatch(...)": with use_fp8 the received rows are
+// FP8 data plus scales; FlashInfer "MoE-EP implementation & usage", section 2 "Call
+// stack": a pure per-expert grouped GEMM; section 4 step 1: w1 [E, 2I, H], w2 [E, H, I]),
+// on e4m3 rows with one float32 scale per 128 columns and e4m3 weights with one scale per
+// 128 x 128 block:
+//     GEMM1   h   = sum over k-blocks kb of  sa[row, kb] * sw1[n-block, kb] * (xq . w1q)_kb
+//     SwiGLU  act = silu(h[:, :I]) * h[:, I:]                                 fp32
+//             act -> e4m3 codes + one scale per 128 columns (the second GEMM's A operand)
+//     GEMM2   y   = sum over kb of  sa_act[row, kb] * sw2[n-block, kb] * (aq . w2q)_kb   fp32
+// A k-block is 128 columns, the block size of every scale, so each k-block's product sum
+// (four K=32 MMAs, exact e4m3 products accumulated in fp32 in tensor memory) is scaled as a
+// whole and added to an fp32 register accumulator: the "promotion" of the partial sum.
+//
+// One persistent kernel per GEMM, one CTA per SM, 384 threads:
+//   warp 0      TMA producer: 128 x 128 B A tile + up to 256 x 128 B B tile per stage
+//               (SWIZZLE_128B, the same byte layout as the bf16 kernel's 64-column tiles),
+//               4-stage mbarrier ring
+//   warp 1      MMA issuer: per k-block four tcgen05.mma.cta_group::1.kind::f8f6f4 (M=128,
+//               N=256 or 128, K=32) into one of two 256-column TMEM partial-sum buffers
+//   warp 2      TMEM allocator (512 columns)
+//   warps 4-11  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).., warps 4-7 and 8-11
+//               split the columns; per k-block they load the partial sums (tcgen05.ld),
+//               multiply by row scale x weight-block scale and add into registers, then
+//               release the buffer; after the last k-block they write the tile
+//               (GEMM1: SwiGLU, per-row amax over the tile's 128 activation columns
+//               exchanged between the two warps of a lane quarter, e4m3 codes + scale;
+//               GEMM2: fp32 rows)
+// The tile order, bounded waits and abort path are those of the bf16 kernel (ffn_tc.cu).
+#include <cuda.h>
+#include <cuda_fp8.h>
+
+#include "tc_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int F_BM = 128;                       // rows per tile
+constexpr int F_BN = 256;                       // widest n-tile
+constexpr int F_BK = 128;                       // k elements (bytes) per stage
+constexpr int F_A_BYTES = F_BM * F_BK;          // 16 KB
+constexpr int F_B_BYTES = F_BN * F_BK;          // 32 KB
+constexpr int F_STAGE = F_A_BYTES + F_B_BYTES;  // 48 KB
+constexpr int F_STAGES = 4;
+constexpr int F_THREADS = 384;
+constexpr int F_EPI_WARPS = 8;
+constexpr int F_TMEM_COLS = 512;                // two 128 x 256 fp32 partial-sum buffers
+constexpr int F_RED_BUFS = 4;                   // amax exchange buffers (tiles in flight)
+// ring | barriers (256 B) | amax exchange [4][2][128] floats
+constexpr int F_SMEM = F_STAGES * F_STAGE + 1024 /*align*/ + 256 + F_RED_BUFS * 2 * 128 * 4;
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B
+// e4m3 (format 0 in bits 7-9 and 10-12), both K-major (bits 15/16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc_f8(int m, int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+struct F8Args {
+    const int32_t *counts, *offsets;
+    const int32_t *mprefix;   // prefix over experts of ceil(rows / 128)
+    int E;
+    int bn;                   // n-tile width: 256 or 128
+    int nb;                   // n-blocks per expert (N / bn)
+    int kb;                   // k-blocks (K / 128)
+    int a_mode;               // 0: A row = e*a_cap + m; 1: A row = offsets[e] + m
+    int64_t a_cap;
+    const float *a_scale;     // [K/128][a_scale_ld]: scale of A row r, k-block kb
+    int64_t a_scale_ld;
+    int64_t b_rows;           // rows of B per expert (N)
+    const float *b_scale;     // [E][N/128][K/128]
+    int mode;                 // 0: SwiGLU -> e4m3 act + scales; 1: fp32 rows
+    void *out;                // mode 0: act codes [P, I]; mode 1: fp32 rows
+    float *out_scale;         // mode 0: act scales [I/128][out_scale_ld]
+    int64_t out_scale_ld;
+    int64_t out_ld;           // elements per output row
+    int out_mode;             // 0: row = e*out_cap + m; 1: row = offsets[e] + m
+    int64_t out_cap;
+    int32_t *status;
+};
+
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void decode_tile_f8(const F8Args &a, int tile, int &e, int &mb, int &nbk) {
+    const int q = tile / a.nb;
+    int lo = 0, hi = a.E - 1;   // largest e with mprefix[e] <= q
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.mprefix + mid) <= q) lo = mid;
+        else hi = mid - 1;
+    }
+    e = lo;
+    const int m0 = __ldg(a.mprefix + e);
+    const int mt = __ldg(a.mprefix + e + 1) - m0;
+    const int local = tile - m0 * a.nb;
+    nbk = local / mt;
+    mb = local - nbk * mt;
+}
+
+__device__ __forceinline__ void fp8_scale_dev(float amax, float &scale, float &inv) {
+    const float a = fmaxf(amax, 0x1p-100f);
+    scale = __fdiv_rn(a, 448.0f);
+    inv = __fdiv_rn(448.0f, a);
+}
+
+__device__ __forceinline__ uint32_t e4m3x4_dev(float v0, float v1, float v2, float v3, float inv) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(v0, inv), __fmul_rn(v1, inv)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(v2, inv), __fmul_rn(v3, inv)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+// acc[base + i] += c * partial[col + i], i < 16, for this warp's 32 TMEM lanes
+template <int BASE>
+__device__ __forceinline__ void promote16(float (&acc)[128], uint32_t taddr, float c) {
+    uint32_t v[16];
+    tmem_ld16(taddr, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[BASE + i] = fmaf(__uint_as_float(v[i]), c, acc[BASE + i]);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(F_THREADS, 1)
+    ffn_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        F8Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;                          // [STAGES] A tiles
+    uint8_t *sB = smem + F_STAGES * F_A_BYTES;   // [STAGES] B tiles
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + F_STAGES * F_STAGE);
+    // bars: full[STAGES], empty[STAGES], pfull[2], pempty[2], xfull[F_RED_BUFS]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * F_STAGES + 4 + F_RED_BUFS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *red = reinterpret_cast<float *>(smem + F_STAGES * F_STAGE + 256);   // [4][2][128]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + F_STAGES);
+    const uint32_t pfull0 = smem_u32(bars + 2 * F_STAGES), pempty0 = smem_u32(bars + 2 * F_STAGES + 2);
+    const uint32_t xfull0 = smem_u32(bars + 2 * F_STAGES + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < F_STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(pfull0 + 8 * s, 1);
+            mbar_init(pempty0 + 8 * s, F_EPI_WARPS);   // one arrival per promotion warp
+        }
+        for (int s = 0; s < F_RED_BUFS; ++s) mbar_init(xfull0 + 8 * s, F_EPI_WARPS);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(F_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = __ldg(a.mprefix + a.E) * a.nb;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------- TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        const uint32_t tx = (uint32_t)(F_A_BYTES + a.bn * F_BK);
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            int e, mb, nbk;
+            decode_tile_f8(a, tile, e, mb, nbk);
+            const int64_t arow = (a.a_mode == 0 ? (int64_t)e * a.a_cap : (int64_t)__ldg(a.offsets + e)) +
+                                 (int64_t)mb * F_BM;
+            const int64_t brow = (int64_t)e * a.b_rows + (int64_t)nbk * a.bn;
+            for (int kb = 0; kb < a.kb; ++kb) {
+                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+                const uint32_t fb = full0 + 8 * stage;
+                mbar_expect_tx(fb, tx);
+                tma_load_2d(smem_u32(sA + stage * F_A_BYTES), &tmA, kb * F_BK, (int)arow, fb);
+                tma_load_2d(smem_u32(sB + stage * F_B_BYTES), &tmB, kb * F_BK, (int)brow, fb);
+                if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------------- MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t it = 0;   // k-blocks issued so far (partial-sum buffer it & 1)
+        bool ok = true;
+        const uint32_t idesc = make_idesc_f8(F_BM, a.bn);
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int kb = 0; kb < a.kb; ++kb, ++it) {
+                const uint32_t pb = it & 1, pph = (it >> 1) & 1;
+                if (!mbar_wait(pempty0 + 8 * pb, pph ^ 1, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + pb * (uint32_t)F_BN;
+                const uint32_t a0 = smem_u32(sA + stage * F_A_BYTES);
+                const uint32_t b0 = smem_u32(sB + stage * F_B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < F_BK / 32; ++kk)
+                    mma_f8(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, kk != 0 ? 1u : 0u);
+                mma_commit(empty0 + 8 * stage);   // the stage is reusable once these finish
+                mma_commit(pfull0 + 8 * pb);      // the partial sum is ready
+                if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
+    } else if (warp >= 4) {
+        // -------------------------------------------------------- promotion + epilogue
+        const int quad = warp & 3;                  // TMEM lanes 32*quad .. 32*quad+31
+        const int half = (warp - 4) >> 2;           // which columns of the tile
+        const int row = quad * 32 + lane;           // row inside the tile
+        // columns of this thread: GEMM1 gate [64h, 64h+64) and up [128+64h, ...);
+        // GEMM2 [h*bn/2, (h+1)*bn/2)
+        const int ncol = MODE == 0 ? 64 : a.bn / 2;
+        uint32_t it = 0;
+        int ntile = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++ntile) {
+            int e, mb, nbk;
+            decode_tile_f8(a, tile, e, mb, nbk);
+            const int m0 = mb * F_BM;
+            const bool live = row < __ldg(a.counts + e) - m0;
+            const int64_t arow = (a.a_mode == 0 ? (int64_t)e * a.a_cap : (int64_t)__ldg(a.offsets + e)) +
+                                 (int64_t)m0 + row;
+            const int bblocks = (int)(a.b_rows / 128);
+            const int blk0 = MODE == 0 ? 2 * nbk : (a.bn == 256 ? 2 * nbk + half : nbk);
+            const float *sb0p = a.b_scale + ((int64_t)e * bblocks + blk0) * a.kb;
+            const float *sb1p = sb0p + a.kb;   // GEMM1: the up block (2 * nbk + 1)
+            float acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+            float sa_n = live ? __ldg(a.a_scale + arow) : 0.f;
+            float sb0_n = __ldg(sb0p), sb1_n = MODE == 0 ? __ldg(sb1p) : 0.f;
+            for (int kb = 0; kb < a.kb; ++kb, ++it) {
+                const float sa = sa_n, sb0 = sb0_n, sb1 = sb1_n;
+                if (kb + 1 < a.kb) {   // next k-block's scales, loaded while this one waits
+                    sa_n = live ? __ldg(a.a_scale + (int64_t)(kb + 1) * a.a_scale_ld + arow) : 0.f;
+                    sb0_n = __ldg(sb0p + kb + 1);
+                    if (MODE == 0) sb1_n = __ldg(sb1p + kb + 1);
+                }
+                const uint32_t pb = it & 1, pph = (it >> 1) & 1;
+                if (!mbar_wait(pfull0 + 8 * pb, pph, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t tb = tmem_base + pb * (uint32_t)F_BN + ((uint32_t)(quad * 32) << 16);
+                const float c0 = sa * sb0;
+                if (MODE == 0) {
+                    const float c1 = sa * sb1;
+                    const uint32_t g0 = tb + 64 * half, u0 = tb + 128 + 64 * half;
+                    promote16<0>(acc, g0 + 0, c0);
+                    promote16<16>(acc, g0 + 16, c0);
+                    promote16<32>(acc, g0 + 32, c0);
+                    promote16<48>(acc, g0 + 48, c0);
+                    promote16<64>(acc, u0 + 0, c1);
+                    promote16<80>(acc, u0 + 16, c1);
+                    promote16<96>(acc, u0 + 32, c1);
+                    promote16<112>(acc, u0 + 48, c1);
+                } else {
+                    const uint32_t t0 = tb + (uint32_t)(ncol * half);
+                    promote16<0>(acc, t0 + 0, c0);
+                    promote16<16>(acc, t0 + 16, c0);
+                    promote16<32>(acc, t0 + 32, c0);
+                    promote16<48>(acc, t0 + 48, c0);
+                    if (ncol == 128) {
+                        promote16<64>(acc, t0 + 64, c0);
+                        promote16<80>(acc, t0 + 80, c0);
+                        promote16<96>(acc, t0 + 96, c0);
+                        promote16<112>(acc, t0 + 112, c0);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pempty0 + 8 * pb);   // buffer free for k-block it + 2
+            }
+            if (!ok) break;
+            const int64_t orow = (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) +
+                                 (int64_t)m0 + row;
+            if (MODE == 0) {
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    acc[i] = silu_mul(acc[i], acc[64 + i]);
+                    amax = fmaxf(amax, fabsf(acc[i]));
+                }
+                // the row's other 64 activation columns live in the other warp of this
+                // lane quarter: exchange the partial amax through shared memory
+                const int rb = ntile % F_RED_BUFS;
+                float *rbuf = red + rb * 256;
+                rbuf[half * 128 + row] = amax;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xfull0 + 8 * rb);
+                if (!mbar_wait(xfull0 + 8 * rb, (uint32_t)(ntile / F_RED_BUFS) & 1, abort_flag, a.status)) break;
+                amax = fmaxf(rbuf[row], rbuf[128 + row]);
+                float scale, inv;
+                fp8_scale_dev(amax, scale, inv);
+                if (live) {
+                    uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(a.out) +
+                                                         orow * a.out_ld + (int64_t)nbk * 128 + half * 64);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        o[v] = make_uint4(
+                            e4m3x4_dev(acc[16 * v + 0], acc[16 * v + 1], acc[16 * v + 2], acc[16 * v + 3], inv),
+                            e4m3x4_dev(acc[16 * v + 4], acc[16 * v + 5], acc[16 * v + 6], acc[16 * v + 7], inv),
+                            e4m3x4_dev(acc[16 * v + 8], acc[16 * v + 9], acc[16 * v + 10], acc[16 * v + 11], inv),
+                            e4m3x4_dev(acc[16 * v + 12], acc[16 * v + 13], acc[16 * v + 14], acc[16 * v + 15], inv));
+                    if (half == 0) a.out_scale[(int64_t)nbk * a.out_scale_ld + orow] = scale;
+                }
+            } else if (live) {
+                float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + orow * a.out_ld +
+                                                       (int64_t)nbk * a.bn + half * ncol);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                if (ncol == 128) {
+#pragma unroll
+                    for (int q = 16; q < 32; ++q)
+                        o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag) {
+        // Give in-flight TMA copies and MMAs time to land before the memory is released.
+        unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 1000000ull) {}
+    }
+    if (warp == 2) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(F_TMEM_COLS)
+                     : "memory");
+    }
+}
+
+template <int MODE>
+int launch_gemm_fp8(const CUtensorMap &ma, const CUtensorMap &mb, const F8Args &args, int64_t max_tiles,
+                    cudaStream_t s) {
+    if (max_tiles <= 0) return MOE_OK;
+    auto kernel = ffn_gemm_fp8_kernel<MODE>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
+    });
+    if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+    int grid = num_sms();
+    if ((int64_t)grid > max_tiles) grid = (int)max_tiles;
+    kernel<<<grid, F_THREADS, F_SMEM, s>>>(ma, mb, args);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+bool make_map_u8(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows) {
+    return make_map_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, cols, box_rows);
+}
+
+F8Args base_args_f8(const Routing &r) {
+    const Plan &p = *r.p;
+    F8Args g{};
+    g.counts = r.counts; g.offsets = r.offsets; g.mprefix = r.mprefix;
+    g.E = (int)p.E;
+    g.status = r.status;
+    return g;
+}
+
+}  // namespace
+
+int launch_gemm1_fp8(const Routing &r, const uint8_t *w1qp, const float *w1sp, cudaStream_t s) {
+    const Plan &p = *r.p;
+    if (p.P == 0) return MOE_OK;
+    const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    CUtensorMap mA, mB;
+    const void *a1 = em ? (const void *)r.recv_x : (const void *)r.apick;
+    const int64_t a1_rows = em ? p.E * p.cap : p.P;
+    if (!make_map_u8(&mA, a1, a1_rows, p.H, F_BM) || !make_map_u8(&mB, w1qp, p.E * 2 * p.I, p.H, F_BN))
+        return MOE_ERR_CUDA;
+    F8Args g = base_args_f8(r);
+    g.bn = F_BN; g.nb = (int)(2 * p.I / F_BN); g.kb = (int)(p.H / F_BK);
+    g.a_mode = em ? 0 : 1; g.a_cap = p.cap;
+    g.a_scale = em ? r.recv_scales : r.apick_scales; g.a_scale_ld = em ? p.nrecv : p.P;
+    g.b_rows = 2 * p.I; g.b_scale = w1sp;
+    g.mode = 0; g.out = r.act; g.out_scale = r.act_scales; g.out_scale_ld = p.P;
+    g.out_ld = p.I; g.out_mode = 1; g.out_cap = 0;
+    return launch_gemm_fp8<0>(mA, mB, g, (p.P / F_BM + p.E) * g.nb, s);
+}
+
+int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, float *expert_out,
+                     cudaStream_t s) {
+    const Plan &p = *r.p;
+    if (p.P == 0) return MOE_OK;
+    const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    const int bn = (p.H % 256 == 0) ? 256 : 128;
+    CUtensorMap mA, mB;
+    if (!make_map_u8(&mA, r.act, p.P, p.I, F_BM) || !make_map_u8(&mB, w2q, p.E * p.H, p.I, bn))
+        return MOE_ERR_CUDA;
+    F8Args g = base_args_f8(r);
+    g.bn = bn; g.nb = (int)(p.H / bn); g.kb = (int)(p.I / F_BK);
+    g.a_mode = 1; g.a_cap = 0; g.a_scale = r.act_scales; g.a_scale_ld = p.P;
+    g.b_rows = p.H; g.b_scale = w2s;
+    g.mode = 1; g.out_ld = p.H;
+    if (em) { g.out = expert_out; g.out_mode = 0; g.out_cap = p.cap; }
+    else { g.out = r.ypick; g.out_mode = 1; g.out_cap = 0; }
+    return launch_gemm_fp8<1>(mA, mB, g, (p.P / F_BM + p.E) * g.nb, s);
+}
+
+}  // namespace moe

@@ -51,7 +51,8 @@ int make_plan(const moe_geom &g, Plan *p) {
     if (g.world < 1 || g.max_tok < 1 || g.num_tokens < 0 || g.hidden < 1 || g.num_experts < 1 ||
         g.intermediate < 1)
         return MOE_ERR_INVALID_ARGUMENT;
-    if (g.layout < 0 || g.layout > 2 || g.algorithm < 0 || g.algorithm > 1)
+    if (g.layout < 0 || g.layout > 2 || g.algorithm < 0 || g.algorithm > 1 || g.quant < 0 ||
+        g.quant > 1)
         return MOE_ERR_INVALID_ARGUMENT;
     if (g.top_k < 1 || g.top_k > MOE_MAX_TOPK) return MOE_ERR_TOPK;
     if (g.num_experts % g.world != 0) return MOE_ERR_EXPERTS_NOT_DIVISIBLE;
@@ -70,6 +71,7 @@ int make_plan(const moe_geom &g, Plan *p) {
     Plan &q = *p;
     q.T = g.num_tokens; q.W = g.world; q.Tr = g.max_tok; q.cap = cap; q.E = g.num_experts;
     q.k = g.top_k; q.H = g.hidden; q.I = g.intermediate; q.P = P; q.layout = g.layout;
+    q.quant = g.quant;
     // routing chunk: about 256 chunks over the whole capacity, 32..1024 tokens each
     int64_t want = (cap + 255) / 256;
     int tb = 32;
@@ -79,7 +81,10 @@ int make_plan(const moe_geom &g, Plan *p) {
     q.nb = g.world * q.nbpr;
 
     const bool em = g.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    const bool f8 = g.quant == MOE_QUANT_FP8_E4M3;
     const int64_t E = q.E, W = q.W, k = q.k, H = q.H, I = q.I, nb = q.nb;
+    const int64_t eb = f8 ? 1 : 2;   // bytes per element of rows and activations
+    q.nrecv = (em ? E : W) * cap;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;
@@ -105,10 +110,13 @@ int make_plan(const moe_geom &g, Plan *p) {
     q.recv_topk_w = take(em ? 0 : 4 * W * cap * k);
     q.blk_dhist = take(4 * W * nb);
     q.blk_dbase = take(4 * W * nb);
-    q.recv_x = take(2 * (em ? E : W) * cap * H);
-    q.act = take(2 * P * I);
-    q.act_lo = take(2 * P * I);
-    q.apick = take(em ? 0 : 2 * P * H);
+    q.recv_x = take(eb * q.nrecv * H);
+    q.recv_scales = take(f8 ? 4 * q.nrecv * (H / 128) : 0);
+    q.act = take(eb * P * I);
+    q.act_lo = take(f8 ? 0 : 2 * P * I);
+    q.act_scales = take(f8 ? 4 * P * (I / 128) : 0);
+    q.apick = take(em ? 0 : eb * P * H);
+    q.apick_scales = take(em || !f8 ? 0 : 4 * P * (H / 128));
     q.ypick = take(em ? 0 : 4 * P * H);
     q.total = off;
     return MOE_OK;
@@ -132,6 +140,11 @@ Routing carve(const Plan &p, void *ws) {
     r.act_lo = reinterpret_cast<uint16_t *>(b + p.act_lo);
     r.apick = reinterpret_cast<uint16_t *>(b + p.apick);
     r.ypick = reinterpret_cast<float *>(b + p.ypick);
+    const bool f8 = p.quant == MOE_QUANT_FP8_E4M3;
+    r.recv_scales = f8 ? reinterpret_cast<float *>(b + p.recv_scales) : nullptr;
+    r.act_scales = f8 ? reinterpret_cast<float *>(b + p.act_scales) : nullptr;
+    r.apick_scales = f8 && p.layout != MOE_LAYOUT_EXPERT_MAJOR ? reinterpret_cast<float *>(b + p.apick_scales)
+                                                               : nullptr;
     return r;
 }
 
@@ -203,6 +216,9 @@ int moe_dispatch(const moe_geom *g, const void *x_dev, const void *topk_ids_dev,
     h->num_events = num_events;
     h->geom = *g;
     h->recv_x = r.recv_x;
+    h->recv_scales = r.recv_scales;
+    h->ffn_act = r.act;
+    h->ffn_act_scales = r.act_scales;
     h->counts = r.counts;
     h->offsets = r.offsets;
     h->pick_pos = r.pick_pos;
@@ -227,8 +243,10 @@ int moe_dispatch(const moe_geom *g, const void *x_dev, const void *topk_ids_dev,
                        active_ranks_dev, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     record(h, MOE_EV_ROUTING_END, s);
-    if (launch_dispatch_copy(r, static_cast<const uint16_t *>(x_dev), s) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    const cudaError_t ce = p.quant == MOE_QUANT_FP8_E4M3
+                               ? launch_dispatch_quant(r, static_cast<const uint16_t *>(x_dev), s)
+                               : launch_dispatch_copy(r, static_cast<const uint16_t *>(x_dev), s);
+    if (ce != cudaSuccess) return MOE_ERR_CUDA;
     record(h, MOE_EV_DISPATCH_END, s);
     h->magic = kHandleMagic;
     return MOE_OK;
@@ -254,6 +272,7 @@ int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void 
     int rc = handle_plan(h, &p);
     if (rc != MOE_OK) return rc;
     if (!w1_prepared_dev || !w2_dev || !expert_out_dev) return MOE_ERR_INVALID_ARGUMENT;
+    if (p.quant != MOE_QUANT_NONE) return MOE_ERR_INVALID_ARGUMENT;   // moe_expert_ffn_fp8
     if (!aligned(w1_prepared_dev, 16) || !aligned(w2_dev, 16) || !aligned(expert_out_dev, 16))
         return MOE_ERR_MISALIGNED;
     if ((rc = check_device()) != MOE_OK) return rc;
@@ -271,6 +290,80 @@ int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void 
     if (!em && launch_reduce_ranks(r, expert_out_dev, s) != cudaSuccess) return MOE_ERR_CUDA;
     record(h, MOE_EV_FFN_END, s);
     return MOE_OK;
+}
+
+int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
+                       const float *w1_scales_prepared_dev, const void *w2q_dev,
+                       const float *w2_scales_dev, float *expert_out_dev, void *stream) {
+    Plan p;
+    int rc = handle_plan(h, &p);
+    if (rc != MOE_OK) return rc;
+    if (p.quant != MOE_QUANT_FP8_E4M3) return MOE_ERR_INVALID_ARGUMENT;
+    if (!w1q_prepared_dev || !w1_scales_prepared_dev || !w2q_dev || !w2_scales_dev || !expert_out_dev)
+        return MOE_ERR_INVALID_ARGUMENT;
+    if (!aligned(w1q_prepared_dev, 16) || !aligned(w2q_dev, 16) || !aligned(expert_out_dev, 16) ||
+        !aligned(w1_scales_prepared_dev, 4) || !aligned(w2_scales_dev, 4))
+        return MOE_ERR_MISALIGNED;
+    if ((rc = check_device()) != MOE_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Routing r = carve(p, h->workspace);
+    const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    record(h, MOE_EV_FFN_BEGIN, s);
+    if (!em && launch_gather_picks_fp8(r, s) != cudaSuccess) return MOE_ERR_CUDA;
+    record(h, MOE_EV_GATHER_END, s);
+    if ((rc = launch_gemm1_fp8(r, static_cast<const uint8_t *>(w1q_prepared_dev), w1_scales_prepared_dev,
+                               s)) != MOE_OK)
+        return rc;
+    record(h, MOE_EV_GEMM1_END, s);
+    if ((rc = launch_gemm2_fp8(r, static_cast<const uint8_t *>(w2q_dev), w2_scales_dev, expert_out_dev,
+                               s)) != MOE_OK)
+        return rc;
+    record(h, MOE_EV_GEMM2_END, s);
+    if (!em && launch_reduce_ranks(r, expert_out_dev, s) != cudaSuccess) return MOE_ERR_CUDA;
+    record(h, MOE_EV_FFN_END, s);
+    return MOE_OK;
+}
+
+int moe_quantize_weights_fp8(const moe_geom *g, const void *w1_dev, const void *w2_dev,
+                             void *w1q_prepared_dev, float *w1_scales_prepared_dev, void *w2q_dev,
+                             float *w2_scales_dev, void *stream) {
+    if (!g || !w1_dev || !w2_dev || !w1q_prepared_dev || !w1_scales_prepared_dev || !w2q_dev ||
+        !w2_scales_dev)
+        return MOE_ERR_INVALID_ARGUMENT;
+    Plan p;
+    int rc = make_plan(*g, &p);
+    if (rc != MOE_OK) return rc;
+    if (!aligned(w1_dev, 16) || !aligned(w2_dev, 16) || !aligned(w1q_prepared_dev, 16) ||
+        !aligned(w2q_dev, 16) || !aligned(w1_scales_prepared_dev, 4) || !aligned(w2_scales_dev, 4))
+        return MOE_ERR_MISALIGNED;
+    if ((rc = check_device()) != MOE_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_quantize_weights_fp8(static_cast<const uint16_t *>(w1_dev), p.E, 2 * p.I, p.H, p.I,
+                                    static_cast<uint8_t *>(w1q_prepared_dev), w1_scales_prepared_dev,
+                                    s) != cudaSuccess ||
+        launch_quantize_weights_fp8(static_cast<const uint16_t *>(w2_dev), p.E, p.H, p.I, 0,
+                                    static_cast<uint8_t *>(w2q_dev), w2_scales_dev, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_prepare_weights_fp8(const moe_geom *g, const void *w1q_dev, const float *w1_scales_dev,
+                            void *w1q_prepared_dev, float *w1_scales_prepared_dev, void *stream) {
+    if (!g || !w1q_dev || !w1_scales_dev || !w1q_prepared_dev || !w1_scales_prepared_dev ||
+        w1q_dev == w1q_prepared_dev || (const void *)w1_scales_dev == (const void *)w1_scales_prepared_dev)
+        return MOE_ERR_INVALID_ARGUMENT;
+    Plan p;
+    int rc = make_plan(*g, &p);
+    if (rc != MOE_OK) return rc;
+    if (!aligned(w1q_dev, 16) || !aligned(w1q_prepared_dev, 16) || !aligned(w1_scales_dev, 4) ||
+        !aligned(w1_scales_prepared_dev, 4))
+        return MOE_ERR_MISALIGNED;
+    if ((rc = check_device()) != MOE_OK) return rc;
+    return launch_prepare_w1_fp8(*g, static_cast<const uint8_t *>(w1q_dev), w1_scales_dev,
+                                 static_cast<uint8_t *>(w1q_prepared_dev), w1_scales_prepared_dev,
+                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 int moe_combine(const moe_handle *h, const float *expert_out_dev, const float *topk_weights_dev,
@@ -305,6 +398,7 @@ int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids
     Plan p;
     int rc = make_plan(*g, &p);
     if (rc != MOE_OK) return rc;
+    if (p.quant != MOE_QUANT_NONE) return MOE_ERR_INVALID_ARGUMENT;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p.T > 0) {
         if (!x_host || !topk_ids_host || !topk_weights_host || !out_host || !x_dev ||

@@ -19,12 +19,15 @@ constexpr uint64_t kHandleMagic = 0x4d6f4545702d3130ull;
 struct Plan {
     int64_t T, W, Tr, cap, E, k, H, I, P;   // P = T*k picks
     int layout;
+    int quant;      // moe_quant
+    int64_t nrecv;  // rows of the receive buffer: E*cap (EM) or W*cap (RM/FLAT)
     int tb;         // tokens per routing block
     int nbpr;       // routing blocks per logical rank
     int nb;         // routing blocks in total (W * nbpr)
     size_t status, counts, offsets, mprefix, mprefix2, pick_pos, pick_src, slot, layout_range,
         blk_hist, blk_base, recv_row, recv_count, num_recv, recv_src, recv_topk_idx,
-        recv_topk_w, blk_dhist, blk_dbase, recv_x, act, act_lo, apick, ypick, total;
+        recv_topk_w, blk_dhist, blk_dbase, recv_x, recv_scales, act, act_lo, act_scales, apick,
+        apick_scales, ypick, total;
 };
 
 // Returns MOE_OK or a moe_error for an invalid geometry.
@@ -39,6 +42,9 @@ struct Routing {
     float *recv_topk_w;
     uint16_t *recv_x, *act, *act_lo, *apick;   // act / act_lo: SwiGLU output as a bf16 pair
     float *ypick;
+    // FP8 geometry: recv_x / act / apick hold e4m3 codes (one byte per element); their
+    // scales are column-block major ([cols/128][rows]); act_lo is unused
+    float *recv_scales, *act_scales, *apick_scales;
 };
 
 Routing carve(const Plan &p, void *ws);
@@ -58,6 +64,19 @@ cudaError_t launch_prepare_w1(const moe_geom &g, const uint16_t *w1, uint16_t *w
 // per-pick scratch (RM/FLAT).  Return MOE_OK or a moe_error.
 int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s);
 int launch_gemm2(const Routing &r, const uint16_t *w2, float *expert_out, cudaStream_t s);
+
+// ---- FP8 (moe_quant MOE_QUANT_FP8_E4M3) -----------------------------------------------
+cudaError_t launch_dispatch_quant(const Routing &r, const uint16_t *x, cudaStream_t s);
+cudaError_t launch_gather_picks_fp8(const Routing &r, cudaStream_t s);
+// 128x128-block quantisation of bf16 [E, rows, cols] weights; w1_inter = I interleaves the
+// gate/up row blocks of W1 (0: keep the order)
+cudaError_t launch_quantize_weights_fp8(const uint16_t *w, int64_t E, int64_t rows, int64_t cols,
+                                        int64_t w1_inter, uint8_t *q, float *sc, cudaStream_t s);
+cudaError_t launch_prepare_w1_fp8(const moe_geom &g, const uint8_t *w1q, const float *w1s,
+                                  uint8_t *w1qp, float *w1sp, cudaStream_t s);
+int launch_gemm1_fp8(const Routing &r, const uint8_t *w1qp, const float *w1sp, cudaStream_t s);
+int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, float *expert_out,
+                     cudaStream_t s);
 
 int num_sms();   // SM count of the current device (cached per device)
 

@@ -34,6 +34,7 @@ class MoeConfig:
     seed: int = 0
     ids_dtype: str = "int64"
     mask_frac: float = 0.0   # fraction of picks replaced by -1 (masked picks)
+    quant: str = "bf16"      # "bf16" | "fp8": FP8 dispatch and FP8 expert GEMMs
 
     @property
     def tokens(self) -> int:
@@ -94,7 +95,10 @@ SMALL.update({
                              layout="FLAT", algo="HT", routing="uniform", T=4300, mask_frac=0.1),
 })
 
-ALL = {**CONFIGS, **SMALL}
+# The same workloads with FP8 dispatch and FP8 expert GEMMs (use_fp8).
+FP8 = {name + "_fp8": cfg.with_(name=name + "_fp8", quant="fp8") for name, cfg in CONFIGS.items()}
+
+ALL = {**CONFIGS, **SMALL, **FP8}
 
 # A smaller EXPERT_MAJOR case for detailed (multi-pass) profiler captures of the same
 # kernels: 4 experts, weights 0.7 GB (larger than L2), about 1.3 GB on the device.

@@ -56,6 +56,22 @@ typedef enum { MOE_ALGO_LOW_LATENCY = 0, MOE_ALGO_HIGH_THROUGHPUT = 1 } moe_algo
 
 typedef enum { MOE_IDS_INT32 = 0, MOE_IDS_INT64 = 1 } moe_ids_dtype;
 
+/*
+ * Precision of the received rows and of the expert GEMMs [MC-EP Buffer.dispatch use_fp8:
+ * with it the dispatch returns (packed FP8 data, packed scales) instead of bf16 rows].
+ *   MOE_QUANT_NONE      bf16 rows, bf16 x bf16 -> fp32 GEMMs (moe_expert_ffn).
+ *   MOE_QUANT_FP8_E4M3  the dispatch quantises every token row to OCP e4m3 ("fn": bias 7,
+ *                       largest finite 448, no infinities) with one float32 scale per 128
+ *                       columns; the FFN (moe_expert_ffn_fp8) runs e4m3 x e4m3 -> fp32
+ *                       GEMMs on FP8 weights with one scale per 128 x 128 block and
+ *                       quantises the SwiGLU activation the same way per 128 columns.
+ *   Quantisation of a block with largest magnitude amax (all float32, IEEE rounding):
+ *       a = max(amax, 2^-100); scale = a / 448; code = e4m3_rne_satfinite(v * (448 / a));
+ *   the dequantised value is code * scale.  The page leaves the scale granularity and
+ *   rule open; this is the library's reading.
+ */
+typedef enum { MOE_QUANT_NONE = 0, MOE_QUANT_FP8_E4M3 = 1 } moe_quant;
+
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARGUMENT = -1,      /* null pointer, non-positive size, bad enum          */
@@ -110,6 +126,7 @@ typedef struct {
     int32_t intermediate; /* I: SwiGLU FFN width, multiple of 128                          */
     int32_t layout;       /* moe_layout                                                    */
     int32_t algorithm;    /* moe_algorithm                                                 */
+    int32_t quant;        /* moe_quant: precision of the received rows and expert GEMMs    */
 } moe_geom;
 
 /*
@@ -122,9 +139,14 @@ typedef struct {
  */
 typedef struct {
     moe_geom geom;
-    void *recv_x;              /* bf16. EM: [E, cap, H]; RM: [W(dst), W(src)*Tr, H];
+    void *recv_x;              /* bf16 (FP8: e4m3 codes, one byte each).
+                                  EM: [E, cap, H]; RM: [W(dst), W(src)*Tr, H];
                                   FLAT: [W(dst), cap, H].  Rows past the counts are
                                   unspecified and never read.                            */
+    float *recv_scales;        /* FP8 only (else NULL): scales of recv_x, column-block
+                                  major: scale of row r, columns [128b, 128b+128) at
+                                  recv_scales[b * nrows + r], nrows = E*cap (EM) or
+                                  W*cap (RM/FLAT)                                        */
     int32_t *counts;           /* [E] rows of expert e (packed_recv_count)               */
     int32_t *offsets;          /* [E+1] exclusive prefix of counts: the expert-grouped
                                   pick list of the FFN                                   */
@@ -144,6 +166,12 @@ typedef struct {
                                   pick [FI-3], int32                                     */
     float *recv_topk_weights;  /* RM/FLAT: [W][cap][k] topk weight, 0 for non-local      */
     int32_t *status;           /* device status word (MOE_STATUS_* bits)                 */
+    void *ffn_act;             /* written by the FFN: the SwiGLU activation, [R, I] in
+                                  pick-list order (row offsets[e] + position), the second
+                                  GEMM's operand.  bf16: the high half of the bf16 pair;
+                                  FP8: e4m3 codes                                        */
+    float *ffn_act_scales;     /* FP8 only (else NULL): scales of ffn_act, column-block
+                                  major [I/128][T*k] (row p, block b at b*T*k + p)        */
     void *workspace;           /* base of the workspace the handle lives in              */
     size_t workspace_bytes;
     /* Optional per-kernel timing, the analogue of FlashInfer's enable_timing stage events
@@ -189,7 +217,10 @@ int moe_expert_out_size(const moe_geom *g, size_t *bytes);
  * Computes (deterministically; atomics decide no position): per-expert counts and
  * offsets, the position of every pick in its expert's rows in ascending (token, pick)
  * order, the EM slots and layout ranges or the RM/FLAT per-destination rows, local
- * ids and weights, then copies each token row to every place it is received.
+ * ids and weights, then copies each token row to every place it is received.  With
+ * g->quant = MOE_QUANT_FP8_E4M3 each token row is quantised once (e4m3 codes plus one
+ * scale per 128 columns, moe_quant rule) as it is copied: recv_x holds the codes and
+ * recv_scales the scales.
  */
 int moe_dispatch(const moe_geom *g, const void *x_dev, const void *topk_ids_dev,
                  int ids_dtype, const float *topk_weights_dev, const int32_t *active_ranks_dev,
@@ -234,11 +265,50 @@ int moe_combine(const moe_handle *h, const float *expert_out_dev,
                 const float *topk_weights_dev, void *out_dev, void *stream);
 
 /*
+ * moe_quantize_weights_fp8 - one-time FP8 quantisation of bf16 expert weights for
+ * moe_expert_ffn_fp8 (geometry with quant = MOE_QUANT_FP8_E4M3).  Every 128 x 128 block of
+ * w1[e] [2I, H] and w2[e] [H, I] is quantised with the rule of moe_quant (amax over the
+ * block).  W1 is written in the gate/up interleaved order of moe_prepare_weights (blocks of
+ * 128 gate rows and the matching 128 up rows alternate), its block scales likewise:
+ *   w1_dev            bf16 [E, 2I, H]          w2_dev            bf16 [E, H, I]
+ *   w1q_prepared_dev  e4m3 [E, 2I, H]          w1_scales_prepared_dev float [E, 2I/128, H/128]
+ *   w2q_dev           e4m3 [E, H, I]           w2_scales_dev     float [E, H/128, I/128]
+ * All 16-byte aligned (scales 4-byte), distinct buffers.
+ */
+int moe_quantize_weights_fp8(const moe_geom *g, const void *w1_dev, const void *w2_dev,
+                             void *w1q_prepared_dev, float *w1_scales_prepared_dev, void *w2q_dev,
+                             float *w2_scales_dev, void *stream);
+
+/*
+ * moe_prepare_weights_fp8 - the gate/up interleave of moe_prepare_weights for W1 that is
+ * already FP8 (e4m3 codes [E, 2I, H] with float block scales [E, 2I/128, H/128], rows
+ * [0, I) gate and [I, 2I) up per expert): writes the interleaved codes and scales that
+ * moe_expert_ffn_fp8 reads.  W2 needs no preparation.  Distinct, 16-byte aligned buffers.
+ */
+int moe_prepare_weights_fp8(const moe_geom *g, const void *w1q_dev, const float *w1_scales_dev,
+                            void *w1q_prepared_dev, float *w1_scales_prepared_dev, void *stream);
+
+/*
+ * moe_expert_ffn_fp8 - moe_expert_ffn for a handle of an FP8 dispatch: per expert e,
+ * h = x^ W1^[e]^T with e4m3 x e4m3 products accumulated in fp32 (tensor memory), every
+ * 128-column k-block's partial sum scaled by its row scale times its weight-block scale
+ * and added in fp32; act = silu(h[:I]) * h[I:] in fp32, quantised per 128 columns
+ * (moe_quant rule) into ffn_act / ffn_act_scales; y = act^ W2^[e]^T the same way, fp32.
+ * expert_out as in moe_expert_ffn.  Weights from moe_quantize_weights_fp8 or
+ * moe_prepare_weights_fp8.  MOE_ERR_INVALID_ARGUMENT for a bf16 handle (and
+ * moe_expert_ffn returns it for an FP8 handle).
+ */
+int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
+                       const float *w1_scales_prepared_dev, const void *w2q_dev,
+                       const float *w2_scales_dev, float *expert_out_dev, void *stream);
+
+/*
  * moe_forward_host - the whole layer end to end from HOST buffers, on one stream:
  * copy x_host / topk_ids_host / topk_weights_host into the caller's device buffers
  * (x_dev, topk_ids_dev, topk_weights_dev, same shapes as in moe_dispatch), then
  * moe_dispatch (all ranks active) -> moe_expert_ffn -> moe_combine into out_dev, then copy out_dev to
- * out_host (bf16 [T, H]).  Asynchronous like the other calls: out_host is valid once the
+ * out_host (bf16 [T, H]).  bf16 geometries only (MOE_ERR_INVALID_ARGUMENT for FP8).
+ * Asynchronous like the other calls: out_host is valid once the
  * stream has been synchronised.  Host buffers should be page-locked for the copies to
  * overlap; pageable memory works but the copies then synchronise.  Returns the first
  * error of the sequence.

@@ -30,7 +30,8 @@ Functions (none of their values is printed by the pages: "parity unpinned" by th
 pinned in tests by torch's float8_e4m3fn conversion, closed forms, round trips, error
 bounds and the bf16 oracle):
   e4m3_values, round_e4m3, quantize_rows, dequantize_rows, quantize_blocks,
-  dequantize_blocks, expert_fp8, act_band, valid_act_codes, flip_allowance.
+  dequantize_blocks, expert_fp8, act_band, valid_act_codes, flip_allowance, pick_results,
+  layer_fp8.
 """
 import numpy as np
 
@@ -192,3 +193,54 @@ def flip_allowance(gpu_codes, gpu_scales, act_codes, act_scales, w2):
     dv = np.abs(dequantize_rows(gpu_codes, gpu_scales) - dequantize_rows(act_codes, act_scales))
     dv = np.where(gpu_codes != act_codes, dv, 0.0)
     return dv @ np.abs(w2).T
+
+
+def _weight_codes(w1, w2, e, cache):
+    """Block-quantised weights of expert e from the bf16 bit arrays (or per-expert
+    callables) w1 [E, 2I, H] / w2 [E, H, I]: (w1q, w1s, w2q, w2s)."""
+    if e not in cache:
+        from . import bf16_bits_to_f64
+        a = w1(e) if callable(w1) else w1[e]
+        b = w2(e) if callable(w2) else w2[e]
+        cache[e] = quantize_blocks(bf16_bits_to_f64(a)) + quantize_blocks(bf16_bits_to_f64(b))
+    return cache[e]
+
+
+def pick_results(geom, rt, x_bits, w1, w2, picks, cache=None):
+    """FP8 expert stage of the given valid picks (t*k + j): each pick's token row, as the
+    FP8 dispatch delivers it, through expert_fp8 of its expert.  Returns
+    ({pick: dict(y, act_codes, act_scales, act_quo, act_band)}, {expert: dequantised W2})."""
+    from . import bf16_bits_to_f64
+    cache = {} if cache is None else cache
+    k = geom["k"]
+    ids = rt["ids"].reshape(-1)
+    by_e = {}
+    for i in picks:
+        by_e.setdefault(int(ids[i]), []).append(int(i))
+    out, w2d = {}, {}
+    for e, lst in sorted(by_e.items()):
+        w1q, w1s, w2q, w2s = _weight_codes(w1, w2, e, cache)
+        r = expert_fp8(bf16_bits_to_f64(x_bits[np.array(lst) // k]), w1q, w1s, w2q, w2s)
+        for n, i in enumerate(lst):
+            out[i] = {key: r[key][n] for key in ("y", "act_codes", "act_scales", "act_quo", "act_band")}
+        w2d[e] = r["w2"]
+    return out, w2d
+
+
+def layer_fp8(geom, x_bits, ids, topk_w, w1, w2, tokens=None, active=None):
+    """The FP8 layer for `tokens` (default all): route -> FP8 dispatch -> FP8 expert FFN ->
+    combine (as in the bf16 oracle, float64 sums, one rounding to bf16).  Returns
+    (route metadata, out [len(tokens), H], pick results of pick_results, W2 per expert)."""
+    from . import combine_em, combine_ranks, ffn_ranks, route
+    T, k = geom["T"], geom["k"]
+    rt = route(geom, ids, topk_w, active)
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens)
+    picks = [t * k + j for t in tokens for j in range(k) if rt["pick_pos"][t, j] >= 0]
+    res, w2d = pick_results(geom, rt, x_bits, w1, w2, picks)
+    y = lambda i: res[i]["y"]  # noqa: E731
+    if geom["layout"] == "EM":
+        return rt, combine_em(geom, rt, topk_w, y, tokens), res, w2d
+    rows = sorted({(d, int(rt["recv_row"][t, d])) for t in tokens for d in range(geom["W"])
+                   if rt["recv_row"][t, d] >= 0})
+    eo = dict(zip(rows, ffn_ranks(geom, rt, topk_w, y, rows)))
+    return rt, combine_ranks(geom, rt, lambda d, r: eo[(d, r)], tokens), res, w2d

@@ -52,7 +52,7 @@ def _geom(**kw):
     (dict(I=100), -4),               # intermediate % 128
     (dict(T=65), -5),                # num_tokens > world * max_tok
     (dict(k=0), -6), (dict(k=33), -6),
-    (dict(W=0), -1), (dict(layout=3), -1), (dict(algo=2), -1),
+    (dict(W=0), -1), (dict(layout=3), -1), (dict(algo=2), -1), (dict(quant=2), -1),
     (dict(W=128, E=128, Tr=1, T=1), -13),
 ])
 def test_geometry_errors(lib, kw, code):
@@ -70,6 +70,9 @@ def test_workspace_size_grows_with_capacity(lib):
     assert a >= 8 * 64 * 256 * 2
     assert moe.moe_expert_out_size(_geom()) == 8 * 64 * 256 * 4
     assert moe.moe_expert_out_size(_geom(layout="RM")) == 2 * 64 * 256 * 4
+    # FP8 rows take one byte per element (plus a float scale per 128 columns)
+    f = moe.moe_workspace_size(_geom(quant="fp8"))
+    assert f < a and f >= 8 * 64 * 256 + 8 * 64 * 2 * 4
 
 
 def test_dispatch_host_errors_before_any_launch(lib):
@@ -89,10 +92,21 @@ def test_dispatch_host_errors_before_any_launch(lib):
     assert h.magic == 0
 
 
+def test_fp8_weight_calls_validate_before_launch(lib):
+    g = _geom(quant="fp8")
+    p = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.moe_quantize_weights_fp8(ctypes.byref(g), p, p, odd, p, p, p, None) == -9
+    assert lib.moe_quantize_weights_fp8(ctypes.byref(g), p, None, p, p, p, p, None) == -1
+    assert lib.moe_prepare_weights_fp8(ctypes.byref(g), p, p, p, p, None) == -1   # in place
+    assert lib.moe_prepare_weights_fp8(ctypes.byref(_geom(E=7, quant="fp8")), p, p, odd, odd, None) == -2
+
+
 def test_calls_reject_an_unfilled_handle(lib):
     h = moe.MoeHandle()
     p = ctypes.c_void_p(1 << 20)
     assert lib.moe_expert_ffn(ctypes.byref(h), p, p, p, None) == -10
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(h), p, p, p, p, p, None) == -10
     assert lib.moe_combine(ctypes.byref(h), p, p, p, None) == -10
     v = ctypes.c_int32()
     assert lib.moe_get_status(ctypes.byref(h), ctypes.byref(v), None) == -10
