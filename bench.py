@@ -34,6 +34,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # tokens of the workload the CPU oracle evaluates per timed sample (bounded CPU work)
 ORACLE_SAMPLE_TOKENS = {"tiny_ll_em": 64, "mixtral_ll_em": 4, "dsv3_ll_rm": 4, "dsv3_ht_flat": 2,
                         "ragged_em": 16}
+ORACLE_SAMPLE_TOKENS.update({k + "_fp8": v for k, v in list(ORACLE_SAMPLE_TOKENS.items())})
 
 
 def parse_args():
@@ -69,14 +70,19 @@ def algorithmic_work(cfg, rt):
     nrecv = rt["n_recv"]
     em = cfg.layout == "EM"
     ids_b = 8 if cfg.ids_dtype == "int64" else 4
+    f8 = cfg.quant == "fp8"
+    eb = 1 if f8 else 2                       # bytes per element of rows, activations, weights
+    rs = (4.0 / 128) if f8 else 0.0           # scale bytes per element (one float per 128)
+    ws = (4.0 / (128 * 128)) if f8 else 0.0   # weight-block scale bytes per weight
     w = {}
     w["routing"] = dict(bytes=2 * T * k * ids_b + T * k * 4 * (3 if em else 2) +
                         (0 if em else T * k * 4 + nrecv * (4 + 8 * k) + T * cfg.W * 4), flops=0)
-    w["dispatch_copy"] = dict(bytes=T * H * 2 + (R if em else nrecv) * H * 2, flops=0)
+    w["dispatch_copy"] = dict(bytes=T * H * 2 + (R if em else nrecv) * H * (eb + rs), flops=0)
     if not em:
-        w["gather_picks"] = dict(bytes=2 * R * H * 2, flops=0)
-    w["gemm1_swiglu"] = dict(bytes=active * 2 * I * H * 2 + R * H * 2 + R * I * 2, flops=4 * R * H * I)
-    w["gemm2"] = dict(bytes=active * H * I * 2 + R * I * 2 + R * H * 4, flops=2 * R * H * I)
+        w["gather_picks"] = dict(bytes=2 * R * H * (eb + rs), flops=0)
+    w["gemm1_swiglu"] = dict(bytes=active * 2 * I * H * (eb + ws) + R * H * (eb + rs) + R * I * (eb + rs),
+                             flops=4 * R * H * I)
+    w["gemm2"] = dict(bytes=active * H * I * (eb + ws) + R * I * (eb + rs) + R * H * 4, flops=2 * R * H * I)
     if not em:
         w["reduce_ranks"] = dict(bytes=R * H * 4 + nrecv * H * 4 + R * 8, flops=0)
     w["combine"] = dict(bytes=(R * H * 4 + T * k * 8 if em else nrecv * H * 4) + T * H * 2, flops=0)
@@ -193,6 +199,14 @@ def oracle_sample_time(cfg, case, n_tokens):
         f1, f2 = w1.__getitem__, w2.__getitem__
     else:
         f1, f2 = case.w1_host, case.w2_host
+    if cfg.quant == "fp8":
+        from oracle import fp8
+        cache = {}
+        for e in experts:   # weights are quantised once, before timing (as on the GPU)
+            fp8.weight_codes(f1, f2, e, cache)
+        t0 = time.perf_counter()
+        fp8.layer_fp8(g, case.x_bits, case.ids_np, case.w_np, f1, f2, tokens=np.arange(n_tokens), cache=cache)
+        return time.perf_counter() - t0
     t0 = time.perf_counter()
     oracle.layer(g, case.x_bits, case.ids_np, case.w_np, f1, f2, tokens=np.arange(n_tokens))
     return time.perf_counter() - t0
@@ -250,7 +264,8 @@ def workload_config(cfg, n):
             "algorithm": {"LL": "LOW_LATENCY", "HT": "HIGH_THROUGHPUT"}[cfg.algo],
             "tokens": cfg.tokens, "world": cfg.W, "max_tok_per_rank": cfg.Tr, "hidden": cfg.H,
             "experts": cfg.E, "top_k": cfg.k, "intermediate": cfg.I, "routing": cfg.routing,
-            "ids_dtype": cfg.ids_dtype, "l2": "flushed (512 MiB write) before every timed step",
+            "ids_dtype": cfg.ids_dtype, "quant": cfg.quant,
+            "l2": "flushed (512 MiB write) before every timed step",
             "parallelism": "replicas x%d" % n if n > 1 else "single GPU"}
 
 
@@ -265,7 +280,8 @@ def run_ours(args, cfg, rank, world, dist):
         moe.build()
     dev = torch.device("cuda", torch.cuda.current_device())
     case = make_case(cfg, dev)
-    layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout, cfg.algo)
+    layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout, cfg.algo,
+                             quant=cfg.quant)
     layer.set_weights(case.w1, case.w2)
     layer.enable_timing(True)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -313,7 +329,9 @@ def run_ours(args, cfg, rank, world, dist):
     work = algorithmic_work(cfg, rt)
     peaks, peak_src = load_peaks()
     bw = peaks["hbm_gbs"] * 1e9
-    tc = peaks["bf16_tflops"] * 1e12
+    # FP8 contractions: the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+    tc_ratio = 2.0 if cfg.quant == "fp8" else 1.0
+    tc = peaks["bf16_tflops"] * tc_ratio * 1e12
     kernels = [k for k in work if k in kmean]
     dom = max(kernels, key=lambda k: kmean[k])
     wd = work[dom]
@@ -322,14 +340,16 @@ def run_ours(args, cfg, rank, world, dist):
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": wd["bytes"] / t_dom / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
-        roof = {"bound": "tensor", "achieved": wd["flops"] / t_dom / 1e12, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": wd["flops"] / t_dom / 1e12,
+                "peak": peaks["bf16_tflops"] * tc_ratio, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = ncu_traffic(cfg.name, dom)
     roof["kernel"] = dom
     roof["algorithmic_bytes"] = wd["bytes"]
     roof["algorithmic_flops"] = wd["flops"]
     roof["peak_source"] = "%s (MEASURED_PEAKS.json)" % peak_src if peak_src == "measured" else "fallback"
+    if bound == "tensor" and tc_ratio != 1.0:
+        roof["peak_source"] += ", fp8 = measured bf16 x 2 (nominal 4.5 / 2.25 PFLOP/s)"
     sum_b = sum(v["bytes"] for v in work.values())
     sum_f = sum(v["flops"] for v in work.values())
     t_roof = max(sum_b / bw, sum_f / tc)
@@ -337,17 +357,27 @@ def run_ours(args, cfg, rank, world, dist):
     layer_roof = {"t_roofline_us": t_roof * 1e6, "t_step_us": step_s * 1e6, "frac": t_roof / step_s,
                   "bytes": sum_b, "flops": sum_f}
 
-    # end to end from host buffers through moe_forward_host (copies inside the events)
+    # end to end from host buffers through moe_forward_host (copies inside the events); the
+    # FP8 layer has no one-call host entry point: the same copies (cudaMemcpyAsync from
+    # pinned memory) around its dispatch / FFN / combine calls
     e2e = None
     if not args.no_e2e:
         pin = lambda t: t.cpu().pin_memory()  # noqa: E731
         x_h, ids_h, w_h = pin(case.x), pin(case.ids), pin(case.w)
         out_h = torch.empty((cfg.tokens, cfg.H), dtype=torch.bfloat16).pin_memory()
         x_d, ids_d, w_d = torch.empty_like(case.x), torch.empty_like(case.ids), torch.empty_like(case.w)
-        h = moe.MoeHandle()
-        call = lambda: moe.moe_forward_host(layer.geom, x_h, ids_h, w_h, out_h, x_d, ids_d, w_d,  # noqa: E731
-                                            layer.out, layer.w1p, layer.w2, layer.expert_out,
-                                            layer.workspace, h)
+        h = moe.MoeHandle() if cfg.quant == "bf16" else layer.handle
+
+        def call():
+            if cfg.quant == "bf16":
+                moe.moe_forward_host(layer.geom, x_h, ids_h, w_h, out_h, x_d, ids_d, w_d, layer.out, layer.w1p,
+                                     layer.w2, layer.expert_out, layer.workspace, h)
+                return
+            x_d.copy_(x_h, non_blocking=True)
+            ids_d.copy_(ids_h, non_blocking=True)
+            w_d.copy_(w_h, non_blocking=True)
+            layer.forward(x_d, ids_d, w_d)
+            out_h.copy_(layer.out, non_blocking=True)
         for _ in range(max(args.warmup, 3)):
             flush.zero_()
             call()
@@ -413,7 +443,9 @@ def run_ours(args, cfg, rank, world, dist):
     per_step = moe.moe_launches_per_layer(layer.geom)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "ours",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3 (fp32 accumulate)" if cfg.quant == "fp8" else "bf16",
+            "data": "synthetic", "impl": "ours",
             "config": workload_config(cfg, world),
             "stages_us": {k: round(v * 1e3, 2) for k, v in kmean.items()},
             "roofline": roof, "layer_roofline": layer_roof, "cpu_baseline": cpu, "e2e": e2e,

@@ -47,6 +47,14 @@ constexpr int F_THREADS = 384;
 constexpr int F_EPI_WARPS = 8;
 constexpr int F_TMEM_COLS = 512;                // two 128 x 256 fp32 partial-sum buffers
 constexpr int F_RED_BUFS = 4;                   // amax exchange buffers (tiles in flight)
+// Register split (setmaxnreg): the control warpgroup (warps 0-3) gives registers to the two
+// promotion warpgroups, which hold a 128-float accumulator plus a 64-column load per thread.
+// The shares must add up to the launch's total, F_THREADS x F_LAUNCH_REGS (checked on the
+// host against the compiled register count before the first launch).
+constexpr int F_LAUNCH_REGS = 168;
+constexpr int F_REGS_CTRL = 40;
+constexpr int F_REGS_EPI = 232;
+static_assert(128 * F_REGS_CTRL + 256 * F_REGS_EPI <= F_THREADS * F_LAUNCH_REGS, "register split");
 // ring | barriers (256 B) | amax exchange [4][2][128] floats
 constexpr int F_SMEM = F_STAGES * F_STAGE + 1024 /*align*/ + 256 + F_RED_BUFS * 2 * 128 * 4;
 
@@ -120,14 +128,19 @@ __device__ __forceinline__ uint32_t e4m3x4_dev(float v0, float v1, float v2, flo
     return lo | (hi << 16);
 }
 
-// acc[base + i] += c * partial[col + i], i < 16, for this warp's 32 TMEM lanes
+// acc[base/2 + i] += c * partial[col + 2i, col + 2i + 1], i < 32, for this warp's 32 TMEM
+// lanes: one tensor-memory load round trip per 64 columns, packed fp32x2 FMAs (half the
+// issue slots of scalar FMAs, which otherwise bound the promotion)
 template <int BASE>
-__device__ __forceinline__ void promote16(float (&acc)[128], uint32_t taddr, float c) {
-    uint32_t v[16];
-    tmem_ld16(taddr, v);
+__device__ __forceinline__ void promote64(float2 (&acc)[64], uint32_t taddr, float c) {
+    uint32_t v[64];
+    tmem_ld64(taddr, v);
     tmem_wait_ld();
+    const float2 cc = make_float2(c, c);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[BASE + i] = fmaf(__uint_as_float(v[i]), c, acc[BASE + i]);
+    for (int i = 0; i < 32; ++i)
+        acc[BASE / 2 + i] = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                       cc, acc[BASE / 2 + i]);
 }
 
 template <int MODE>
@@ -177,54 +190,57 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = __ldg(a.mprefix + a.E) * a.nb;
-
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------------------- TMA producer
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        const uint32_t tx = (uint32_t)(F_A_BYTES + a.bn * F_BK);
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-            int e, mb, nbk;
-            decode_tile_f8(a, tile, e, mb, nbk);
-            const int64_t arow = (a.a_mode == 0 ? (int64_t)e * a.a_cap : (int64_t)__ldg(a.offsets + e)) +
-                                 (int64_t)mb * F_BM;
-            const int64_t brow = (int64_t)e * a.b_rows + (int64_t)nbk * a.bn;
-            for (int kb = 0; kb < a.kb; ++kb) {
-                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, a.status)) { ok = false; break; }
-                const uint32_t fb = full0 + 8 * stage;
-                mbar_expect_tx(fb, tx);
-                tma_load_2d(smem_u32(sA + stage * F_A_BYTES), &tmA, kb * F_BK, (int)arow, fb);
-                tma_load_2d(smem_u32(sB + stage * F_B_BYTES), &tmB, kb * F_BK, (int)brow, fb);
-                if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(F_REGS_CTRL));
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            const uint32_t tx = (uint32_t)(F_A_BYTES + a.bn * F_BK);
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                int e, mb, nbk;
+                decode_tile_f8(a, tile, e, mb, nbk);
+                const int64_t arow = (a.a_mode == 0 ? (int64_t)e * a.a_cap : (int64_t)__ldg(a.offsets + e)) +
+                                     (int64_t)mb * F_BM;
+                const int64_t brow = (int64_t)e * a.b_rows + (int64_t)nbk * a.bn;
+                for (int kb = 0; kb < a.kb; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_expect_tx(fb, tx);
+                    tma_load_2d(smem_u32(sA + stage * F_A_BYTES), &tmA, kb * F_BK, (int)arow, fb);
+                    tma_load_2d(smem_u32(sB + stage * F_B_BYTES), &tmB, kb * F_BK, (int)brow, fb);
+                    if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+                }
             }
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------------------------------------------------------- MMA issuer
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t it = 0;   // k-blocks issued so far (partial-sum buffer it & 1)
-        bool ok = true;
-        const uint32_t idesc = make_idesc_f8(F_BM, a.bn);
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-            for (int kb = 0; kb < a.kb; ++kb, ++it) {
-                const uint32_t pb = it & 1, pph = (it >> 1) & 1;
-                if (!mbar_wait(pempty0 + 8 * pb, pph ^ 1, abort_flag, a.status)) { ok = false; break; }
-                tc_fence_after();
-                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, a.status)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + pb * (uint32_t)F_BN;
-                const uint32_t a0 = smem_u32(sA + stage * F_A_BYTES);
-                const uint32_t b0 = smem_u32(sB + stage * F_B_BYTES);
+        } else if (warp == 1 && lane == 0) {
+            // ---------------------------------------------------------------- MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t it = 0;   // k-blocks issued so far (partial-sum buffer it & 1)
+            bool ok = true;
+            const uint32_t idesc = make_idesc_f8(F_BM, a.bn);
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < a.kb; ++kb, ++it) {
+                    const uint32_t pb = it & 1, pph = (it >> 1) & 1;
+                    if (!mbar_wait(pempty0 + 8 * pb, pph ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + pb * (uint32_t)F_BN;
+                    const uint32_t a0 = smem_u32(sA + stage * F_A_BYTES);
+                    const uint32_t b0 = smem_u32(sB + stage * F_B_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < F_BK / 32; ++kk)
-                    mma_f8(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, kk != 0 ? 1u : 0u);
-                mma_commit(empty0 + 8 * stage);   // the stage is reusable once these finish
-                mma_commit(pfull0 + 8 * pb);      // the partial sum is ready
-                if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+                    for (int kk = 0; kk < F_BK / 32; ++kk)
+                        mma_f8(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc, kk != 0 ? 1u : 0u);
+                    mma_commit(empty0 + 8 * stage);   // the stage is reusable once these finish
+                    mma_commit(pfull0 + 8 * pb);      // the partial sum is ready
+                    if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
+                }
             }
         }
-    } else if (warp >= 4) {
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(F_REGS_EPI));
         // -------------------------------------------------------- promotion + epilogue
         const int quad = warp & 3;                  // TMEM lanes 32*quad .. 32*quad+31
         const int half = (warp - 4) >> 2;           // which columns of the tile
@@ -246,46 +262,38 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             const int blk0 = MODE == 0 ? 2 * nbk : (a.bn == 256 ? 2 * nbk + half : nbk);
             const float *sb0p = a.b_scale + ((int64_t)e * bblocks + blk0) * a.kb;
             const float *sb1p = sb0p + a.kb;   // GEMM1: the up block (2 * nbk + 1)
-            float acc[128];
+            float2 acc[64];   // columns 2i, 2i + 1
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-            float sa_n = live ? __ldg(a.a_scale + arow) : 0.f;
-            float sb0_n = __ldg(sb0p), sb1_n = MODE == 0 ? __ldg(sb1p) : 0.f;
+            for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.f, 0.f);
+            // Scales of the next four k-blocks, shifted along a register queue (a k-block's
+            // row scales are 4 * a_scale_ld bytes apart: after the L2 flush each one is a DRAM
+            // round trip, longer than one k-block of promotion)
+            auto ld_sa = [&](int kb) {
+                return kb < a.kb && live ? __ldg(a.a_scale + (int64_t)kb * a.a_scale_ld + arow) : 0.f;
+            };
+            auto ld_sb = [&](const float *p, int kb) { return kb < a.kb ? __ldg(p + kb) : 0.f; };
+            float sa0 = ld_sa(0), sa1 = ld_sa(1), sa2 = ld_sa(2), sa3 = ld_sa(3);
+            float sg0 = ld_sb(sb0p, 0), sg1 = ld_sb(sb0p, 1), sg2 = ld_sb(sb0p, 2), sg3 = ld_sb(sb0p, 3);
+            float su0 = 0.f, su1 = 0.f, su2 = 0.f, su3 = 0.f;
+            if (MODE == 0) {
+                su0 = ld_sb(sb1p, 0); su1 = ld_sb(sb1p, 1); su2 = ld_sb(sb1p, 2); su3 = ld_sb(sb1p, 3);
+            }
             for (int kb = 0; kb < a.kb; ++kb, ++it) {
-                const float sa = sa_n, sb0 = sb0_n, sb1 = sb1_n;
-                if (kb + 1 < a.kb) {   // next k-block's scales, loaded while this one waits
-                    sa_n = live ? __ldg(a.a_scale + (int64_t)(kb + 1) * a.a_scale_ld + arow) : 0.f;
-                    sb0_n = __ldg(sb0p + kb + 1);
-                    if (MODE == 0) sb1_n = __ldg(sb1p + kb + 1);
-                }
+                const float c0 = sa0 * sg0, c1 = sa0 * su0;
+                sa0 = sa1; sa1 = sa2; sa2 = sa3; sa3 = ld_sa(kb + 4);
+                sg0 = sg1; sg1 = sg2; sg2 = sg3; sg3 = ld_sb(sb0p, kb + 4);
+                if (MODE == 0) { su0 = su1; su1 = su2; su2 = su3; su3 = ld_sb(sb1p, kb + 4); }
                 const uint32_t pb = it & 1, pph = (it >> 1) & 1;
                 if (!mbar_wait(pfull0 + 8 * pb, pph, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t tb = tmem_base + pb * (uint32_t)F_BN + ((uint32_t)(quad * 32) << 16);
-                const float c0 = sa * sb0;
                 if (MODE == 0) {
-                    const float c1 = sa * sb1;
-                    const uint32_t g0 = tb + 64 * half, u0 = tb + 128 + 64 * half;
-                    promote16<0>(acc, g0 + 0, c0);
-                    promote16<16>(acc, g0 + 16, c0);
-                    promote16<32>(acc, g0 + 32, c0);
-                    promote16<48>(acc, g0 + 48, c0);
-                    promote16<64>(acc, u0 + 0, c1);
-                    promote16<80>(acc, u0 + 16, c1);
-                    promote16<96>(acc, u0 + 32, c1);
-                    promote16<112>(acc, u0 + 48, c1);
+                    promote64<0>(acc, tb + 64 * half, c0);         // gate columns
+                    promote64<64>(acc, tb + 128 + 64 * half, c1);  // up columns
                 } else {
                     const uint32_t t0 = tb + (uint32_t)(ncol * half);
-                    promote16<0>(acc, t0 + 0, c0);
-                    promote16<16>(acc, t0 + 16, c0);
-                    promote16<32>(acc, t0 + 32, c0);
-                    promote16<48>(acc, t0 + 48, c0);
-                    if (ncol == 128) {
-                        promote16<64>(acc, t0 + 64, c0);
-                        promote16<80>(acc, t0 + 80, c0);
-                        promote16<96>(acc, t0 + 96, c0);
-                        promote16<112>(acc, t0 + 112, c0);
-                    }
+                    promote64<0>(acc, t0, c0);
+                    if (ncol == 128) promote64<64>(acc, t0 + 64, c0);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -295,11 +303,13 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             const int64_t orow = (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) +
                                  (int64_t)m0 + row;
             if (MODE == 0) {
+                // act = silu(gate) * up; gate columns in acc[0, 32), up in acc[32, 64)
                 float amax = 0.f;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    acc[i] = silu_mul(acc[i], acc[64 + i]);
-                    amax = fmaxf(amax, fabsf(acc[i]));
+                for (int i = 0; i < 32; ++i) {
+                    acc[i] = make_float2(silu_mul_fast(acc[i].x, acc[32 + i].x),
+                                         silu_mul_fast(acc[i].y, acc[32 + i].y));
+                    amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
                 }
                 // the row's other 64 activation columns live in the other warp of this
                 // lane quarter: exchange the partial amax through shared memory
@@ -316,23 +326,25 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(a.out) +
                                                          orow * a.out_ld + (int64_t)nbk * 128 + half * 64);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        o[v] = make_uint4(
-                            e4m3x4_dev(acc[16 * v + 0], acc[16 * v + 1], acc[16 * v + 2], acc[16 * v + 3], inv),
-                            e4m3x4_dev(acc[16 * v + 4], acc[16 * v + 5], acc[16 * v + 6], acc[16 * v + 7], inv),
-                            e4m3x4_dev(acc[16 * v + 8], acc[16 * v + 9], acc[16 * v + 10], acc[16 * v + 11], inv),
-                            e4m3x4_dev(acc[16 * v + 12], acc[16 * v + 13], acc[16 * v + 14], acc[16 * v + 15], inv));
+                    for (int v = 0; v < 4; ++v) {
+                        const float2 *q = acc + 8 * v;
+                        o[v] = make_uint4(e4m3x4_dev(q[0].x, q[0].y, q[1].x, q[1].y, inv),
+                                          e4m3x4_dev(q[2].x, q[2].y, q[3].x, q[3].y, inv),
+                                          e4m3x4_dev(q[4].x, q[4].y, q[5].x, q[5].y, inv),
+                                          e4m3x4_dev(q[6].x, q[6].y, q[7].x, q[7].y, inv));
+                    }
                     if (half == 0) a.out_scale[(int64_t)nbk * a.out_scale_ld + orow] = scale;
                 }
             } else if (live) {
                 float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + orow * a.out_ld +
                                                        (int64_t)nbk * a.bn + half * ncol);
 #pragma unroll
-                for (int q = 0; q < 16; ++q) o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                for (int q = 0; q < 16; ++q)
+                    o[q] = make_float4(acc[2 * q].x, acc[2 * q].y, acc[2 * q + 1].x, acc[2 * q + 1].y);
                 if (ncol == 128) {
 #pragma unroll
                     for (int q = 16; q < 32; ++q)
-                        o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                        o[q] = make_float4(acc[2 * q].x, acc[2 * q].y, acc[2 * q + 1].x, acc[2 * q + 1].y);
                 }
             }
         }
@@ -361,6 +373,12 @@ int launch_gemm_fp8(const CUtensorMap &ma, const CUtensorMap &mb, const F8Args &
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
+        // setmaxnreg.inc waits until the registers it asks for are free in the CTA's launch
+        // allocation: never launch a build whose register count makes the split too large
+        cudaFuncAttributes fa{};
+        if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, kernel);
+        if (attr_err == cudaSuccess && fa.numRegs * F_THREADS < 128 * F_REGS_CTRL + 256 * F_REGS_EPI)
+            attr_err = cudaErrorInvalidConfiguration;
     });
     if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
     int grid = num_sms();

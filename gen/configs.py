@@ -109,4 +109,6 @@ PROFILE = {
                                 layout="FLAT", algo="HT", routing="uniform"),
 }
 
+PROFILE.update({name + "_fp8": cfg.with_(name=name + "_fp8", quant="fp8") for name, cfg in list(PROFILE.items())})
+
 ALL.update(PROFILE)

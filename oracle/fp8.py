@@ -195,7 +195,7 @@ def flip_allowance(gpu_codes, gpu_scales, act_codes, act_scales, w2):
     return dv @ np.abs(w2).T
 
 
-def _weight_codes(w1, w2, e, cache):
+def weight_codes(w1, w2, e, cache):
     """Block-quantised weights of expert e from the bf16 bit arrays (or per-expert
     callables) w1 [E, 2I, H] / w2 [E, H, I]: (w1q, w1s, w2q, w2s)."""
     if e not in cache:
@@ -219,7 +219,7 @@ def pick_results(geom, rt, x_bits, w1, w2, picks, cache=None):
         by_e.setdefault(int(ids[i]), []).append(int(i))
     out, w2d = {}, {}
     for e, lst in sorted(by_e.items()):
-        w1q, w1s, w2q, w2s = _weight_codes(w1, w2, e, cache)
+        w1q, w1s, w2q, w2s = weight_codes(w1, w2, e, cache)
         r = expert_fp8(bf16_bits_to_f64(x_bits[np.array(lst) // k]), w1q, w1s, w2q, w2s)
         for n, i in enumerate(lst):
             out[i] = {key: r[key][n] for key in ("y", "act_codes", "act_scales", "act_quo", "act_band")}
@@ -227,16 +227,17 @@ def pick_results(geom, rt, x_bits, w1, w2, picks, cache=None):
     return out, w2d
 
 
-def layer_fp8(geom, x_bits, ids, topk_w, w1, w2, tokens=None, active=None):
+def layer_fp8(geom, x_bits, ids, topk_w, w1, w2, tokens=None, active=None, cache=None):
     """The FP8 layer for `tokens` (default all): route -> FP8 dispatch -> FP8 expert FFN ->
     combine (as in the bf16 oracle, float64 sums, one rounding to bf16).  Returns
-    (route metadata, out [len(tokens), H], pick results of pick_results, W2 per expert)."""
+    (route metadata, out [len(tokens), H], pick results of pick_results, W2 per expert).
+    cache: optional dict of already quantised expert weights (see weight_codes)."""
     from . import combine_em, combine_ranks, ffn_ranks, route
     T, k = geom["T"], geom["k"]
     rt = route(geom, ids, topk_w, active)
     tokens = np.arange(T) if tokens is None else np.asarray(tokens)
     picks = [t * k + j for t in tokens for j in range(k) if rt["pick_pos"][t, j] >= 0]
-    res, w2d = pick_results(geom, rt, x_bits, w1, w2, picks)
+    res, w2d = pick_results(geom, rt, x_bits, w1, w2, picks, cache)
     y = lambda i: res[i]["y"]  # noqa: E731
     if geom["layout"] == "EM":
         return rt, combine_em(geom, rt, topk_w, y, tokens), res, w2d
