@@ -42,21 +42,27 @@ constexpr int F_BK = 128;                       // k elements (bytes) per stage
 constexpr int F_A_BYTES = F_BM * F_BK;          // 16 KB
 constexpr int F_B_BYTES = F_BN * F_BK;          // 32 KB
 constexpr int F_STAGE = F_A_BYTES + F_B_BYTES;  // 48 KB
-constexpr int F_STAGES = 4;
 constexpr int F_THREADS = 384;
 constexpr int F_EPI_WARPS = 8;
 constexpr int F_TMEM_COLS = 512;                // two 128 x 256 fp32 partial-sum buffers
-constexpr int F_RED_BUFS = 4;                   // amax exchange buffers (tiles in flight)
 // Register split (setmaxnreg): the control warpgroup (warps 0-3) gives registers to the two
 // promotion warpgroups, which hold a 128-float accumulator plus a 64-column load per thread.
 // The shares must add up to the launch's total, F_THREADS x F_LAUNCH_REGS (checked on the
 // host against the compiled register count before the first launch).
 constexpr int F_LAUNCH_REGS = 168;
-constexpr int F_REGS_CTRL = 40;
-constexpr int F_REGS_EPI = 232;
+constexpr int F_REGS_CTRL = 56;
+constexpr int F_REGS_EPI = 224;
 static_assert(128 * F_REGS_CTRL + 256 * F_REGS_EPI <= F_THREADS * F_LAUNCH_REGS, "register split");
-// ring | barriers (256 B) | amax exchange [4][2][128] floats
-constexpr int F_SMEM = F_STAGES * F_STAGE + 1024 /*align*/ + 256 + F_RED_BUFS * 2 * 128 * 4;
+
+// Shared memory: the TMA ring, 256 B of barriers, and for GEMM1 a 128 x 128 fp32 staging
+// buffer of the tile's activation plus the two half-row maxima of each row (handed from the
+// promotion warps to the quantising warps 2-3, so that the next tile's promotion does not
+// wait for the quantisation).
+template <int MODE> struct F8Smem {
+    static constexpr int kStages = MODE == 0 ? 3 : 4;
+    static constexpr int kActBytes = MODE == 0 ? F_BM * 128 * 4 : 0;
+    static constexpr int kBytes = kStages * F_STAGE + 1024 /*align*/ + 256 + kActBytes + (MODE == 0 ? 1024 : 0);
+};
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B
 // e4m3 (format 0 in bits 7-9 and 10-12), both K-major (bits 15/16 = 0), N >> 3 at bits
@@ -147,21 +153,25 @@ template <int MODE>
 __global__ void __launch_bounds__(F_THREADS, 1)
     ffn_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         F8Args a) {
+    constexpr int F_STAGES = F8Smem<MODE>::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;                          // [STAGES] A tiles
     uint8_t *sB = smem + F_STAGES * F_A_BYTES;   // [STAGES] B tiles
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + F_STAGES * F_STAGE);
-    // bars: full[STAGES], empty[STAGES], pfull[2], pempty[2], xfull[F_RED_BUFS]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * F_STAGES + 4 + F_RED_BUFS);
+    // bars: full[STAGES], empty[STAGES], pfull[2], pempty[2], afull, aempty
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * F_STAGES + 6);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *red = reinterpret_cast<float *>(smem + F_STAGES * F_STAGE + 256);   // [4][2][128]
+    // GEMM1: activation staging [128 rows][32 chunks of 4 floats], chunk q of row r stored
+    // at slot q ^ (r % 32) (conflict-free row writes by lane = row and row reads by lane = q)
+    float4 *act_s = reinterpret_cast<float4 *>(smem + F_STAGES * F_STAGE + 256);
+    float *amax_s = reinterpret_cast<float *>(smem + F_STAGES * F_STAGE + 256 + F8Smem<MODE>::kActBytes);  // [2][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + F_STAGES);
     const uint32_t pfull0 = smem_u32(bars + 2 * F_STAGES), pempty0 = smem_u32(bars + 2 * F_STAGES + 2);
-    const uint32_t xfull0 = smem_u32(bars + 2 * F_STAGES + 4);
+    const uint32_t afull = smem_u32(bars + 2 * F_STAGES + 4), aempty = smem_u32(bars + 2 * F_STAGES + 5);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < F_STAGES; ++s) {
@@ -172,7 +182,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             mbar_init(pfull0 + 8 * s, 1);
             mbar_init(pempty0 + 8 * s, F_EPI_WARPS);   // one arrival per promotion warp
         }
-        for (int s = 0; s < F_RED_BUFS; ++s) mbar_init(xfull0 + 8 * s, F_EPI_WARPS);
+        mbar_init(afull, F_EPI_WARPS);   // activation staged (promotion warps)
+        mbar_init(aempty, 2);            // activation consumed (quantising warps 2, 3)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -237,6 +248,40 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     mma_commit(pfull0 + 8 * pb);      // the partial sum is ready
                     if (++stage == F_STAGES) { stage = 0; phase ^= 1; }
                 }
+            }
+        } else if (MODE == 0 && (warp == 2 || warp == 3)) {
+            // ------------------------------------------- activation quantisation (GEMM1)
+            // Thread t (0..63) owns rows t and t + 64: the row's amax is the larger of the
+            // two half-row maxima the promotion warps staged, the scale is computed once per
+            // row, and the 128 codes go out as eight 16-byte stores.
+            const int qt = threadIdx.x - 64;
+            int ntile = 0;
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++ntile) {
+                int e, mb, nbk;
+                decode_tile_f8(a, tile, e, mb, nbk);
+                const int m0 = mb * F_BM;
+                const int valid = min(F_BM, __ldg(a.counts + e) - m0);
+                const int64_t obase = (int64_t)__ldg(a.offsets + e) + m0;   // act rows: pick list
+                if (!mbar_wait(afull, (uint32_t)ntile & 1, abort_flag, a.status)) break;
+                for (int r = qt; r < valid; r += 64) {
+                    float scale, inv;
+                    fp8_scale_dev(fmaxf(amax_s[r], amax_s[F_BM + r]), scale, inv);
+                    uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(a.out) + (obase + r) * a.out_ld +
+                                                         (int64_t)nbk * 128);
+#pragma unroll 2
+                    for (int c = 0; c < 8; ++c) {   // 16 columns: chunks 4c .. 4c + 3
+                        uint32_t w[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 v = act_s[r * 32 + ((4 * c + j) ^ (r & 31))];
+                            w[j] = e4m3x4_dev(v.x, v.y, v.z, v.w, inv);
+                        }
+                        o[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    a.out_scale[(int64_t)nbk * a.out_scale_ld + obase + r] = scale;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(aempty);
             }
         }
     } else {
@@ -303,38 +348,22 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             const int64_t orow = (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) +
                                  (int64_t)m0 + row;
             if (MODE == 0) {
-                // act = silu(gate) * up; gate columns in acc[0, 32), up in acc[32, 64)
+                // act = silu(gate) * up (gate columns in acc[0, 32), up in acc[32, 64)),
+                // staged for the quantising warps once they are done with the previous tile
+                if (!mbar_wait(aempty, ((uint32_t)ntile & 1) ^ 1, abort_flag, a.status)) break;
                 float amax = 0.f;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    acc[i] = make_float2(silu_mul_fast(acc[i].x, acc[32 + i].x),
-                                         silu_mul_fast(acc[i].y, acc[32 + i].y));
-                    amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
+                for (int j = 0; j < 16; ++j) {
+                    const float2 g0 = acc[2 * j], g1 = acc[2 * j + 1];
+                    const float2 u0 = acc[32 + 2 * j], u1 = acc[32 + 2 * j + 1];
+                    const float4 v = make_float4(silu_mul_fast(g0.x, u0.x), silu_mul_fast(g0.y, u0.y),
+                                                 silu_mul_fast(g1.x, u1.x), silu_mul_fast(g1.y, u1.y));
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+                    act_s[row * 32 + ((16 * half + j) ^ (row & 31))] = v;
                 }
-                // the row's other 64 activation columns live in the other warp of this
-                // lane quarter: exchange the partial amax through shared memory
-                const int rb = ntile % F_RED_BUFS;
-                float *rbuf = red + rb * 256;
-                rbuf[half * 128 + row] = amax;
+                amax_s[half * F_BM + row] = amax;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(xfull0 + 8 * rb);
-                if (!mbar_wait(xfull0 + 8 * rb, (uint32_t)(ntile / F_RED_BUFS) & 1, abort_flag, a.status)) break;
-                amax = fmaxf(rbuf[row], rbuf[128 + row]);
-                float scale, inv;
-                fp8_scale_dev(amax, scale, inv);
-                if (live) {
-                    uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(a.out) +
-                                                         orow * a.out_ld + (int64_t)nbk * 128 + half * 64);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const float2 *q = acc + 8 * v;
-                        o[v] = make_uint4(e4m3x4_dev(q[0].x, q[0].y, q[1].x, q[1].y, inv),
-                                          e4m3x4_dev(q[2].x, q[2].y, q[3].x, q[3].y, inv),
-                                          e4m3x4_dev(q[4].x, q[4].y, q[5].x, q[5].y, inv),
-                                          e4m3x4_dev(q[6].x, q[6].y, q[7].x, q[7].y, inv));
-                    }
-                    if (half == 0) a.out_scale[(int64_t)nbk * a.out_scale_ld + orow] = scale;
-                }
+                if (lane == 0) mbar_arrive(afull);
             } else if (live) {
                 float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + orow * a.out_ld +
                                                        (int64_t)nbk * a.bn + half * ncol);
@@ -369,10 +398,11 @@ int launch_gemm_fp8(const CUtensorMap &ma, const CUtensorMap &mb, const F8Args &
                     cudaStream_t s) {
     if (max_tiles <= 0) return MOE_OK;
     auto kernel = ffn_gemm_fp8_kernel<MODE>;
+    constexpr int smem = F8Smem<MODE>::kBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
+        attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         // setmaxnreg.inc waits until the registers it asks for are free in the CTA's launch
         // allocation: never launch a build whose register count makes the split too large
         cudaFuncAttributes fa{};
@@ -383,7 +413,7 @@ int launch_gemm_fp8(const CUtensorMap &ma, const CUtensorMap &mb, const F8Args &
     if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
     int grid = num_sms();
     if ((int64_t)grid > max_tiles) grid = (int)max_tiles;
-    kernel<<<grid, F_THREADS, F_SMEM, s>>>(ma, mb, args);
+    kernel<<<grid, F_THREADS, smem, s>>>(ma, mb, args);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
