@@ -54,13 +54,15 @@ constexpr int F_REGS_CTRL = 56;
 constexpr int F_REGS_EPI = 224;
 static_assert(128 * F_REGS_CTRL + 256 * F_REGS_EPI <= F_THREADS * F_LAUNCH_REGS, "register split");
 
-// Shared memory: the TMA ring, 256 B of barriers, and for GEMM1 a 128 x 128 fp32 staging
-// buffer of the tile's activation plus the two half-row maxima of each row (handed from the
-// promotion warps to the quantising warps 2-3, so that the next tile's promotion does not
-// wait for the quantisation).
+// Shared memory: the TMA ring, 256 B of barriers and a 128 x 128 fp32 staging buffer,
+// through which the promotion warps hand a finished tile to warps 2-3 so that the next
+// tile's promotion does not wait for the epilogue.  GEMM1 stages the tile's activation
+// (plus the two half-row maxima of each row) and warps 2-3 quantise and store it; GEMM2
+// stages the 256-column fp32 tile in two 128-column halves and warps 2-3 store each half
+// as coalesced rows.
 template <int MODE> struct F8Smem {
-    static constexpr int kStages = MODE == 0 ? 3 : 4;
-    static constexpr int kActBytes = MODE == 0 ? F_BM * 128 * 4 : 0;
+    static constexpr int kStages = 3;
+    static constexpr int kActBytes = F_BM * 128 * 4;
     static constexpr int kBytes = kStages * F_STAGE + 1024 /*align*/ + 256 + kActBytes + (MODE == 0 ? 1024 : 0);
 };
 
@@ -160,18 +162,20 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     uint8_t *sA = smem;                          // [STAGES] A tiles
     uint8_t *sB = smem + F_STAGES * F_A_BYTES;   // [STAGES] B tiles
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + F_STAGES * F_STAGE);
-    // bars: full[STAGES], empty[STAGES], pfull[2], pempty[2], afull, aempty
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * F_STAGES + 6);
+    // bars: full[STAGES], empty[STAGES], pfull[2], pempty[2], afull[2], aempty[2] (one pair
+    // per staged half: GEMM1 uses pair 0 for the whole tile)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * F_STAGES + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    // GEMM1: activation staging [128 rows][32 chunks of 4 floats], chunk q of row r stored
-    // at slot q ^ (r % 32) (conflict-free row writes by lane = row and row reads by lane = q)
+    // staging [128 rows][32 chunks of 4 floats], chunk q of row r stored at slot q ^ (r % 32)
+    // (conflict-free row writes by lane = row and row reads by lane = q)
     float4 *act_s = reinterpret_cast<float4 *>(smem + F_STAGES * F_STAGE + 256);
     float *amax_s = reinterpret_cast<float *>(smem + F_STAGES * F_STAGE + 256 + F8Smem<MODE>::kActBytes);  // [2][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + F_STAGES);
     const uint32_t pfull0 = smem_u32(bars + 2 * F_STAGES), pempty0 = smem_u32(bars + 2 * F_STAGES + 2);
-    const uint32_t afull = smem_u32(bars + 2 * F_STAGES + 4), aempty = smem_u32(bars + 2 * F_STAGES + 5);
+    const uint32_t afull0 = smem_u32(bars + 2 * F_STAGES + 4), aempty0 = smem_u32(bars + 2 * F_STAGES + 6);
+    const uint32_t afull = afull0, aempty = aempty0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < F_STAGES; ++s) {
@@ -182,8 +186,11 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             mbar_init(pfull0 + 8 * s, 1);
             mbar_init(pempty0 + 8 * s, F_EPI_WARPS);   // one arrival per promotion warp
         }
-        mbar_init(afull, F_EPI_WARPS);   // activation staged (promotion warps)
-        mbar_init(aempty, 2);            // activation consumed (quantising warps 2, 3)
+        for (int h = 0; h < 2; ++h) {
+            // staged by the promotion warps (GEMM1: all eight; GEMM2: the four of the half)
+            mbar_init(afull0 + 8 * h, MODE == 0 ? F_EPI_WARPS : F_EPI_WARPS / 2);
+            mbar_init(aempty0 + 8 * h, 2);   // consumed by warps 2, 3
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -201,6 +208,11 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = __ldg(a.mprefix + a.E) * a.nb;
+    // GEMM2 stages 256-column tiles of at least three k-blocks: then a promotion warp that
+    // stages a half is never two phases of that half's barrier ahead of the storing warps
+    // (the MMA of its tile's last k-block waited for every warp's promotion of an earlier
+    // k-block of the same tile).  Otherwise the promotion warps store their rows directly.
+    const bool staged = MODE == 0 || (a.bn == 256 && a.kb >= 3);
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(F_REGS_CTRL));
         if (warp == 0 && lane == 0) {
@@ -283,6 +295,30 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(aempty);
             }
+        } else if (MODE == 1 && staged && (warp == 2 || warp == 3)) {
+            // --------------------------------------------------- fp32 tile store (GEMM2)
+            // Per half of the tile: one row per warp at a time (warp 2 even rows, warp 3
+            // odd); lane l holds columns 4l..4l+3 of the half, so a row leaves as one
+            // coalesced 512-byte store.
+            int ntile = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++ntile) {
+                int e, mb, nbk;
+                decode_tile_f8(a, tile, e, mb, nbk);
+                const int m0 = mb * F_BM;
+                const int valid = min(F_BM, __ldg(a.counts + e) - m0);
+                const int64_t obase =
+                    (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) + m0;
+                for (int h = 0; h < 2; ++h) {
+                    if (!mbar_wait(afull0 + 8 * h, (uint32_t)ntile & 1, abort_flag, a.status)) { ok = false; break; }
+                    float *out = reinterpret_cast<float *>(a.out) + (int64_t)nbk * a.bn + 128 * h + 4 * lane;
+#pragma unroll 4
+                    for (int r = warp - 2; r < valid; r += 2)
+                        *reinterpret_cast<float4 *>(out + (obase + r) * a.out_ld) = act_s[r * 32 + (lane ^ (r & 31))];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(aempty0 + 8 * h);
+                }
+            }
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(F_REGS_EPI));
@@ -364,7 +400,20 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 amax_s[half * F_BM + row] = amax;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(afull);
+            } else if (staged) {
+                // fp32 rows, staged half by half: half 0 once the storing warps are done with
+                // half 1 of the previous tile, half 1 once they are done with this tile's half 0
+                const uint32_t wait_bar = half == 0 ? aempty0 + 8 : aempty0;
+                const uint32_t wait_par = half == 0 ? (((uint32_t)ntile & 1) ^ 1) : ((uint32_t)ntile & 1);
+                if (!mbar_wait(wait_bar, wait_par, abort_flag, a.status)) break;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    act_s[row * 32 + (j ^ (row & 31))] =
+                        make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull0 + 8 * half);
             } else if (live) {
+                // direct row stores: ncol = 64 (128-column tiles) or 128 columns per thread
                 float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + orow * a.out_ld +
                                                        (int64_t)nbk * a.bn + half * ncol);
 #pragma unroll

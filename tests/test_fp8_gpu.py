@@ -28,6 +28,10 @@ CASES = {
     "f8_pair_em": gen.SMALL["pair_em"].with_(quant="fp8"),                         # several m-blocks
     "f8_pair_flat_masked": gen.SMALL["pair_flat"].with_(quant="fp8", mask_frac=0.2, seed=9),
     "f8_tiny": gen.CONFIGS["tiny_ll_em"].with_(quant="fp8"),
+    # second GEMM with fewer than three k-blocks per tile (direct row stores) and with
+    # 128-column tiles; many routing blocks
+    "f8_blocks_flat": gen.SMALL["blocks_flat"].with_(quant="fp8"),
+    "f8_pair_rm": gen.SMALL["pair_rm"].with_(quant="fp8"),
 }
 
 
