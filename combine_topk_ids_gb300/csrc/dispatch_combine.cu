@@ -36,6 +36,40 @@ __device__ __forceinline__ float4 ld_nc_f4(const float *p) {
     return v;
 }
 
+__device__ __forceinline__ uint2 ld_nc_v2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Four consecutive elements (index elem, a multiple of 4) of a float32 or bf16 row as fp32,
+// and the store back (bf16: round to nearest even).
+template <bool BF16>
+__device__ __forceinline__ float4 ld_row4(const void *base, int64_t elem) {
+    if (BF16) {
+        const uint2 v = ld_nc_v2(reinterpret_cast<const uint16_t *>(base) + elem);
+        return make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+    }
+    return ld_nc_f4(reinterpret_cast<const float *>(base) + elem);
+}
+
+template <bool BF16>
+__device__ __forceinline__ void st_row4(void *base, int64_t elem, float4 v) {
+    if (BF16) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+        uint2 w;
+        w.x = *reinterpret_cast<uint32_t *>(&lo);
+        w.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(base) + elem) = w;
+    } else {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(base) + elem) = v;
+    }
+}
+
 // ---------------------------------------------------------------- dispatch row scatter
 // x[t] is read once and written to each of its receive rows
 // (EM: the slot of every kept pick; RM/FLAT: the row in every destination that got it).
@@ -141,14 +175,15 @@ __global__ void __launch_bounds__(kCopyThreads) gather_picks_kernel(GatherArgs a
 // expert_out[d*cap + r] = sum_j (ascending) recv_topk_w[d, r, j] * y(pick (t, j)) over the
 // local picks j (recv_topk_idx >= 0); the others are masked to weight 0 (skipped).
 struct ReduceArgs {
-    const float *ypick;
-    float *out;
+    const void *ypick;   // float32 or bf16 rows (the kernel's BF16 parameter)
+    void *out;
     const int32_t *recv_count, *num_recv, *recv_src, *recv_topk_idx, *pick_pos;
     const float *recv_topk_w;
     int W, Tr, k, H, layout, nchunk;
     int64_t cap;
 };
 
+template <bool BF16>
 __global__ void __launch_bounds__(kCopyThreads) reduce_ranks_kernel(ReduceArgs a) {
     __shared__ int64_t src[kWarpsPerBlock][MOE_MAX_TOPK];
     __shared__ float wt[kWarpsPerBlock][MOE_MAX_TOPK];
@@ -188,12 +223,12 @@ __global__ void __launch_bounds__(kCopyThreads) reduce_ranks_kernel(ReduceArgs a
 #pragma unroll
     for (int u = 0; u < kCopyU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int q = 0; q < n; ++q) {
-        const float *row = a.ypick + src[warp][q] * a.H;
+        const int64_t row = src[warp][q] * a.H;
         const float w = wt[warp][q];
         float4 y[kCopyU];
 #pragma unroll
         for (int u = 0; u < kCopyU; ++u)
-            if (c0 + 32 * u < nv) y[u] = ld_nc_f4(row + 4 * (c0 + 32 * u));
+            if (c0 + 32 * u < nv) y[u] = ld_row4<BF16>(a.ypick, row + 4 * (c0 + 32 * u));
 #pragma unroll
         for (int u = 0; u < kCopyU; ++u) {
             acc[u].x = fmaf(w, y[u].x, acc[u].x);
@@ -202,17 +237,16 @@ __global__ void __launch_bounds__(kCopyThreads) reduce_ranks_kernel(ReduceArgs a
             acc[u].w = fmaf(w, y[u].w, acc[u].w);
         }
     }
-    float4 *o = reinterpret_cast<float4 *>(a.out + gr * a.H);
 #pragma unroll
     for (int u = 0; u < kCopyU; ++u)
-        if (c0 + 32 * u < nv) o[c0 + 32 * u] = acc[u];
+        if (c0 + 32 * u < nv) st_row4<BF16>(a.out, gr * a.H + 4 * (c0 + 32 * u), acc[u]);
 }
 
 // ----------------------------------------------------------------------------- combine
 // EM:      out[t] = bf16( sum_j w[t, j] * expert_out[slot[t, j]] ), kept picks, ascending j
 // RM/FLAT: out[t] = bf16( sum_d expert_out[d*cap + recv_row[t, d]] ), ascending d
 struct CombineArgs {
-    const float *eo;
+    const void *eo;      // float32 or bf16 rows (the kernel's BF16 parameter)
     const float *topk_w;
     const int32_t *slot, *recv_row;
     uint16_t *out;
@@ -220,6 +254,7 @@ struct CombineArgs {
     int64_t cap;
 };
 
+template <bool BF16>
 __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
     __shared__ int64_t src[kWarpsPerBlock][MOE_MAX_WORLD > MOE_MAX_TOPK ? MOE_MAX_WORLD : MOE_MAX_TOPK];
     __shared__ float wt[kWarpsPerBlock][MOE_MAX_WORLD > MOE_MAX_TOPK ? MOE_MAX_WORLD : MOE_MAX_TOPK];
@@ -259,12 +294,12 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
 #pragma unroll
     for (int u = 0; u < kCopyU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int q = 0; q < ns; ++q) {
-        const float *row = a.eo + src[warp][q] * a.H;
+        const int64_t row = src[warp][q] * a.H;
         const float w = wt[warp][q];
         float4 y[kCopyU];
 #pragma unroll
         for (int u = 0; u < kCopyU; ++u)
-            if (c0 + 32 * u < nv) y[u] = ld_nc_f4(row + 4 * (c0 + 32 * u));
+            if (c0 + 32 * u < nv) y[u] = ld_row4<BF16>(a.eo, row + 4 * (c0 + 32 * u));
 #pragma unroll
         for (int u = 0; u < kCopyU; ++u) {
             if (em) {
@@ -327,9 +362,6 @@ __device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v
                                                  __NV_SATFINITE, __NV_E4M3);
     return lo | (hi << 16);
 }
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // FP8 dispatch: like dispatch_copy_kernel, but each 128-column block of x[t] is quantised
 // once (16 lanes x 8 columns: the half-warp reduces amax) and the e4m3 codes plus the
@@ -541,25 +573,27 @@ cudaError_t launch_gather_picks(const Routing &r, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_reduce_ranks(const Routing &r, float *expert_out, cudaStream_t s) {
+cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.T == 0) return cudaSuccess;
     const int nchunk = (int)((p.H / 4 + 32 * kCopyU - 1) / (32 * kCopyU));
     ReduceArgs a{r.ypick, expert_out, r.recv_count, r.num_recv, r.recv_src, r.recv_topk_idx,
                  r.pick_pos, r.recv_topk_w, (int)p.W, (int)p.Tr, (int)p.k, (int)p.H, p.layout,
                  nchunk, p.cap};
-    reduce_ranks_kernel<<<blocks_for(p.W * p.cap * nchunk), kCopyThreads, 0, s>>>(a);
+    if (p.eo_bf16) reduce_ranks_kernel<true><<<blocks_for(p.W * p.cap * nchunk), kCopyThreads, 0, s>>>(a);
+    else reduce_ranks_kernel<false><<<blocks_for(p.W * p.cap * nchunk), kCopyThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const Routing &r, const float *expert_out, const float *topk_w,
+cudaError_t launch_combine(const Routing &r, const void *expert_out, const float *topk_w,
                            uint16_t *out, cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.T == 0) return cudaSuccess;
     const int nchunk = (int)((p.H / 4 + 32 * kCopyU - 1) / (32 * kCopyU));
     CombineArgs a{expert_out, topk_w, r.slot, r.recv_row, out, (int)p.T, (int)p.k, (int)p.W,
                   (int)p.H, p.layout, nchunk, p.cap};
-    combine_kernel<<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
+    if (p.eo_bf16) combine_kernel<true><<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
+    else combine_kernel<false><<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

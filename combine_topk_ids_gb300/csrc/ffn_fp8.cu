@@ -29,6 +29,7 @@
 //               GEMM2: fp32 rows)
 // The tile order, bounded waits and abort path are those of the bf16 kernel (ffn_tc.cu).
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
 #include "tc_common.cuh"
@@ -87,6 +88,7 @@ struct F8Args {
     int64_t b_rows;           // rows of B per expert (N)
     const float *b_scale;     // [E][N/128][K/128]
     int mode;                 // 0: SwiGLU -> e4m3 act + scales; 1: fp32 rows
+    int out_bf16;             // mode 1: rows stored as bf16 (round to nearest even)
     void *out;                // mode 0: act codes [P, I]; mode 1: fp32 rows
     float *out_scale;         // mode 0: act scales [I/128][out_scale_ld]
     int64_t out_scale_ld;
@@ -311,10 +313,22 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) + m0;
                 for (int h = 0; h < 2; ++h) {
                     if (!mbar_wait(afull0 + 8 * h, (uint32_t)ntile & 1, abort_flag, a.status)) { ok = false; break; }
-                    float *out = reinterpret_cast<float *>(a.out) + (int64_t)nbk * a.bn + 128 * h + 4 * lane;
+                    const int64_t col = (int64_t)nbk * a.bn + 128 * h + 4 * lane;
+                    if (a.out_bf16) {
+                        __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) + col;
 #pragma unroll 4
-                    for (int r = warp - 2; r < valid; r += 2)
-                        *reinterpret_cast<float4 *>(out + (obase + r) * a.out_ld) = act_s[r * 32 + (lane ^ (r & 31))];
+                        for (int r = warp - 2; r < valid; r += 2) {
+                            const float4 v = act_s[r * 32 + (lane ^ (r & 31))];
+                            __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                            *reinterpret_cast<uint2 *>(out + (obase + r) * a.out_ld) =
+                                make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                        }
+                    } else {
+                        float *out = reinterpret_cast<float *>(a.out) + col;
+#pragma unroll 4
+                        for (int r = warp - 2; r < valid; r += 2)
+                            *reinterpret_cast<float4 *>(out + (obase + r) * a.out_ld) = act_s[r * 32 + (lane ^ (r & 31))];
+                    }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(aempty0 + 8 * h);
                 }
@@ -412,8 +426,23 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                         make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(afull0 + 8 * half);
-            } else if (live) {
+            } else if (live && a.out_bf16) {
                 // direct row stores: ncol = 64 (128-column tiles) or 128 columns per thread
+                uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + orow * a.out_ld +
+                                                     (int64_t)nbk * a.bn + half * ncol);
+                auto pk = [](float2 v) {
+                    __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+                    return *reinterpret_cast<uint32_t *>(&b);
+                };
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    o[q] = make_uint4(pk(acc[4 * q]), pk(acc[4 * q + 1]), pk(acc[4 * q + 2]), pk(acc[4 * q + 3]));
+                if (ncol == 128) {
+#pragma unroll
+                    for (int q = 8; q < 16; ++q)
+                        o[q] = make_uint4(pk(acc[4 * q]), pk(acc[4 * q + 1]), pk(acc[4 * q + 2]), pk(acc[4 * q + 3]));
+                }
+            } else if (live) {
                 float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + orow * a.out_ld +
                                                        (int64_t)nbk * a.bn + half * ncol);
 #pragma unroll
@@ -500,7 +529,7 @@ int launch_gemm1_fp8(const Routing &r, const uint8_t *w1qp, const float *w1sp, c
     return launch_gemm_fp8<0>(mA, mB, g, (p.P / F_BM + p.E) * g.nb, s);
 }
 
-int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, float *expert_out,
+int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, void *expert_out,
                      cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.P == 0) return MOE_OK;
@@ -513,7 +542,7 @@ int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, flo
     g.bn = bn; g.nb = (int)(p.H / bn); g.kb = (int)(p.I / F_BK);
     g.a_mode = 1; g.a_cap = 0; g.a_scale = r.act_scales; g.a_scale_ld = p.P;
     g.b_rows = p.H; g.b_scale = w2s;
-    g.mode = 1; g.out_ld = p.H;
+    g.mode = 1; g.out_ld = p.H; g.out_bf16 = p.eo_bf16;
     if (em) { g.out = expert_out; g.out_mode = 0; g.out_cap = p.cap; }
     else { g.out = r.ypick; g.out_mode = 1; g.out_cap = 0; }
     return launch_gemm_fp8<1>(mA, mB, g, (p.P / F_BM + p.E) * g.nb, s);

@@ -70,6 +70,7 @@ struct FfnArgs {
     int64_t a_cap;
     int64_t b_rows;   // rows of B per expert (N)
     int mode;      // 0: SwiGLU epilogue -> act as a bf16 (hi, lo) pair; 1: fp32 store
+    int out_bf16;  // mode 1: store the rows as bf16 (round to nearest even) instead
     void *out;     // mode 0: act_hi; mode 1: fp32 rows
     void *out2;    // mode 0: act_lo
     int64_t out_ld;   // elements per output row
@@ -351,6 +352,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 }
+            } else if (a.out_bf16) {
+                __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) + orow * a.out_ld + (int64_t)nbk * a.bn;
+#pragma unroll 1
+                for (int c = 0; c < a.bn; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c, v);
+                    tmem_wait_ld();
+                    if (row < valid) {
+                        uint4 *o = reinterpret_cast<uint4 *>(out + c);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * h]),
+                                                                         __uint_as_float(v[8 * q + 2 * h + 1]));
+                                w[h] = *reinterpret_cast<uint32_t *>(&b);
+                            }
+                            o[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
             } else {
                 float *out = reinterpret_cast<float *>(a.out) + orow * a.out_ld + (int64_t)nbk * a.bn;
 #pragma unroll 1
@@ -500,7 +523,7 @@ int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s) {
     return launch_gemm<false, false>(mA, mA, mB, g, max_mblocks(p, BM) * g.nb, s);
 }
 
-int launch_gemm2(const Routing &r, const uint16_t *w2, float *expert_out, cudaStream_t s) {
+int launch_gemm2(const Routing &r, const uint16_t *w2, void *expert_out, cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.P == 0) return MOE_OK;
     const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
@@ -512,7 +535,7 @@ int launch_gemm2(const Routing &r, const uint16_t *w2, float *expert_out, cudaSt
         return MOE_ERR_CUDA;
     FfnArgs g = base_args(r, pair);
     g.bn = bn; g.nb = (int)(p.H / bn); g.kb = (int)(p.I / BK);
-    g.a_mode = 1; g.a_cap = 0; g.b_rows = p.H; g.mode = 1; g.out_ld = p.H;
+    g.a_mode = 1; g.a_cap = 0; g.b_rows = p.H; g.mode = 1; g.out_ld = p.H; g.out_bf16 = p.eo_bf16;
     if (em) { g.out = expert_out; g.out_mode = 0; g.out_cap = p.cap; }
     else { g.out = r.ypick; g.out_mode = 1; g.out_cap = 0; }
     if (pair) return launch_gemm<true, true>(mA, mA2, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);

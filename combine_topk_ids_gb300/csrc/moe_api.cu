@@ -52,7 +52,7 @@ int make_plan(const moe_geom &g, Plan *p) {
         g.intermediate < 1)
         return MOE_ERR_INVALID_ARGUMENT;
     if (g.layout < 0 || g.layout > 2 || g.algorithm < 0 || g.algorithm > 1 || g.quant < 0 ||
-        g.quant > 1)
+        g.quant > 1 || g.expert_out_dtype < 0 || g.expert_out_dtype > 1)
         return MOE_ERR_INVALID_ARGUMENT;
     if (g.top_k < 1 || g.top_k > MOE_MAX_TOPK) return MOE_ERR_TOPK;
     if (g.num_experts % g.world != 0) return MOE_ERR_EXPERTS_NOT_DIVISIBLE;
@@ -72,6 +72,7 @@ int make_plan(const moe_geom &g, Plan *p) {
     q.T = g.num_tokens; q.W = g.world; q.Tr = g.max_tok; q.cap = cap; q.E = g.num_experts;
     q.k = g.top_k; q.H = g.hidden; q.I = g.intermediate; q.P = P; q.layout = g.layout;
     q.quant = g.quant;
+    q.eo_bf16 = g.expert_out_dtype == MOE_EXPERT_OUT_BFLOAT16;
     // routing chunk: about 256 chunks over the whole capacity, 32..1024 tokens each
     int64_t want = (cap + 255) / 256;
     int tb = 32;
@@ -117,7 +118,7 @@ int make_plan(const moe_geom &g, Plan *p) {
     q.act_scales = take(f8 ? 4 * P * (I / 128) : 0);
     q.apick = take(em ? 0 : eb * P * H);
     q.apick_scales = take(em || !f8 ? 0 : 4 * P * (H / 128));
-    q.ypick = take(em ? 0 : 4 * P * H);
+    q.ypick = take(em ? 0 : (q.eo_bf16 ? 2 : 4) * P * H);
     q.total = off;
     return MOE_OK;
 }
@@ -139,7 +140,7 @@ Routing carve(const Plan &p, void *ws) {
     r.act = reinterpret_cast<uint16_t *>(b + p.act);
     r.act_lo = reinterpret_cast<uint16_t *>(b + p.act_lo);
     r.apick = reinterpret_cast<uint16_t *>(b + p.apick);
-    r.ypick = reinterpret_cast<float *>(b + p.ypick);
+    r.ypick = b + p.ypick;
     const bool f8 = p.quant == MOE_QUANT_FP8_E4M3;
     r.recv_scales = f8 ? reinterpret_cast<float *>(b + p.recv_scales) : nullptr;
     r.act_scales = f8 ? reinterpret_cast<float *>(b + p.act_scales) : nullptr;
@@ -184,7 +185,7 @@ int moe_expert_out_size(const moe_geom *g, size_t *bytes) {
     int rc = make_plan(*g, &p);
     if (rc != MOE_OK) return rc;
     const int64_t rows = (p.layout == MOE_LAYOUT_EXPERT_MAJOR ? p.E : p.W) * p.cap;
-    *bytes = (size_t)rows * (size_t)p.H * sizeof(float);
+    *bytes = (size_t)rows * (size_t)p.H * (p.eo_bf16 ? 2 : 4);
     return MOE_OK;
 }
 
@@ -267,7 +268,7 @@ int moe_prepare_weights(const moe_geom *g, const void *w1_dev, void *w1_prepared
 }
 
 int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void *w2_dev,
-                   float *expert_out_dev, void *stream) {
+                   void *expert_out_dev, void *stream) {
     Plan p;
     int rc = handle_plan(h, &p);
     if (rc != MOE_OK) return rc;
@@ -294,7 +295,7 @@ int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void 
 
 int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
                        const float *w1_scales_prepared_dev, const void *w2q_dev,
-                       const float *w2_scales_dev, float *expert_out_dev, void *stream) {
+                       const float *w2_scales_dev, void *expert_out_dev, void *stream) {
     Plan p;
     int rc = handle_plan(h, &p);
     if (rc != MOE_OK) return rc;
@@ -366,7 +367,7 @@ int moe_prepare_weights_fp8(const moe_geom *g, const void *w1q_dev, const float 
                : MOE_ERR_CUDA;
 }
 
-int moe_combine(const moe_handle *h, const float *expert_out_dev, const float *topk_weights_dev,
+int moe_combine(const moe_handle *h, const void *expert_out_dev, const float *topk_weights_dev,
                 void *out_dev, void *stream) {
     Plan p;
     int rc = handle_plan(h, &p);
@@ -391,7 +392,7 @@ int moe_combine(const moe_handle *h, const float *expert_out_dev, const float *t
 int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids_host,
                      int ids_dtype, const float *topk_weights_host, void *out_host,
                      void *x_dev, void *topk_ids_dev, float *topk_weights_dev, void *out_dev,
-                     const void *w1_prepared_dev, const void *w2_dev, float *expert_out_dev,
+                     const void *w1_prepared_dev, const void *w2_dev, void *expert_out_dev,
                      void *workspace_dev, size_t workspace_bytes, moe_handle *h, void *stream) {
     if (!g || !h) return MOE_ERR_INVALID_ARGUMENT;
     if (ids_dtype != MOE_IDS_INT32 && ids_dtype != MOE_IDS_INT64) return MOE_ERR_IDS_DTYPE;

@@ -20,6 +20,7 @@ struct Plan {
     int64_t T, W, Tr, cap, E, k, H, I, P;   // P = T*k picks
     int layout;
     int quant;      // moe_quant
+    int eo_bf16;    // expert_out (and the RM/FLAT per-pick rows) in bf16
     int64_t nrecv;  // rows of the receive buffer: E*cap (EM) or W*cap (RM/FLAT)
     int tb;         // tokens per routing block
     int nbpr;       // routing blocks per logical rank
@@ -41,7 +42,7 @@ struct Routing {
         *blk_dhist, *blk_dbase;
     float *recv_topk_w;
     uint16_t *recv_x, *act, *act_lo, *apick;   // act / act_lo: SwiGLU output as a bf16 pair
-    float *ypick;
+    void *ypick;    // RM/FLAT per-pick GEMM2 rows: float32, or bf16 with eo_bf16
     // FP8 geometry: recv_x / act / apick hold e4m3 codes (one byte per element); their
     // scales are column-block major ([cols/128][rows]); act_lo is unused
     float *recv_scales, *act_scales, *apick_scales;
@@ -55,15 +56,16 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
 int routing_launches(const Plan &p);   // kernels launch_routing queues for this geometry
 cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream_t s);
 cudaError_t launch_gather_picks(const Routing &r, cudaStream_t s);
-cudaError_t launch_reduce_ranks(const Routing &r, float *expert_out, cudaStream_t s);
-cudaError_t launch_combine(const Routing &r, const float *expert_out, const float *topk_w,
+// expert_out: float32, or bf16 when the plan's eo_bf16 is set
+cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, cudaStream_t s);
+cudaError_t launch_combine(const Routing &r, const void *expert_out, const float *topk_w,
                            uint16_t *out, cudaStream_t s);
 cudaError_t launch_prepare_w1(const moe_geom &g, const uint16_t *w1, uint16_t *w1p,
                               cudaStream_t s);
 // Grouped SwiGLU FFN: GEMM1 (+SiLU*mul) into act, GEMM2 into expert_out (EM) or the
 // per-pick scratch (RM/FLAT).  Return MOE_OK or a moe_error.
 int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s);
-int launch_gemm2(const Routing &r, const uint16_t *w2, float *expert_out, cudaStream_t s);
+int launch_gemm2(const Routing &r, const uint16_t *w2, void *expert_out, cudaStream_t s);
 
 // ---- FP8 (moe_quant MOE_QUANT_FP8_E4M3) -----------------------------------------------
 cudaError_t launch_dispatch_quant(const Routing &r, const uint16_t *x, cudaStream_t s);
@@ -75,7 +77,7 @@ cudaError_t launch_quantize_weights_fp8(const uint16_t *w, int64_t E, int64_t ro
 cudaError_t launch_prepare_w1_fp8(const moe_geom &g, const uint8_t *w1q, const float *w1s,
                                   uint8_t *w1qp, float *w1sp, cudaStream_t s);
 int launch_gemm1_fp8(const Routing &r, const uint8_t *w1qp, const float *w1sp, cudaStream_t s);
-int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, float *expert_out,
+int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, void *expert_out,
                      cudaStream_t s);
 
 int num_sms();   // SM count of the current device (cached per device)

@@ -72,6 +72,19 @@ typedef enum { MOE_IDS_INT32 = 0, MOE_IDS_INT64 = 1 } moe_ids_dtype;
  */
 typedef enum { MOE_QUANT_NONE = 0, MOE_QUANT_FP8_E4M3 = 1 } moe_quant;
 
+/*
+ * Element type of expert_out (the expert stage's output and combine's input) and of the
+ * per-pick rows the RANK_MAJOR / FLAT expert stage reduces [FI-3: the packed buffers that
+ * return to combine are bf16].
+ *   MOE_EXPERT_OUT_FLOAT32   float32 (default).
+ *   MOE_EXPERT_OUT_BFLOAT16  bfloat16, rounded to nearest even from the fp32 GEMM result
+ *                            (and, for RANK_MAJOR / FLAT, once more after the fp32 sum over
+ *                            the row's local picks); combine accumulates in fp32 as before.
+ *                            Half the bytes of the largest intermediate, at the price of
+ *                            one or two extra bf16 roundings before the final one.
+ */
+typedef enum { MOE_EXPERT_OUT_FLOAT32 = 0, MOE_EXPERT_OUT_BFLOAT16 = 1 } moe_expert_out_dtype;
+
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARGUMENT = -1,      /* null pointer, non-positive size, bad enum          */
@@ -127,6 +140,7 @@ typedef struct {
     int32_t layout;       /* moe_layout                                                    */
     int32_t algorithm;    /* moe_algorithm                                                 */
     int32_t quant;        /* moe_quant: precision of the received rows and expert GEMMs    */
+    int32_t expert_out_dtype; /* moe_expert_out_dtype                                      */
 } moe_geom;
 
 /*
@@ -194,7 +208,8 @@ typedef struct {
 int moe_workspace_size(const moe_geom *g, size_t *bytes);
 
 /*
- * moe_expert_out_size - bytes of the float32 expert_out buffer moe_expert_ffn writes:
+ * moe_expert_out_size - bytes of the expert_out buffer moe_expert_ffn writes (float32, or
+ * bf16 with MOE_EXPERT_OUT_BFLOAT16):
  * EM [E, cap, H]; RM/FLAT [W, cap, H] (the receive layout, float32).
  */
 int moe_expert_out_size(const moe_geom *g, size_t *bytes);
@@ -244,11 +259,12 @@ int moe_prepare_weights(const moe_geom *g, const void *w1_dev, void *w1_prepared
  *   RM/FLAT: expert_out[d*cap + r] = sum over the row's LOCAL picks j (ascending) of
  *            recv_topk_weights[d][r][j] * y_j; non-local picks are masked to weight 0
  *   w1_prepared_dev bf16 from moe_prepare_weights; w2_dev bf16 [E, H, I]
- *   expert_out_dev  float32, moe_expert_out_size bytes, 16-byte aligned
+ *   expert_out_dev  float32 or bf16 (geom expert_out_dtype), moe_expert_out_size bytes,
+ *                   16-byte aligned
  * Runs on tcgen05 tensor cores (bf16 x bf16 -> fp32 in tensor memory).
  */
 int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void *w2_dev,
-                   float *expert_out_dev, void *stream);
+                   void *expert_out_dev, void *stream);
 
 /*
  * moe_combine - return expert outputs to token order [MC-EP Buffer.combine; FI-3]:
@@ -256,12 +272,13 @@ int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void 
  *                           topk_weights[t, j] * expert_out[slot[t, j]] )
  *   RM/FLAT: out[t] = bf16( sum over destinations d ascending that received t of
  *                           expert_out[d*cap + recv_row[t, d]] )   (unweighted)
+ *   expert_out_dev   float32 or bf16 (geom expert_out_dtype), as moe_expert_ffn wrote it
  *   topk_weights_dev float32 [T, k] (EM; ignored and may be NULL for RM/FLAT)
  *   out_dev          bf16 [T, H], 16-byte aligned
  * fp32 accumulation, one round-to-nearest-even to bf16.  Tokens without any kept
  * pick get zeros.
  */
-int moe_combine(const moe_handle *h, const float *expert_out_dev,
+int moe_combine(const moe_handle *h, const void *expert_out_dev,
                 const float *topk_weights_dev, void *out_dev, void *stream);
 
 /*
@@ -300,7 +317,7 @@ int moe_prepare_weights_fp8(const moe_geom *g, const void *w1q_dev, const float 
  */
 int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
                        const float *w1_scales_prepared_dev, const void *w2q_dev,
-                       const float *w2_scales_dev, float *expert_out_dev, void *stream);
+                       const float *w2_scales_dev, void *expert_out_dev, void *stream);
 
 /*
  * moe_forward_host - the whole layer end to end from HOST buffers, on one stream:
@@ -316,7 +333,7 @@ int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
 int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids_host,
                      int ids_dtype, const float *topk_weights_host, void *out_host,
                      void *x_dev, void *topk_ids_dev, float *topk_weights_dev, void *out_dev,
-                     const void *w1_prepared_dev, const void *w2_dev, float *expert_out_dev,
+                     const void *w1_prepared_dev, const void *w2_dev, void *expert_out_dev,
                      void *workspace_dev, size_t workspace_bytes, moe_handle *h, void *stream);
 
 /*

@@ -20,6 +20,8 @@ Sources (page title, section):
   * Mooncake EP guide, "Buffer.combine(...)": expert outputs are returned by routing
     weight and reduced to the token's owner.
 Readings where the pages are silent (each listed in the design notes):
+  * with the bf16 expert_out option the expert stage's outputs are rounded to bf16 where
+    the GPU rounds them (each pick's y; for RANK_MAJOR / FLAT also the per-row sum);
   * gate = rows [0, I) of w1[e], up = rows [I, 2I); SwiGLU act = silu(gate) * up with
     silu(g) = g / (1 + exp(-g))  (parity unpinned by the pages: a fixed convention);
   * the expert FFN is evaluated in full precision from the bf16 weights and inputs: no
@@ -205,9 +207,10 @@ def pick_outputs(geom, rt, x_bits, w1, w2, picks=None, expert_fn=None):
     return out
 
 
-def combine_em(geom, rt, topk_w, y_of_pick, tokens):
+def combine_em(geom, rt, topk_w, y_of_pick, tokens, eo_bf16=False):
     """EXPERT_MAJOR combine: out[t] = bf16( sum_j w[t, j] * expert_out[slot[t, j]] ),
-    masked picks contribute nothing; float64 sum in ascending j."""
+    masked picks contribute nothing; float64 sum in ascending j.  eo_bf16: expert_out
+    holds bf16(y) (the bf16 expert_out option)."""
     k = geom["k"]
     pp = rt["pick_pos"]
     w = np.asarray(topk_w, dtype=np.float64).reshape(-1, k)
@@ -217,17 +220,19 @@ def combine_em(geom, rt, topk_w, y_of_pick, tokens):
         for j in range(k):
             if pp[t, j] < 0:
                 continue
-            term = w[t, j] * y_of_pick(t * k + j)
+            y = y_of_pick(t * k + j)
+            term = w[t, j] * (round_bf16(y) if eo_bf16 else y)
             acc = term if acc is None else acc + term
         res.append(np.zeros(geom["H"]) if acc is None else acc)
     return round_bf16(np.array(res))
 
 
-def ffn_ranks(geom, rt, topk_w, y_of_pick, dest_rows):
+def ffn_ranks(geom, rt, topk_w, y_of_pick, dest_rows, eo_bf16=False):
     """RANK_MAJOR / FLAT expert stage on received rows: for destination d and row r with
     token t, expert_out[d, r] = sum over j ascending of recv_topk_w[d, r, j] * y(t, j),
     non-local picks (recv_topk_idx == -1) masked to weight 0 (skipped).
-    dest_rows: iterable of (d, r).  Returns float64 [len, H]."""
+    dest_rows: iterable of (d, r).  Returns float64 [len, H].  eo_bf16 (the bf16
+    expert_out option): each y(t, j) is held as bf16 and the sum is rounded to bf16."""
     k = geom["k"]
     res = []
     for d, r in dest_rows:
@@ -236,8 +241,9 @@ def ffn_ranks(geom, rt, topk_w, y_of_pick, dest_rows):
         for j in range(k):
             if rt["recv_topk_idx"][d, r, j] < 0:
                 continue
-            acc = acc + float(rt["recv_topk_w"][d, r, j]) * y_of_pick(t * k + j)
-        res.append(acc)
+            y = y_of_pick(t * k + j)
+            acc = acc + float(rt["recv_topk_w"][d, r, j]) * (round_bf16(y) if eo_bf16 else y)
+        res.append(round_bf16(acc) if eo_bf16 else acc)
     return np.array(res)
 
 
@@ -255,20 +261,22 @@ def combine_ranks(geom, rt, expert_out_of, tokens):
     return round_bf16(np.array(res))
 
 
-def layer(geom, x_bits, ids, topk_w, w1, w2, tokens=None, expert_fn=None, active=None):
+def layer(geom, x_bits, ids, topk_w, w1, w2, tokens=None, expert_fn=None, active=None,
+          eo_bf16=False):
     """The whole layer for `tokens` (default all): route -> dispatch -> expert FFN ->
     combine, returning (route metadata, out [len(tokens), H] float64 holding bf16 values).
-    Only the picks of the requested tokens are evaluated.  active: EP rank-health mask."""
+    Only the picks of the requested tokens are evaluated.  active: EP rank-health mask.
+    eo_bf16: expert_out (and the RANK_MAJOR / FLAT per-pick rows) held as bf16."""
     T, k = geom["T"], geom["k"]
     rt = route(geom, ids, topk_w, active)
     tokens = np.arange(T) if tokens is None else np.asarray(tokens)
     picks = [t * k + j for t in tokens for j in range(k) if rt["pick_pos"][t, j] >= 0]
     ys = pick_outputs(geom, rt, x_bits, w1, w2, picks=picks, expert_fn=expert_fn)
     if geom["layout"] == "EM":
-        return rt, combine_em(geom, rt, topk_w, ys.__getitem__, tokens)
+        return rt, combine_em(geom, rt, topk_w, ys.__getitem__, tokens, eo_bf16)
     rows = sorted({(d, int(rt["recv_row"][t, d])) for t in tokens for d in range(geom["W"])
                    if rt["recv_row"][t, d] >= 0})
-    eo = dict(zip(rows, ffn_ranks(geom, rt, topk_w, ys.__getitem__, rows)))
+    eo = dict(zip(rows, ffn_ranks(geom, rt, topk_w, ys.__getitem__, rows, eo_bf16)))
     return rt, combine_ranks(geom, rt, lambda d, r: eo[(d, r)], tokens)
 
 

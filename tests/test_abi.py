@@ -52,7 +52,7 @@ def _geom(**kw):
     (dict(I=100), -4),               # intermediate % 128
     (dict(T=65), -5),                # num_tokens > world * max_tok
     (dict(k=0), -6), (dict(k=33), -6),
-    (dict(W=0), -1), (dict(layout=3), -1), (dict(algo=2), -1), (dict(quant=2), -1),
+    (dict(W=0), -1), (dict(layout=3), -1), (dict(algo=2), -1), (dict(quant=2), -1), (dict(expert_out=2), -1),
     (dict(W=128, E=128, Tr=1, T=1), -13),
 ])
 def test_geometry_errors(lib, kw, code):
@@ -70,6 +70,9 @@ def test_workspace_size_grows_with_capacity(lib):
     assert a >= 8 * 64 * 256 * 2
     assert moe.moe_expert_out_size(_geom()) == 8 * 64 * 256 * 4
     assert moe.moe_expert_out_size(_geom(layout="RM")) == 2 * 64 * 256 * 4
+    # bf16 expert_out: half the bytes, and a smaller workspace (RM/FLAT per-pick rows)
+    assert moe.moe_expert_out_size(_geom(expert_out="bf16")) * 2 == moe.moe_expert_out_size(_geom())
+    assert moe.moe_workspace_size(_geom(layout="RM", expert_out="bf16")) < moe.moe_workspace_size(_geom(layout="RM"))
     # FP8 rows take one byte per element (plus a float scale per 128 columns)
     f = moe.moe_workspace_size(_geom(quant="fp8"))
     assert f < a and f >= 8 * 64 * 256 + 8 * 64 * 2 * 4

@@ -354,11 +354,63 @@ def test_planted_mistakes_are_caught(monkeypatch):
     # a dropped term in the per-destination reduction
     good_fr = oracle.ffn_ranks
 
-    def drop_last(geom, rt, topk_w, y_of_pick, rows):
+    def drop_last(geom, rt, topk_w, y_of_pick, rows, eo_bf16=False):
         rt2 = dict(rt)
         rti = rt["recv_topk_idx"].copy()
         rti[..., -1] = -1
         rt2["recv_topk_idx"] = rti
-        return good_fr(geom, rt2, topk_w, y_of_pick, rows)
+        return good_fr(geom, rt2, topk_w, y_of_pick, rows, eo_bf16)
     monkeypatch.setattr(oracle, "ffn_ranks", drop_last)
     assert not check()
+
+
+# ------------------------------------------------------------- bf16 expert_out option
+def test_bf16_expert_out_identity_expert_em():
+    """EM, identity expert: every y is a bf16 value already, so holding expert_out in bf16
+    changes nothing (closed form of the same layer)."""
+    c = _tiny_cfg("EM", mask_frac=0.2)
+    x, ids, w, w1, w2 = _inputs(c)
+    g = oracle.geom_of(c)
+    ident = lambda e, xr: xr  # noqa: E731
+    _, a = oracle.layer(g, x, ids, w, w1, w2, expert_fn=ident)
+    _, b = oracle.layer(g, x, ids, w, w1, w2, expert_fn=ident, eo_bf16=True)
+    np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("layout", ["RM", "FLAT"])
+def test_bf16_expert_out_single_local_pick(layout):
+    """RANK_MAJOR / FLAT with one pick per token of weight 1 and the identity expert: the
+    per-row sum is x itself, a bf16 value, so both roundings are exact."""
+    c = _tiny_cfg(layout).with_(k=1)
+    x, ids, w, w1, w2 = _inputs(c)
+    w = np.ones_like(w)
+    g = oracle.geom_of(c)
+    ident = lambda e, xr: xr  # noqa: E731
+    _, a = oracle.layer(g, x, ids, w, w1, w2, expert_fn=ident)
+    _, b = oracle.layer(g, x, ids, w, w1, w2, expert_fn=ident, eo_bf16=True)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(b, oracle.bf16_bits_to_f64(x))
+
+
+@pytest.mark.parametrize("layout", ["EM", "RM", "FLAT"])
+def test_bf16_expert_out_within_rounding_bound(layout):
+    """A real expert: the bf16 option moves each output by at most the bf16 rounding of every
+    held term (half an ulp each, times |weight|) plus the final rounding, and it does move
+    some outputs (the option has an effect)."""
+    c = _tiny_cfg(layout)
+    x, ids, w, w1, w2 = _inputs(c)
+    g = oracle.geom_of(c)
+    rt, a = oracle.layer(g, x, ids, w, w1, w2)
+    _, b = oracle.layer(g, x, ids, w, w1, w2, eo_bf16=True)
+    k = c.k
+    picks = [i for i in range(c.tokens * k) if rt["pick_pos"].reshape(-1)[i] >= 0]
+    ys = oracle.pick_outputs(g, rt, x, w1, w2, picks=picks)
+    half_ulp = lambda v: np.ldexp(1.0, np.frexp(np.abs(v))[1] - 9)  # noqa: E731  (bf16: 8 bits)
+    bound = np.zeros((c.tokens, c.H))
+    for i in picks:
+        t = i // k
+        bound[t] += abs(float(w.reshape(-1)[i])) * half_ulp(ys[i]) * (2 if layout != "EM" else 1)
+    # the two final roundings (one per path) and, for RM/FLAT, the row-sum rounding
+    bound += 2 * half_ulp(a) + (2 * half_ulp(np.abs(a) + bound) if layout != "EM" else 0)
+    assert np.all(np.abs(a - b) <= bound + 1e-30)
+    assert np.any(a != b)
