@@ -34,7 +34,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # tokens of the workload the CPU oracle evaluates per timed sample (bounded CPU work)
 ORACLE_SAMPLE_TOKENS = {"tiny_ll_em": 64, "mixtral_ll_em": 4, "dsv3_ll_rm": 4, "dsv3_ht_flat": 2,
                         "ragged_em": 16}
-ORACLE_SAMPLE_TOKENS.update({k + "_fp8": v for k, v in list(ORACLE_SAMPLE_TOKENS.items())})
+ORACLE_SAMPLE_TOKENS.update({k + sfx: v for k, v in list(ORACLE_SAMPLE_TOKENS.items()) for sfx in ("_fp8", "_eo16")})
 
 
 def parse_args():
@@ -73,6 +73,7 @@ def algorithmic_work(cfg, rt):
     f8 = cfg.quant == "fp8"
     eb = 1 if f8 else 2                       # bytes per element of rows, activations, weights
     rs = (4.0 / 128) if f8 else 0.0           # scale bytes per element (one float per 128)
+    ob = 2 if cfg.expert_out == "bf16" else 4  # bytes per expert_out / per-pick row element
     ws = (4.0 / (128 * 128)) if f8 else 0.0   # weight-block scale bytes per weight
     w = {}
     w["routing"] = dict(bytes=2 * T * k * ids_b + T * k * 4 * (3 if em else 2) +
@@ -82,10 +83,10 @@ def algorithmic_work(cfg, rt):
         w["gather_picks"] = dict(bytes=2 * R * H * (eb + rs), flops=0)
     w["gemm1_swiglu"] = dict(bytes=active * 2 * I * H * (eb + ws) + R * H * (eb + rs) + R * I * (eb + rs),
                              flops=4 * R * H * I)
-    w["gemm2"] = dict(bytes=active * H * I * (eb + ws) + R * I * (eb + rs) + R * H * 4, flops=2 * R * H * I)
+    w["gemm2"] = dict(bytes=active * H * I * (eb + ws) + R * I * (eb + rs) + R * H * ob, flops=2 * R * H * I)
     if not em:
-        w["reduce_ranks"] = dict(bytes=R * H * 4 + nrecv * H * 4 + R * 8, flops=0)
-    w["combine"] = dict(bytes=(R * H * 4 + T * k * 8 if em else nrecv * H * 4) + T * H * 2, flops=0)
+        w["reduce_ranks"] = dict(bytes=R * H * ob + nrecv * H * ob + R * 8, flops=0)
+    w["combine"] = dict(bytes=(R * H * ob + T * k * 8 if em else nrecv * H * ob) + T * H * 2, flops=0)
     return w
 
 
@@ -208,7 +209,8 @@ def oracle_sample_time(cfg, case, n_tokens):
         fp8.layer_fp8(g, case.x_bits, case.ids_np, case.w_np, f1, f2, tokens=np.arange(n_tokens), cache=cache)
         return time.perf_counter() - t0
     t0 = time.perf_counter()
-    oracle.layer(g, case.x_bits, case.ids_np, case.w_np, f1, f2, tokens=np.arange(n_tokens))
+    oracle.layer(g, case.x_bits, case.ids_np, case.w_np, f1, f2, tokens=np.arange(n_tokens),
+                 eo_bf16=cfg.expert_out == "bf16")
     return time.perf_counter() - t0
 
 
@@ -264,7 +266,7 @@ def workload_config(cfg, n):
             "algorithm": {"LL": "LOW_LATENCY", "HT": "HIGH_THROUGHPUT"}[cfg.algo],
             "tokens": cfg.tokens, "world": cfg.W, "max_tok_per_rank": cfg.Tr, "hidden": cfg.H,
             "experts": cfg.E, "top_k": cfg.k, "intermediate": cfg.I, "routing": cfg.routing,
-            "ids_dtype": cfg.ids_dtype, "quant": cfg.quant,
+            "ids_dtype": cfg.ids_dtype, "quant": cfg.quant, "expert_out": cfg.expert_out,
             "l2": "flushed (512 MiB write) before every timed step",
             "parallelism": "replicas x%d" % n if n > 1 else "single GPU"}
 
@@ -281,7 +283,7 @@ def run_ours(args, cfg, rank, world, dist):
     dev = torch.device("cuda", torch.cuda.current_device())
     case = make_case(cfg, dev)
     layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout, cfg.algo,
-                             quant=cfg.quant)
+                             quant=cfg.quant, expert_out=cfg.expert_out)
     layer.set_weights(case.w1, case.w2)
     layer.enable_timing(True)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)

@@ -110,28 +110,35 @@ def test_fp8_dispatch_bit_exact(name):
     np.testing.assert_array_equal(scales[:, rows].T, sc[toks])
 
 
-def _check_layer(cfg, active=None):
-    case = make_case(cfg, "cuda")
-    layer = _layer(cfg)
-    layer.set_weights(case.w1, case.w2)
-    act_t = None if active is None else torch.as_tensor(active, dtype=torch.int32, device="cuda")
-    layer.forward(case.x, case.ids, case.w, act_t)
-    torch.cuda.synchronize()
+def _check_layer(cfg, active=None, tokens=None, layer=None, case=None):
+    """The FP8 layer against the FP8 oracle: every activation code of the checked picks valid,
+    expert_out rows and out within the tolerance plus the flip allowance.  tokens: check only
+    these tokens (their picks, received rows and outputs; full-size workloads)."""
+    if layer is None:
+        case = make_case(cfg, "cuda")
+        layer = _layer(cfg)
+        layer.set_weights(case.w1, case.w2)
+        act_t = None if active is None else torch.as_tensor(active, dtype=torch.int32, device="cuda")
+        layer.forward(case.x, case.ids, case.w, act_t)
+        torch.cuda.synchronize()
     assert layer.status() == (0 if active is None else moe.STATUS_INACTIVE_RANK)
     g = geom_dict(cfg)
     rt, out_ref, res, w2d = fp8.layer_fp8(g, case.x_bits, case.ids_np, case.w_np, case.w1_host,
-                                          case.w2_host, active=active)
+                                          case.w2_host, tokens=tokens, active=active)
     check_routing(layer, rt, cfg)
+    toks = np.arange(cfg.tokens) if tokens is None else np.asarray(tokens)
     k, H, I, P = cfg.k, cfg.H, cfg.I, cfg.tokens * cfg.k
     R = rt["R"]
-    act = layer.view("ffn_act", (max(R, 1), I), torch.uint8).cpu().numpy()
-    act_s = layer.view("ffn_act_scales", (I // 128, P), torch.float32).cpu().numpy()
+    picks = sorted(res)
+    pos = torch.as_tensor([int(rt["pick_pos"].reshape(-1)[i]) for i in picks], dtype=torch.int64, device="cuda")
+    act = layer.view("ffn_act", (max(R, 1), I), torch.uint8)[pos].cpu().numpy()
+    act_s = layer.view("ffn_act_scales", (I // 128, P), torch.float32)[:, pos].cpu().numpy()
     ids = rt["ids"].reshape(-1)
     allow = {}
     n_flip = 0
-    for i, r in res.items():
-        pos = int(rt["pick_pos"].reshape(-1)[i])
-        gc, gs = act[pos], act_s[:, pos]
+    for n, i in enumerate(picks):
+        r = res[i]
+        gc, gs = act[n], act_s[:, n]
         ok = fp8.valid_act_codes(gc[None], r["act_quo"][None], r["act_band"][None])
         assert ok.all(), "pick %d: %d activation codes outside the oracle's band" % (i, (~ok).sum())
         np.testing.assert_allclose(gs, r["act_scales"], rtol=fp8.TC_REL * 4, atol=0)
@@ -139,18 +146,20 @@ def _check_layer(cfg, active=None):
         allow[i] = fp8.flip_allowance(gc[None], gs[None], r["act_codes"][None], r["act_scales"][None],
                                       w2d[int(ids[i])])[0]
     # expert_out
-    eo = layer.expert_out.view(-1, H).cpu().numpy().astype(np.float64)
+    eo = layer.expert_out.view(-1, H)
     cap = cfg.W * cfg.Tr
     wabs = np.abs(case.w_np.astype(np.float64)).reshape(-1)
     if cfg.layout == "EM":
-        picks = sorted(res)
-        got = eo[rt["slot"].reshape(-1)[picks]]
+        idx = torch.as_tensor(rt["slot"].reshape(-1)[picks], dtype=torch.int64, device="cuda")
+        got = eo[idx].cpu().numpy().astype(np.float64)
         ref = np.array([res[i]["y"] for i in picks])
         extra = np.array([allow[i] for i in picks])
     else:
-        rows = [(d, r) for d in range(cfg.W) for r in range(cap) if rt["recv_src"][d, r] >= 0]
+        rows = sorted({(d, int(rt["recv_row"][t, d])) for t in toks for d in range(cfg.W)
+                       if rt["recv_row"][t, d] >= 0})
         ref = oracle.ffn_ranks(g, rt, case.w_np, lambda i: res[i]["y"], rows)
-        got = eo[[d * cap + r for d, r in rows]]
+        idx = torch.as_tensor([d * cap + r for d, r in rows], dtype=torch.int64, device="cuda")
+        got = eo[idx].cpu().numpy().astype(np.float64)
         extra = []
         for d, r in rows:
             t = int(rt["recv_src"][d, r])
@@ -165,10 +174,11 @@ def _check_layer(cfg, active=None):
     assert not bad.any(), "expert_out: %d/%d outside tolerance" % (bad.sum(), bad.size)
     plain_fail = float((np.abs(got - ref) > tol).mean())
     # combined output: the allowance of every pick of the token, times |w|
-    out_extra = np.zeros((cfg.tokens, H))
+    out_extra = np.zeros((len(toks), H))
+    row_of = {int(t): n for n, t in enumerate(toks)}
     for i, a in allow.items():
-        out_extra[i // k] += wabs[i] * a
-    got_out = bf16_tensor_to_f64(layer.out)
+        out_extra[row_of[i // k]] += wabs[i] * a
+    got_out = bf16_tensor_to_f64(layer.out[torch.as_tensor(toks, dtype=torch.int64, device="cuda")])
     bad = ~(np.abs(got_out - out_ref) <= RTOL * np.abs(out_ref) + ATOL + out_extra)
     assert not bad.any(), "out: %d/%d outside tolerance" % (bad.sum(), bad.size)
     return n_flip, len(res) * I, plain_fail
@@ -198,3 +208,22 @@ def test_fp8_handle_rejects_bf16_ffn():
     with pytest.raises(moe.MoeError):
         moe.moe_expert_ffn(layer.handle, layer.w1p, layer.w2, layer.expert_out)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name", list(gen.FP8))
+def test_fp8_full_size(name):
+    """The FP8 workloads at full size, in the launch configuration bench.py times: routing
+    bit-exact; activation codes, expert_out and out on the picks of a few sampled tokens."""
+    cfg = gen.FP8[name]
+    case = make_case(cfg, "cuda")
+    layer = _layer(cfg)
+    layer.set_weights(case.w1, case.w2)
+    layer.forward(case.x, case.ids, case.w)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    ntok = 4 if cfg.E * cfg.H * cfg.I <= (1 << 30) else 2
+    toks = np.unique(np.concatenate([[0, cfg.tokens - 1], rng.choice(cfg.tokens, ntok, replace=False)]))
+    n_flip, n_act, plain_fail = _check_layer(cfg, tokens=toks, layer=layer, case=case)
+    assert n_flip <= max(8, n_act // 500), (n_flip, n_act)
+    del layer, case
+    torch.cuda.empty_cache()

@@ -49,3 +49,28 @@ def test_full_size(name):
     check_out(layer, case, tokens=toks)
     del layer, case
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["mixtral_ll_em_eo16", "dsv3_ll_rm_eo16", "ragged_em_eo16"])
+def test_full_size_bf16_expert_out(name):
+    """The bf16 expert_out option at full size: on sampled tokens, the fraction of outputs
+    outside the benchmark spec's bound against the full-precision (float32 expert_out) oracle."""
+    cfg = gen.ALL[name]
+    case = make_case(cfg, "cuda")
+    layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout,
+                             cfg.algo, expert_out="bf16")
+    layer.set_weights(case.w1, case.w2)
+    layer.forward(case.x, case.ids, case.w)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    toks = _sample(cfg.tokens, 16 if cfg.E * cfg.H * cfg.I <= (1 << 30) else 4, 2)
+    _, ref = oracle.layer(geom_dict(cfg), case.x_bits, case.ids_np, case.w_np, case.w1_host,
+                          case.w2_host, tokens=toks)
+    got = oracle.bf16_bits_to_f64(layer.out[torch.as_tensor(toks)].contiguous().view(torch.int16)
+                                  .cpu().numpy().view(np.uint16))
+    fail = float((np.abs(got - ref) > 2e-2 * np.abs(ref) + 1e-3).mean())
+    print("%s: fraction outside the north-star bound vs the float32 expert_out oracle: %.2e"
+          % (name, fail))
+    assert fail < 2e-2
+    del layer, case
+    torch.cuda.empty_cache()
