@@ -16,17 +16,18 @@
 // One persistent kernel per GEMM, one CTA per SM, 384 threads:
 //   warp 0      TMA producer: 128 x 128 B A tile + up to 256 x 128 B B tile per stage
 //               (SWIZZLE_128B, the same byte layout as the bf16 kernel's 64-column tiles),
-//               4-stage mbarrier ring
+//               3-stage mbarrier ring
 //   warp 1      MMA issuer: per k-block four tcgen05.mma.cta_group::1.kind::f8f6f4 (M=128,
 //               N=256 or 128, K=32) into one of two 256-column TMEM partial-sum buffers
 //   warp 2      TMEM allocator (512 columns)
-//   warps 4-11  promotion + epilogue: warp w reads TMEM lanes 32*(w%4).., warps 4-7 and 8-11
-//               split the columns; per k-block they load the partial sums (tcgen05.ld),
-//               multiply by row scale x weight-block scale and add into registers, then
-//               release the buffer; after the last k-block they write the tile
-//               (GEMM1: SwiGLU, per-row amax over the tile's 128 activation columns
-//               exchanged between the two warps of a lane quarter, e4m3 codes + scale;
-//               GEMM2: fp32 rows)
+//   warps 2-3   epilogue writers: take each finished tile from a shared-memory staging
+//               buffer (GEMM1: the SwiGLU activation and per-half-row maxima, quantised one
+//               thread per row into e4m3 codes + scale; GEMM2: fp32 or bf16 rows, stored in
+//               two 128-column halves as coalesced rows)
+//   warps 4-11  promotion: warp w reads TMEM lanes 32*(w%4).., warps 4-7 and 8-11 split the
+//               columns; per k-block they load the partial sums (tcgen05.ld), multiply by
+//               row scale x weight-block scale and add into registers (packed fp32x2 FMAs),
+//               then release the buffer; after the last k-block they stage the tile
 // The tile order, bounded waits and abort path are those of the bf16 kernel (ffn_tc.cu).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -38,7 +39,7 @@ namespace moe {
 namespace {
 
 constexpr int F_BM = 128;                       // rows per tile
-constexpr int F_BN = 256;                       // widest n-tile
+constexpr int F_BN = 256;                       // n-tile width (GEMM2 uses 128 when H % 256 != 0)
 constexpr int F_BK = 128;                       // k elements (bytes) per stage
 constexpr int F_A_BYTES = F_BM * F_BK;          // 16 KB
 constexpr int F_B_BYTES = F_BN * F_BK;          // 32 KB
