@@ -156,21 +156,23 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
 
 
-# sources that define the grouped-GEMM kernels whose ncu counters are committed
-TRAFFIC_SOURCES = ("combine_topk_ids_gb300/csrc/ffn_tc.cu", "combine_topk_ids_gb300/csrc/tc_common.cuh",
-                   "combine_topk_ids_gb300/csrc/moe_internal.cuh",
-                   "combine_topk_ids_gb300/build.py")
+# sources that define the grouped-GEMM kernels whose ncu counters are committed (the bf16
+# kernels, or the FP8 ones for FP8 workloads)
+TRAFFIC_COMMON = ("combine_topk_ids_gb300/csrc/tc_common.cuh", "combine_topk_ids_gb300/csrc/moe_internal.cuh",
+                  "combine_topk_ids_gb300/build.py")
+TRAFFIC_SOURCES = {"bf16": ("combine_topk_ids_gb300/csrc/ffn_tc.cu",) + TRAFFIC_COMMON,
+                   "fp8": ("combine_topk_ids_gb300/csrc/ffn_fp8.cu",) + TRAFFIC_COMMON}
 
 
-def src_hash():
+def src_hash(quant="bf16"):
     h = hashlib.sha256()
-    for f in TRAFFIC_SOURCES:
+    for f in TRAFFIC_SOURCES[quant]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload, kernel):
+def ncu_traffic(workload, kernel, quant="bf16"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
     kernel sources (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -179,7 +181,7 @@ def ncu_traffic(workload, kernel):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("src_sha") != src_hash():
+    if not e or e.get("src_sha") != src_hash(quant):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -345,7 +347,7 @@ def run_ours(args, cfg, rank, world, dist):
         roof = {"bound": "tensor", "achieved": wd["flops"] / t_dom / 1e12,
                 "peak": peaks["bf16_tflops"] * tc_ratio, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(cfg.name, dom)
+    roof["traffic"] = ncu_traffic(cfg.name, dom, cfg.quant)
     roof["kernel"] = dom
     roof["algorithmic_bytes"] = wd["bytes"]
     roof["algorithmic_flops"] = wd["flops"]
