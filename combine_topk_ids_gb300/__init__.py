@@ -81,6 +81,8 @@ def lib():
         L.moe_quantize_weights_fp8.argtypes = [G] + [_P] * 7
         L.moe_prepare_weights_fp8.argtypes = [G] + [_P] * 5
         L.moe_expert_ffn_fp8.argtypes = [H] + [_P] * 6
+        L.moe_selftest_wait_expiry.argtypes = [_P, _P]
+        L.moe_selftest_wait_expiry.restype = ctypes.c_int
         L.moe_strerror.argtypes = [ctypes.c_int]
         L.moe_strerror.restype = ctypes.c_char_p
         for f in ("moe_workspace_size", "moe_expert_out_size", "moe_dispatch",
@@ -197,6 +199,12 @@ def moe_route_noalloc(g, topk_ids, counts, offsets, pick_pos, pick_src, slot, la
                                    _ptr(offsets), _ptr(pick_pos), _ptr(pick_src), _ptr(slot),
                                    _ptr(layout_range), _ptr(status), _stream(stream)),
            "moe_route_noalloc")
+
+
+def moe_selftest_wait_expiry(status, stream=None):
+    """Launch the bounded-wait expiry self-test (about 2 s on the device); status: int32
+    device tensor that receives MOE_STATUS_TIMEOUT."""
+    _check(lib().moe_selftest_wait_expiry(_ptr(status), _stream(stream)), "moe_selftest_wait_expiry")
 
 
 def moe_launches_per_layer(g) -> int:

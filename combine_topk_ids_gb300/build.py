@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libmoe.so")
-SOURCES = ["moe_api.cu", "routing.cu", "dispatch_combine.cu", "ffn_tc.cu", "ffn_fp8.cu", "noalloc.cu"]
+SOURCES = ["moe_api.cu", "routing.cu", "dispatch_combine.cu", "ffn_tc.cu", "ffn_fp8.cu", "noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -379,6 +379,18 @@ int moe_route_noalloc(const moe_geom *g, const void *topk_ids_dev, int ids_dtype
  */
 int moe_launches_per_layer(const moe_geom *g, int32_t *n);
 
+/*
+ * moe_selftest_wait_expiry - exercises the device-side failure path without faulting or
+ * hanging the GPU: one CTA waits on an mbarrier that nothing will complete, through the
+ * same bounded wait every tcgen05 GEMM kernel uses.  After the wait limit (2 s) the wait
+ * gives up, ORs MOE_STATUS_TIMEOUT into *status_dev (device int32) and the kernel returns;
+ * the context stays usable.  Stream-ordered and asynchronous.  The pages have no
+ * counterpart; it exists so that tests can check the expiry path on a real GPU.
+ * Errors: MOE_ERR_INVALID_ARGUMENT (NULL status), MOE_ERR_NOT_BUILT_FOR_DEVICE,
+ * MOE_ERR_CUDA.
+ */
+int moe_selftest_wait_expiry(int32_t *status_dev, void *stream);
+
 /* moe_strerror - static text for a moe_error code. */
 const char *moe_strerror(int err);
 

@@ -110,6 +110,7 @@ def test_calls_reject_an_unfilled_handle(lib):
     p = ctypes.c_void_p(1 << 20)
     assert lib.moe_expert_ffn(ctypes.byref(h), p, p, p, None) == -10
     assert lib.moe_expert_ffn_fp8(ctypes.byref(h), p, p, p, p, p, None) == -10
+    assert lib.moe_selftest_wait_expiry(None, None) == -1
     assert lib.moe_combine(ctypes.byref(h), p, p, p, None) == -10
     v = ctypes.c_int32()
     assert lib.moe_get_status(ctypes.byref(h), ctypes.byref(v), None) == -10
