@@ -167,7 +167,8 @@ TRAFFIC_SOURCES = {"bf16": ("combine_topk_ids_gb300/csrc/ffn_tc.cu",) + TRAFFIC_
 
 
 def src_hash(quant="bf16"):
-    from combine_topk_ids_gb300 import build as B
+    import importlib
+    B = importlib.import_module("combine_topk_ids_gb300.build")
     h = hashlib.sha256()
     for f in TRAFFIC_SOURCES[quant]:
         with open(os.path.join(ROOT, f), "rb") as fh:
