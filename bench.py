@@ -37,7 +37,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # tokens of the workload the CPU oracle evaluates per timed sample (bounded CPU work)
 ORACLE_SAMPLE_TOKENS = {"tiny_ll_em": 64, "mixtral_ll_em": 4, "dsv3_ll_rm": 4, "dsv3_ht_flat": 2,
                         "ragged_em": 16}
-ORACLE_SAMPLE_TOKENS.update({k + sfx: v for k, v in list(ORACLE_SAMPLE_TOKENS.items()) for sfx in ("_fp8", "_eo16")})
+ORACLE_SAMPLE_TOKENS.update({k + sfx: v for k, v in list(ORACLE_SAMPLE_TOKENS.items()) for sfx in ("_fp8", "_eo16", "_actpair")})
 
 
 def parse_args():
@@ -273,7 +273,7 @@ def workload_config(cfg, n):
             "algorithm": {"LL": "LOW_LATENCY", "HT": "HIGH_THROUGHPUT"}[cfg.algo],
             "tokens": cfg.tokens, "world": cfg.W, "max_tok_per_rank": cfg.Tr, "hidden": cfg.H,
             "experts": cfg.E, "top_k": cfg.k, "intermediate": cfg.I, "routing": cfg.routing,
-            "ids_dtype": cfg.ids_dtype, "quant": cfg.quant, "expert_out": cfg.expert_out,
+            "ids_dtype": cfg.ids_dtype, "quant": cfg.quant, "expert_out": cfg.expert_out, "act": cfg.act,
             "l2": "flushed (512 MiB write) before every timed step",
             "parallelism": "replicas x%d" % n if n > 1 else "single GPU"}
 
@@ -290,7 +290,7 @@ def run_ours(args, cfg, rank, world, dist):
     dev = torch.device("cuda", torch.cuda.current_device())
     case = make_case(cfg, dev)
     layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout, cfg.algo,
-                             quant=cfg.quant, expert_out=cfg.expert_out)
+                             quant=cfg.quant, expert_out=cfg.expert_out, act=cfg.act)
     layer.set_weights(case.w1, case.w2)
     layer.enable_timing(True)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)

@@ -19,6 +19,7 @@ LAYOUT = {"EM": 0, "RM": 1, "FLAT": 2}
 ALGO = {"LL": 0, "HT": 1}
 QUANT = {"bf16": 0, "fp8": 1}
 EXPERT_OUT = {"fp32": 0, "bf16": 1}
+ACT = {"bf16": 0, "pair": 1}
 IDS_INT32, IDS_INT64 = 0, 1
 STATUS_BAD_EXPERT_ID, STATUS_EM_OVERFLOW, STATUS_TIMEOUT, STATUS_INACTIVE_RANK = 0x1, 0x2, 0x4, 0x8
 
@@ -26,7 +27,7 @@ STATUS_BAD_EXPERT_ID, STATUS_EM_OVERFLOW, STATUS_TIMEOUT, STATUS_INACTIVE_RANK =
 class MoeGeom(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "world", "max_tok", "num_tokens", "hidden", "num_experts", "top_k", "intermediate",
-        "layout", "algorithm", "quant", "expert_out_dtype")]
+        "layout", "algorithm", "quant", "expert_out_dtype", "act_precision")]
 
 
 _P = ctypes.c_void_p
@@ -103,11 +104,13 @@ def _check(rc, where):
         raise MoeError(rc, where)
 
 
-def make_geom(W, Tr, T, H, E, k, I, layout="EM", algo="LL", quant="bf16", expert_out="fp32") -> MoeGeom:
+def make_geom(W, Tr, T, H, E, k, I, layout="EM", algo="LL", quant="bf16", expert_out="fp32",
+              act="bf16") -> MoeGeom:
     return MoeGeom(W, Tr, T, H, E, k, I, LAYOUT[layout] if isinstance(layout, str) else layout,
                    ALGO[algo] if isinstance(algo, str) else algo,
                    QUANT[quant] if isinstance(quant, str) else quant,
-                   EXPERT_OUT[expert_out] if isinstance(expert_out, str) else expert_out)
+                   EXPERT_OUT[expert_out] if isinstance(expert_out, str) else expert_out,
+                   ACT[act] if isinstance(act, str) else act)
 
 
 def _ptr(t):
@@ -237,14 +240,15 @@ class MoELayer1GPU:
     forward(x, topk_ids, topk_weights) = moe_dispatch -> moe_expert_ffn -> moe_combine,
     all on the current stream, no host synchronisation.  quant="fp8": FP8 dispatch and
     moe_expert_ffn_fp8 on weights quantised by set_weights.  expert_out="bf16": the expert
-    stage's output (and the RANK_MAJOR / FLAT per-pick rows) in bf16.
+    stage's output (and the RANK_MAJOR / FLAT per-pick rows) in bf16.  act="pair": the SwiGLU
+    activation as a bf16 (hi, lo) pair instead of one bf16 value.
     """
 
     def __init__(self, W, Tr, T, H, E, k, I, layout="EM", algo="LL", device="cuda", quant="bf16",
-                 expert_out="fp32"):
+                 expert_out="fp32", act="bf16"):
         import torch
         self.quant = quant
-        self.geom = make_geom(W, Tr, T, H, E, k, I, layout, algo, quant, expert_out)
+        self.geom = make_geom(W, Tr, T, H, E, k, I, layout, algo, quant, expert_out, act)
         self.device = torch.device(device)
         self.workspace = torch.empty(moe_workspace_size(self.geom), dtype=torch.uint8, device=self.device)
         eo_t = torch.bfloat16 if expert_out == "bf16" else torch.float32

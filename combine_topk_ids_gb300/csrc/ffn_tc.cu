@@ -5,11 +5,10 @@
 // for every expert e and each of its n_e rows x,
 //     GEMM1   h   = x W1[e]^T            [n_e, 2I], fp32 accumulate in tensor memory
 //     SwiGLU  act = silu(h[:, :I]) * h[:, I:]   fp32 (fused into GEMM1's epilogue), stored
-//                   as a pair of bf16 arrays act_hi = bf16(act), act_lo = bf16(act - act_hi)
-//     GEMM2   y   = act_hi W2[e]^T + act_lo W2[e]^T   [n_e, H], one fp32 accumulator
-// The pair carries act to about 16 significant bits, so GEMM2 sees the fp32 activation
-// rather than a bf16 re-quantisation of it.  (A single bf16 act is a rounding decision
-// taken on tensor-core-accumulated values; its flips move y by up to |W2| * ulp(act).)
+//                   as bf16 (round to nearest even), or with MOE_ACT_BF16_PAIR as a pair of
+//                   bf16 arrays act_hi = bf16(act), act_lo = bf16(act - act_hi)
+//     GEMM2   y   = act W2[e]^T, or act_hi W2[e]^T + act_lo W2[e]^T   [n_e, H], fp32
+// The pair carries act to about 16 significant bits (GEMM2 then runs two MMAs per k-step).
 //
 // One persistent kernel per GEMM, one CTA per SM, 256 threads:
 //   warp 0      TMA producer: 128x64 A tile(s) + 256x64 B tile per stage (SWIZZLE_128B),
@@ -72,7 +71,7 @@ struct FfnArgs {
     int mode;      // 0: SwiGLU epilogue -> act as a bf16 (hi, lo) pair; 1: fp32 store
     int out_bf16;  // mode 1: store the rows as bf16 (round to nearest even) instead
     void *out;     // mode 0: act_hi; mode 1: fp32 rows
-    void *out2;    // mode 0: act_lo
+    void *out2;    // mode 0: act_lo (NULL: single bf16 activation)
     int64_t out_ld;   // elements per output row
     int out_mode;  // 0: row = e*out_cap + m; 1: row = offsets[e] + m
     int64_t out_cap;
@@ -323,7 +322,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // columns [0,128) gate, [128,256) up of act columns nbk*128 .. +128
                 const int64_t o0 = orow * a.out_ld + (int64_t)nbk * (BN / 2);
                 __nv_bfloat16 *out_hi = reinterpret_cast<__nv_bfloat16 *>(a.out) + o0;
-                __nv_bfloat16 *out_lo = reinterpret_cast<__nv_bfloat16 *>(a.out2) + o0;
+                __nv_bfloat16 *out_lo = a.out2 ? reinterpret_cast<__nv_bfloat16 *>(a.out2) + o0 : nullptr;
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
                     uint32_t g[32], u[32];
@@ -332,7 +331,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_wait_ld();
                     if (row < valid) {
                         uint4 *oh = reinterpret_cast<uint4 *>(out_hi + c);
-                        uint4 *ol = reinterpret_cast<uint4 *>(out_lo + c);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint32_t wh[4], wl[4];
@@ -348,7 +346,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 wl[h] = *reinterpret_cast<uint32_t *>(&lo);
                             }
                             oh[v] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-                            ol[v] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                            if (a.out2) reinterpret_cast<uint4 *>(out_lo + c)[v] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                         }
                     }
                 }
@@ -518,7 +516,8 @@ int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s) {
     FfnArgs g = base_args(r, pair);
     g.bn = BN; g.nb = (int)(2 * p.I / BN); g.kb = (int)(p.H / BK);
     g.a_mode = em ? 0 : 1; g.a_cap = p.cap; g.b_rows = 2 * p.I;
-    g.mode = 0; g.out = r.act; g.out2 = r.act_lo; g.out_ld = p.I; g.out_mode = 1; g.out_cap = 0;
+    g.mode = 0; g.out = r.act; g.out2 = p.act_pair ? r.act_lo : nullptr; g.out_ld = p.I; g.out_mode = 1;
+    g.out_cap = 0;
     if (pair) return launch_gemm<false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
     return launch_gemm<false, false>(mA, mA, mB, g, max_mblocks(p, BM) * g.nb, s);
 }
@@ -530,7 +529,8 @@ int launch_gemm2(const Routing &r, const uint16_t *w2, void *expert_out, cudaStr
     const bool pair = use_pair(p, p.I, p.H);
     const int bn = (p.H % 256 == 0) ? 256 : 128;
     CUtensorMap mA, mA2, mB;
-    if (!make_map(&mA, r.act, p.P, p.I, BM) || !make_map(&mA2, r.act_lo, p.P, p.I, BM) ||
+    if (!make_map(&mA, r.act, p.P, p.I, BM) ||
+        (p.act_pair && !make_map(&mA2, r.act_lo, p.P, p.I, BM)) ||
         !make_map(&mB, w2, p.E * p.H, p.I, pair ? bn / 2 : bn))
         return MOE_ERR_CUDA;
     FfnArgs g = base_args(r, pair);
@@ -538,8 +538,12 @@ int launch_gemm2(const Routing &r, const uint16_t *w2, void *expert_out, cudaStr
     g.a_mode = 1; g.a_cap = 0; g.b_rows = p.H; g.mode = 1; g.out_ld = p.H; g.out_bf16 = p.eo_bf16;
     if (em) { g.out = expert_out; g.out_mode = 0; g.out_cap = p.cap; }
     else { g.out = r.ypick; g.out_mode = 1; g.out_cap = 0; }
-    if (pair) return launch_gemm<true, true>(mA, mA2, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
-    return launch_gemm<true, false>(mA, mA2, mB, g, max_mblocks(p, BM) * g.nb, s);
+    if (p.act_pair) {
+        if (pair) return launch_gemm<true, true>(mA, mA2, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
+        return launch_gemm<true, false>(mA, mA2, mB, g, max_mblocks(p, BM) * g.nb, s);
+    }
+    if (pair) return launch_gemm<false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
+    return launch_gemm<false, false>(mA, mA, mB, g, max_mblocks(p, BM) * g.nb, s);
 }
 
 }  // namespace moe

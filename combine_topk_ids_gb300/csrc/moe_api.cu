@@ -52,7 +52,8 @@ int make_plan(const moe_geom &g, Plan *p) {
         g.intermediate < 1)
         return MOE_ERR_INVALID_ARGUMENT;
     if (g.layout < 0 || g.layout > 2 || g.algorithm < 0 || g.algorithm > 1 || g.quant < 0 ||
-        g.quant > 1 || g.expert_out_dtype < 0 || g.expert_out_dtype > 1)
+        g.quant > 1 || g.expert_out_dtype < 0 || g.expert_out_dtype > 1 || g.act_precision < 0 ||
+        g.act_precision > 1)
         return MOE_ERR_INVALID_ARGUMENT;
     if (g.top_k < 1 || g.top_k > MOE_MAX_TOPK) return MOE_ERR_TOPK;
     if (g.num_experts % g.world != 0) return MOE_ERR_EXPERTS_NOT_DIVISIBLE;
@@ -73,6 +74,7 @@ int make_plan(const moe_geom &g, Plan *p) {
     q.k = g.top_k; q.H = g.hidden; q.I = g.intermediate; q.P = P; q.layout = g.layout;
     q.quant = g.quant;
     q.eo_bf16 = g.expert_out_dtype == MOE_EXPERT_OUT_BFLOAT16;
+    q.act_pair = g.quant == MOE_QUANT_NONE && g.act_precision == MOE_ACT_BF16_PAIR;
     // routing chunk: about 256 chunks over the whole capacity, 32..1024 tokens each
     int64_t want = (cap + 255) / 256;
     int tb = 32;
@@ -114,7 +116,7 @@ int make_plan(const moe_geom &g, Plan *p) {
     q.recv_x = take(eb * q.nrecv * H);
     q.recv_scales = take(f8 ? 4 * q.nrecv * (H / 128) : 0);
     q.act = take(eb * P * I);
-    q.act_lo = take(f8 ? 0 : 2 * P * I);
+    q.act_lo = take(q.act_pair ? 2 * P * I : 0);
     q.act_scales = take(f8 ? 4 * P * (I / 128) : 0);
     q.apick = take(em ? 0 : eb * P * H);
     q.apick_scales = take(em || !f8 ? 0 : 4 * P * (H / 128));
@@ -138,7 +140,7 @@ Routing carve(const Plan &p, void *ws) {
     r.recv_topk_w = reinterpret_cast<float *>(b + p.recv_topk_w);
     r.recv_x = reinterpret_cast<uint16_t *>(b + p.recv_x);
     r.act = reinterpret_cast<uint16_t *>(b + p.act);
-    r.act_lo = reinterpret_cast<uint16_t *>(b + p.act_lo);
+    r.act_lo = p.act_pair ? reinterpret_cast<uint16_t *>(b + p.act_lo) : nullptr;
     r.apick = reinterpret_cast<uint16_t *>(b + p.apick);
     r.ypick = b + p.ypick;
     const bool f8 = p.quant == MOE_QUANT_FP8_E4M3;

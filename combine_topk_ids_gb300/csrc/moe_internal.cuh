@@ -21,6 +21,7 @@ struct Plan {
     int layout;
     int quant;      // moe_quant
     int eo_bf16;    // expert_out (and the RM/FLAT per-pick rows) in bf16
+    int act_pair;   // bf16 geometry: SwiGLU activation as a bf16 (hi, lo) pair
     int64_t nrecv;  // rows of the receive buffer: E*cap (EM) or W*cap (RM/FLAT)
     int tb;         // tokens per routing block
     int nbpr;       // routing blocks per logical rank
@@ -41,7 +42,7 @@ struct Routing {
         *blk_hist, *blk_base, *recv_row, *recv_count, *num_recv, *recv_src, *recv_topk_idx,
         *blk_dhist, *blk_dbase;
     float *recv_topk_w;
-    uint16_t *recv_x, *act, *act_lo, *apick;   // act / act_lo: SwiGLU output as a bf16 pair
+    uint16_t *recv_x, *act, *act_lo, *apick;   // act (and act_lo for the pair): SwiGLU output
     void *ypick;    // RM/FLAT per-pick GEMM2 rows: float32, or bf16 with eo_bf16
     // FP8 geometry: recv_x / act / apick hold e4m3 codes (one byte per element); their
     // scales are column-block major ([cols/128][rows]); act_lo is unused

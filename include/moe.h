@@ -85,6 +85,16 @@ typedef enum { MOE_QUANT_NONE = 0, MOE_QUANT_FP8_E4M3 = 1 } moe_quant;
  */
 typedef enum { MOE_EXPERT_OUT_FLOAT32 = 0, MOE_EXPERT_OUT_BFLOAT16 = 1 } moe_expert_out_dtype;
 
+/*
+ * The SwiGLU activation as the second GEMM's operand (bf16 geometries; FP8 geometries
+ * quantise it to e4m3 instead) [FI-4: the expert GEMMs take bf16 operands].
+ *   MOE_ACT_BF16       act = bf16_rne(silu(g) * u), one bf16 x bf16 GEMM (default).
+ *   MOE_ACT_BF16_PAIR  act carried as act_hi = bf16(act) plus act_lo = bf16(act - act_hi)
+ *                      (about 16 significant bits): GEMM2 runs both halves, twice the
+ *                      tensor work, for outputs that track an unrounded activation.
+ */
+typedef enum { MOE_ACT_BF16 = 0, MOE_ACT_BF16_PAIR = 1 } moe_act_precision;
+
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARGUMENT = -1,      /* null pointer, non-positive size, bad enum          */
@@ -141,6 +151,7 @@ typedef struct {
     int32_t algorithm;    /* moe_algorithm                                                 */
     int32_t quant;        /* moe_quant: precision of the received rows and expert GEMMs    */
     int32_t expert_out_dtype; /* moe_expert_out_dtype                                      */
+    int32_t act_precision;    /* moe_act_precision                                         */
 } moe_geom;
 
 /*
@@ -182,8 +193,9 @@ typedef struct {
     int32_t *status;           /* device status word (MOE_STATUS_* bits)                 */
     void *ffn_act;             /* written by the FFN: the SwiGLU activation, [R, I] in
                                   pick-list order (row offsets[e] + position), the second
-                                  GEMM's operand.  bf16: the high half of the bf16 pair;
-                                  FP8: e4m3 codes                                        */
+                                  GEMM's operand.  bf16: the bf16 activation (with
+                                  MOE_ACT_BF16_PAIR, the high half of the pair); FP8:
+                                  e4m3 codes                                             */
     float *ffn_act_scales;     /* FP8 only (else NULL): scales of ffn_act, column-block
                                   major [I/128][T*k] (row p, block b at b*T*k + p)        */
     void *workspace;           /* base of the workspace the handle lives in              */
@@ -254,7 +266,8 @@ int moe_prepare_weights(const moe_geom *g, const void *w1_dev, void *w1_prepared
 /*
  * moe_expert_ffn - per-expert grouped SwiGLU FFN on the received rows [FI-2; FI-3]:
  * for each expert e and each of its rows x: h = x W1[e]^T (fp32 accumulate),
- * act = bf16(silu(h[:I]) * h[I:]), y = act W2[e]^T (fp32).
+ * act = bf16(silu(h[:I]) * h[I:]) (or the bf16 pair of MOE_ACT_BF16_PAIR),
+ * y = act W2[e]^T (fp32).
  *   EM:      expert_out[e*cap + r] = y of row r (top_k = 1 per dispatched row)
  *   RM/FLAT: expert_out[d*cap + r] = sum over the row's LOCAL picks j (ascending) of
  *            recv_topk_weights[d][r][j] * y_j; non-local picks are masked to weight 0

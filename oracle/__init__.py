@@ -5,8 +5,9 @@ CPU-baseline leg (bench.py --impl reference / cpu_baseline) may import this pack
 The product library never calls it and shares no code with it.
 
 Plain and slow on purpose: routing is the literal (t, j)-ordered loop in moe_oracle.c;
-the FFN and combine are numpy in float64, one expert at a time; the only rounding is the
-final output's to bf16.
+the FFN and combine are numpy in float64, one expert at a time; the only roundings are
+the SwiGLU activation's and the final output's to bf16 (plus expert_out's with the bf16
+expert_out option).
 
 Sources (page title, section):
   * FlashInfer "MoE-EP implementation & usage", section 2 "Call stack": dispatch ->
@@ -24,16 +25,19 @@ Readings where the pages are silent (each listed in the design notes):
     the GPU rounds them (each pick's y; for RANK_MAJOR / FLAT also the per-row sum);
   * gate = rows [0, I) of w1[e], up = rows [I, 2I); SwiGLU act = silu(gate) * up with
     silu(g) = g / (1 + exp(-g))  (parity unpinned by the pages: a fixed convention);
-  * the expert FFN is evaluated in full precision from the bf16 weights and inputs: no
-    re-quantisation of the SwiGLU activation or of expert_out (float64 here); the final
-    combined output is rounded to bf16 (round-to-nearest-even);
+  * the expert FFN is evaluated in full precision (float64) from the bf16 weights and
+    inputs; the SwiGLU activation, the operand of the second bf16 GEMM, is rounded to bf16
+    (round to nearest even) unless geom["act"] == "pair" (the library's bf16-pair option,
+    which tracks the unrounded activation); expert_out is not rounded (float64 here); the
+    final combined output is rounded to bf16 (round-to-nearest-even);
   * RANK_MAJOR / FLAT apply topk_weights in the FFN stage's reduction over the local
     picks of a received row (ascending j), and combine sums over destinations without
     weights (ascending d).
 
 Functions whose values the pages never print ("parity unpinned" by the pages; pinned in
 tests by brute force, closed forms, a library special case and exact invariants):
-route, pick_outputs, ffn_ranks, combine_em, combine_ranks, layer.
+route, pick_outputs, ffn_ranks, combine_em, combine_ranks, layer (swiglu_act_band and bf16_act_allowance
+are the tolerance helpers of the default bf16 activation).
 """
 import ctypes
 import os
@@ -159,15 +163,72 @@ def dispatch_rows(geom, rt):
     return d_idx.astype(np.int64) * cap + rr[t_idx, d_idx], t_idx
 
 
-def swiglu_expert(xrows, w1e, w2e):
-    """One expert's FFN on the rows xrows [n, H] (float64 values of bf16 inputs):
-    h = x W1e^T, act = silu(h[:, :I]) * h[:, I:], y = act W2e^T, all float64."""
-    I = w2e.shape[1]
+def swiglu_act(xrows, w1e):
+    """SwiGLU activation of the rows xrows [n, H] (float64 values of bf16 inputs):
+    h = x W1e^T, act = silu(h[:, :I]) * h[:, I:], float64, unrounded."""
+    I = w1e.shape[0] // 2
     h = xrows @ w1e.T
     g, u = h[:, :I], h[:, I:]
     with np.errstate(over="ignore"):
-        act = g / (1.0 + np.exp(-g)) * u
-    return act @ w2e.T
+        return g / (1.0 + np.exp(-g)) * u
+
+
+def swiglu_act_band(xrows, w1e, rel=2.0 ** -14):
+    """Half-width (absolute, in activation units) of the band around each exact activation
+    inside which a GPU that accumulates h = x W1e^T in float32 on tensor cores may land:
+    h moves by at most rel * sum_k |x_k w_k|, act = silu(g) * u by 1.1 |u| dg + |silu(g)| du
+    (|silu'| <= 1.1) plus 2**-18 |act| for the float32 evaluation of silu and the product.
+    A bf16 activation code of the GPU is then a correct result if it is the rounding of some
+    value inside [act - band, act + band]."""
+    I = w1e.shape[0] // 2
+    h = xrows @ w1e.T
+    habs = np.abs(xrows) @ np.abs(w1e).T
+    g, u = h[:, :I], h[:, I:]
+    with np.errstate(over="ignore"):
+        silu = g / (1.0 + np.exp(-g))
+    act = silu * u
+    return act, 1.1 * np.abs(u) * rel * habs[:, :I] + np.abs(silu) * rel * habs[:, I:] + 2.0 ** -18 * np.abs(act)
+
+
+def bf16_act_allowance(geom, rt, x_bits, w1, w2, picks, gpu_act):
+    """For the default bf16 activation: which of a GPU's activation codes are correct
+    results, and what their differences from the oracle's codes may do to y.
+
+    gpu_act: float64 [len(picks), I], the GPU's bf16 activation of each pick.  A code is
+    correct if it is the bf16 rounding of some value within swiglu_act_band of the exact
+    activation.  Returns (allowance {pick: [H]} = sum over columns c whose GPU code differs
+    from round_bf16(act) of |W2[:, c]| * |difference|, number of incorrect codes, number of
+    differing codes)."""
+    k = geom["k"]
+    ids = rt["ids"].reshape(-1)
+    row_of = {int(i): n for n, i in enumerate(picks)}
+    by_e = {}
+    for i in picks:
+        by_e.setdefault(int(ids[i]), []).append(int(i))
+    out, n_bad, n_flip = {}, 0, 0
+    for e, lst in sorted(by_e.items()):
+        w1e, w2e = _expert_weights(w1, w2, e)
+        act, band = swiglu_act_band(bf16_bits_to_f64(x_bits[np.array(lst) // k]), w1e)
+        ref = round_bf16(act)
+        lo, hi = round_bf16(act - band), round_bf16(act + band)
+        v = np.asarray(gpu_act, dtype=np.float64)[[row_of[i] for i in lst]]
+        n_bad += int((~((v >= np.minimum(lo, hi)) & (v <= np.maximum(lo, hi)))).sum())
+        dv = np.abs(v - ref)
+        n_flip += int((dv != 0).sum())
+        allow = dv @ np.abs(w2e).T
+        for n, i in enumerate(lst):
+            out[i] = allow[n]
+    return out, n_bad, n_flip
+
+
+def swiglu_expert(xrows, w1e, w2e, act_bf16=False, return_act=False):
+    """One expert's FFN on the rows xrows [n, H]: y = act W2e^T in float64, act from
+    swiglu_act; act_bf16: the activation is the second GEMM's bf16 operand, rounded to
+    nearest even first (the library's default activation precision).  return_act: also
+    return the unrounded activation."""
+    act = swiglu_act(xrows, w1e)
+    y = (round_bf16(act) if act_bf16 else act) @ w2e.T
+    return (y, act) if return_act else y
 
 
 def _expert_weights(w1, w2, e):
@@ -178,14 +239,18 @@ def _expert_weights(w1, w2, e):
     return bf16_bits_to_f64(a), bf16_bits_to_f64(b)
 
 
-def pick_outputs(geom, rt, x_bits, w1, w2, picks=None, expert_fn=None):
+def pick_outputs(geom, rt, x_bits, w1, w2, picks=None, expert_fn=None, acts=None):
     """Expert output y(t, j) = FFN_e(x[t]) of each valid pick, e = topk_ids[t, j].
 
     This is EXPERT_MAJOR's expert stage (top_k = 1 per dispatched row) and the per-pick
     term of the RANK_MAJOR / FLAT stage.  Returns {pick index t*k+j: float64 [H]} for
     `picks` (default: all valid picks).  expert_fn(e, xrows) replaces the SwiGLU expert
-    (the identity-expert pin uses it).
+    (the identity-expert pin uses it).  The activation is rounded to bf16 unless
+    geom["act"] == "pair" (reading: the expert GEMMs take bf16 operands, FlashInfer
+    "MoE-EP implementation & usage" section 4 step 3, so the second one's is rounded).
+    acts: optional dict that receives each pick's unrounded activation (float64 [I]).
     """
+    act_bf16 = geom.get("act", "bf16") == "bf16"
     k = geom["k"]
     pp = rt["pick_pos"].reshape(-1)
     ids = rt["ids"].reshape(-1)
@@ -201,7 +266,10 @@ def pick_outputs(geom, rt, x_bits, w1, w2, picks=None, expert_fn=None):
             y = expert_fn(e, xr)
         else:
             a, b = _expert_weights(w1, w2, e)
-            y = swiglu_expert(xr, a, b)
+            y, act = swiglu_expert(xr, a, b, act_bf16=act_bf16, return_act=True)
+            if acts is not None and act is not None:
+                for n, i in enumerate(lst):
+                    acts[i] = act[n]
         for n, i in enumerate(lst):
             out[i] = y[n]
     return out
@@ -283,4 +351,4 @@ def layer(geom, x_bits, ids, topk_w, w1, w2, tokens=None, expert_fn=None, active
 def geom_of(cfg):
     """Geometry dict of a gen.configs.MoeConfig."""
     return dict(W=cfg.W, Tr=cfg.Tr, T=cfg.tokens, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I,
-                layout=cfg.layout)
+                layout=cfg.layout, act=getattr(cfg, "act", "bf16"))

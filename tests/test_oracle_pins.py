@@ -226,15 +226,21 @@ def _f64(bits):
     return torch.from_numpy(oracle.bf16_bits_to_f64(bits))
 
 
-def test_swiglu_expert_vs_torch_dense_mlp():
-    """E=1, k=1, w=1: the layer is a dense SwiGLU MLP (library special case)."""
-    c = gen.MoeConfig("d", W=1, Tr=40, H=128, E=1, k=1, I=96, layout="EM", algo="LL", routing="uniform")
+@pytest.mark.parametrize("act_mode", ["bf16", "pair"])
+def test_swiglu_expert_vs_torch_dense_mlp(act_mode):
+    """E=1, k=1, w=1: the layer is a dense SwiGLU MLP (library special case).  With the
+    default activation precision the activation is rounded to bf16 (round_bf16, pinned
+    against torch below) before the second matmul; the pair tracks the unrounded value."""
+    c = gen.MoeConfig("d", W=1, Tr=40, H=128, E=1, k=1, I=96, layout="EM", algo="LL", routing="uniform",
+                      act=act_mode)
     x, ids, w, w1, w2 = _inputs(c)
     w = np.ones_like(w)
     _, out = oracle.layer(oracle.geom_of(c), x, ids, w, w1, w2)
     X, W1, W2 = _f64(x), _f64(w1[0]), _f64(w2[0])
     gate, up = X @ W1[:96].T, X @ W1[96:].T
     act = torch.nn.functional.silu(gate) * up
+    if act_mode == "bf16":
+        act = torch.from_numpy(oracle.round_bf16(act.numpy()))
     y = (act @ W2.T).numpy()
     # the oracle rounds once to bf16; torch's float64 value rounded the same way, up to the
     # last-bit differences of two float64 evaluations (ties land within 1e-12 relative)
@@ -242,7 +248,8 @@ def test_swiglu_expert_vs_torch_dense_mlp():
 
 
 def _dense_moe_torch(c, x, ids, w, w1, w2):
-    """Textbook dense MoE: out = sum_e G[:, e] * FFN_e(X) with G[t, e] = sum_j w[t,j][ids[t,j]==e]."""
+    """Textbook dense MoE: out = sum_e G[:, e] * FFN_e(X) with G[t, e] = sum_j w[t,j][ids[t,j]==e]
+    (the activation held in bf16 unless c.act == "pair")."""
     X = _f64(x)
     G = torch.zeros(c.tokens, c.E, dtype=torch.float64)
     for j in range(c.k):
@@ -252,14 +259,17 @@ def _dense_moe_torch(c, x, ids, w, w1, w2):
     for e in range(c.E):
         W1, W2 = _f64(w1[e]), _f64(w2[e])
         act = torch.nn.functional.silu(X @ W1[:c.I].T) * (X @ W1[c.I:].T)
+        if c.act == "bf16":
+            act = torch.from_numpy(oracle.round_bf16(act.numpy()))
         out += G[:, e:e + 1] * (act @ W2.T)
     return out.numpy()
 
 
 @pytest.mark.parametrize("layout", ["EM", "RM", "FLAT"])
 @pytest.mark.parametrize("mask", [0.0, 0.25])
-def test_layer_vs_dense_moe(layout, mask):
-    c = _tiny_cfg(layout, mask_frac=mask)
+@pytest.mark.parametrize("act_mode", ["bf16", "pair"])
+def test_layer_vs_dense_moe(layout, mask, act_mode):
+    c = _tiny_cfg(layout, mask_frac=mask, act=act_mode)
     x, ids, w, w1, w2 = _inputs(c)
     _, out = oracle.layer(oracle.geom_of(c), x, ids, w, w1, w2)
     ref = _dense_moe_torch(c, x, ids, w, w1, w2)
@@ -326,8 +336,9 @@ def test_layouts_agree():
 
 
 # ------------------------------------------------------------- planted mistakes fail
-def test_planted_mistakes_are_caught(monkeypatch):
-    c = _tiny_cfg("RM")
+@pytest.mark.parametrize("act_mode", ["pair", "bf16"])
+def test_planted_mistakes_are_caught(monkeypatch, act_mode):
+    c = _tiny_cfg("RM", act=act_mode)
     x, ids, w, w1, w2 = _inputs(c)
     ref = _dense_moe_torch(c, x, ids, w, w1, w2)
     good = oracle.swiglu_expert
@@ -336,19 +347,24 @@ def test_planted_mistakes_are_caught(monkeypatch):
         _, out = oracle.layer(oracle.geom_of(c), x, ids, w, w1, w2)
         return np.allclose(out, ref, rtol=2 ** -8 + 1e-9, atol=1e-12)
 
+    def mutant(fn):   # an expert with the oracle's signature, computing fn(xr, W1e, W2e)
+        return lambda xr, a, b, act_bf16=False, return_act=False: (fn(xr, a, b), None) if return_act else fn(xr, a, b)
+
     assert check()
     I = c.I
+    rnd = oracle.round_bf16 if act_mode == "bf16" else (lambda v: v)
     mutants = {
-        "gate/up swapped": lambda xr, a, b: good(xr, np.concatenate([a[I:], a[:I]]), b),
-        "W2 transposed use": lambda xr, a, b: (lambda h: (
+        "gate/up swapped": lambda xr, a, b: good(xr, np.concatenate([a[I:], a[:I]]), b, act_mode == "bf16"),
+        "W2 transposed use": lambda xr, a, b: (lambda h: rnd(
             h[:, :I] / (1 + np.exp(-h[:, :I])) * h[:, I:]) @ b.reshape(b.shape[1], b.shape[0]))(xr @ a.T),
-        "silu sign": lambda xr, a, b: (lambda h: (
+        "silu sign": lambda xr, a, b: (lambda h: rnd(
             h[:, :I] / (1 + np.exp(h[:, :I])) * h[:, I:]) @ b.T)(xr @ a.T),
-        "act rounded to bf16": lambda xr, a, b: (lambda h: oracle.round_bf16(
+        # the activation's precision swapped: rounded when it must not be, or the reverse
+        "act precision": lambda xr, a, b: (lambda h: (oracle.round_bf16 if act_mode == "pair" else (lambda v: v))(
             h[:, :I] / (1 + np.exp(-h[:, :I])) * h[:, I:]) @ b.T)(xr @ a.T),
     }
     for name, fn in mutants.items():
-        monkeypatch.setattr(oracle, "swiglu_expert", fn)
+        monkeypatch.setattr(oracle, "swiglu_expert", mutant(fn))
         assert not check(), name
     monkeypatch.setattr(oracle, "swiglu_expert", good)
     # a dropped term in the per-destination reduction
@@ -414,3 +430,56 @@ def test_bf16_expert_out_within_rounding_bound(layout):
     bound += 2 * half_ulp(a) + (2 * half_ulp(np.abs(a) + bound) if layout != "EM" else 0)
     assert np.all(np.abs(a - b) <= bound + 1e-30)
     assert np.any(a != b)
+
+
+def test_bf16_act_allowance_checker():
+    """The checker the GPU tests use for the default bf16 activation: the oracle's own codes
+    are all accepted with zero allowance; a code moved one bf16 ulp where the band does not
+    reach the next code is rejected; a code moved where it does is accepted and its effect
+    through W2 is |W2[:, c]| * ulp, worked out by hand here."""
+    c = _tiny_cfg("EM", act="bf16")
+    x, ids, w, w1, w2 = _inputs(c)
+    g = oracle.geom_of(c)
+    rt = oracle.route(g, ids, w)
+    picks = [i for i in range(c.tokens * c.k) if rt["pick_pos"].reshape(-1)[i] >= 0]
+    flat = ids.reshape(-1)
+    acts = []
+    bands = []
+    for i in picks:
+        w1e = oracle.bf16_bits_to_f64(w1[flat[i]])
+        a, b = oracle.swiglu_act_band(oracle.bf16_bits_to_f64(x[i // c.k])[None, :], w1e)
+        acts.append(a[0])
+        bands.append(b[0])
+    acts, bands = np.array(acts), np.array(bands)
+    codes = oracle.round_bf16(acts)
+    allow, n_bad, n_flip = oracle.bf16_act_allowance(g, rt, x, w1, w2, picks, codes)
+    assert (n_bad, n_flip) == (0, 0) and all(np.all(allow[i] == 0) for i in picks)
+    ulp = np.where(codes != 0, np.ldexp(1.0, np.frexp(np.abs(codes))[1] - 8), 2.0 ** -133)
+    # one code whose band is far from the next code up, pushed there: rejected
+    far = np.argwhere((codes + ulp - acts) > 4 * bands + ulp / 2)
+    n, col = far[0]
+    bad = codes.copy()
+    bad[n, col] += ulp[n, col]
+    assert oracle.bf16_act_allowance(g, rt, x, w1, w2, picks, bad)[1] == 1
+    # one code whose exact value sits on a rounding midpoint (planted by widening its band):
+    # accepted, and the allowance of that pick is |W2[:, col]| * ulp
+    wide = codes.copy()
+    near = np.argwhere(np.abs(acts) > 0.05)[0]
+    n, col = near
+    e = int(flat[picks[n]])
+    mid = acts[n, col]
+    nxt = oracle.round_bf16(np.array(mid + np.sign(mid) * ulp[n, col]))
+    wide[n, col] = nxt
+    orig = oracle.swiglu_act_band
+
+    def band_plus(xr, w1e, rel=2.0 ** -14):
+        a, b = orig(xr, w1e, rel)
+        return a, b + ulp[n, col]
+    try:
+        oracle.swiglu_act_band = band_plus
+        allow, n_bad, n_flip = oracle.bf16_act_allowance(g, rt, x, w1, w2, picks, wide)
+    finally:
+        oracle.swiglu_act_band = orig
+    assert (n_bad, n_flip) == (0, 1)
+    w2e = oracle.bf16_bits_to_f64(w2[e])
+    np.testing.assert_array_equal(allow[picks[n]], np.abs(w2e[:, col]) * abs(nxt - codes[n, col]))

@@ -33,6 +33,10 @@ SMALL_CASES = {
     "blocks_em": gen.SMALL["blocks_em"],
     "blocks_rm": gen.SMALL["blocks_rm"],
     "blocks_flat": gen.SMALL["blocks_flat"],
+    # the bf16-pair activation (hi + lo operand of the second GEMM)
+    "actpair_em": gen.SMALL["small_em"].with_(act="pair", seed=13),
+    "actpair_rm_h384": gen.SMALL["small_rm"].with_(act="pair", H=384, seed=14),
+    "actpair_twosm_flat": gen.SMALL["pair_flat"].with_(act="pair", seed=15),
 }
 
 
