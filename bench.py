@@ -173,7 +173,9 @@ def src_hash(quant="bf16"):
     for f in TRAFFIC_SOURCES[quant]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
-    h.update(repr(B._flags()).encode())
+    # the include path is absolute; hash it relative to the checkout so the key is the
+    # same wherever the repository is copied
+    h.update(repr([f.replace(B.ROOT, ".") for f in B._flags()]).encode())
     return h.hexdigest()[:16]
 
 
