@@ -17,8 +17,10 @@
 //               N=256, K=16, bf16 x bf16 -> fp32 into one of two 256-column TMEM
 //               accumulators, tcgen05.commit frees smem stages and hands tiles over
 //   warp 2      TMEM allocator (512 columns)
-//   warps 4-7   epilogue: tcgen05.ld 32x32b rows -> registers -> SwiGLU / fp32 store,
-//               overlapped with the next tile's mainloop (double-buffered accumulator)
+//   warps 4-7   epilogue: tcgen05.ld 32x32b rows -> registers -> SwiGLU / fp32 or bf16
+//               -> a 4 KB shared-memory buffer per warp -> whole 128-byte row segments
+//               in global memory, overlapped with the next tile's mainloop
+//               (double-buffered accumulator)
 // Tiles: per expert ceil(n_e/128) m-blocks x (N/256) n-blocks, enumerated expert by expert,
 // n-block-major with the m-blocks of one weight tile adjacent (they run on neighbouring
 // SMs at the same time and share the weight tile through L2).  Experts with no rows issue
@@ -37,6 +39,7 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int THREADS = 256;
 constexpr int TMEM_COLS = 2 * BN;               // two fp32 accumulators of 128 x 256
+constexpr int kStageRowsBytes = 32 * 128;       // one epilogue warp's 32 rows x 128 B
 
 // Pipeline shape.  HILO: the A operand is a bf16 pair (two A tiles per stage).  PAIR: a
 // cluster of two CTAs on two SMs computes a 256-row tile with tcgen05.mma.cta_group::2;
@@ -46,7 +49,8 @@ template <bool HILO, bool PAIR> struct Pipe {
     static constexpr int kBBytes = PAIR ? B_BYTES / 2 : B_BYTES;
     static constexpr int kStageBytes = kATiles * A_BYTES + kBBytes;     // 32..64 KB
     static constexpr int kStages = (192 * 1024) / kStageBytes;          // 3..6
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int kSmemBytes =
+        kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/ + 4 * kStageRowsBytes /*epilogue*/;
     static constexpr int kMRows = PAIR ? 2 * BM : BM;                   // rows of one tile
 };
 
@@ -144,6 +148,39 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
+}
+
+// Store 32 rows x 128 bytes held one row per lane (w = lane's row) to global rows
+// gbase + r * row_bytes, r < nvalid, as full 128-byte segments: the rows pass through this
+// warp's 4 KB shared-memory buffer (16-byte chunk q of row r at chunk q ^ (r & 7), so that
+// neither the row-per-lane writes nor the segment-per-8-lanes reads conflict on banks),
+// then each store instruction writes four whole rows' 128-byte segments.
+__device__ __forceinline__ void warp_store_rows(uint32_t stg, const uint32_t (&w)[32], char *gbase,
+                                                int64_t row_bytes, int nvalid, int lane) {
+    const uint32_t mine = stg + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(mine + (uint32_t)((q ^ (lane & 7)) << 4)),
+                     "r"(w[4 * q]), "r"(w[4 * q + 1]), "r"(w[4 * q + 2]), "r"(w[4 * q + 3])
+                     : "memory");
+    __syncwarp();
+    const int ch = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = (lane >> 3) + 4 * i;
+        uint4 v;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(stg + (uint32_t)r * 128u + (uint32_t)((ch ^ (r & 7)) << 4))
+                     : "memory");
+        if (r < nvalid) *reinterpret_cast<uint4 *>(gbase + (int64_t)r * row_bytes + ch * 16) = v;
+    }
+    __syncwarp();   // the buffer is reused by the next call
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&b);
 }
 
 // Tile index -> (expert, m-block, n-block).  Experts are laid out by the m-block prefix:
@@ -304,23 +341,30 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------------ epilogue
-        const int quad = warp & 3;                 // TMEM lanes 32*quad .. 32*quad+31
-        const int row = quad * 32 + lane;          // row inside this CTA's 128 rows
+        // Warp quad reads TMEM lanes 32*quad .. +31 (rows of the tile; lane i holds row
+        // 32*quad + i).  GEMM2 rows go through the warp's shared-memory buffer and leave as
+        // whole 128-byte row segments (32 fp32 or 64 bf16 columns at a time); GEMM1's
+        // SwiGLU activation is stored from registers (staging it measured slower).
+        const int quad = warp & 3;
+        const uint32_t stg = smem_u32(smem + STAGES * P::kStageBytes + 256) + (uint32_t)(quad * kStageRowsBytes);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = first_tile; tile < total; tile += tile_step) {
             int e, mb, nbk;
             decode_tile(a, tile, e, mb, nbk);
             const int m0 = mb * P::kMRows + (int)rank * BM;   // first row of this CTA's half
-            const int valid = min(BM, __ldg(a.counts + e) - m0);
-            const int64_t orow = (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) +
-                                 (int64_t)m0 + row;
+            const int nvalid = min(32, __ldg(a.counts + e) - m0 - quad * 32);   // rows this warp stores
+            const int64_t orow0 = (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) +
+                                  (int64_t)m0 + quad * 32;
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
-            if (a.mode == 0) {
-                // columns [0,128) gate, [128,256) up of act columns nbk*128 .. +128
-                const int64_t o0 = orow * a.out_ld + (int64_t)nbk * (BN / 2);
+            if (nvalid <= 0) {
+                // every row of this warp is padding: nothing to store
+            } else if (a.mode == 0) {
+                // columns [0,128) gate, [128,256) up of act columns nbk*128 .. +128, stored
+                // straight from registers (64 bytes of a row per lane and round)
+                const int64_t o0 = (orow0 + lane) * a.out_ld + (int64_t)nbk * (BN / 2);
                 __nv_bfloat16 *out_hi = reinterpret_cast<__nv_bfloat16 *>(a.out) + o0;
                 __nv_bfloat16 *out_lo = a.out2 ? reinterpret_cast<__nv_bfloat16 *>(a.out2) + o0 : nullptr;
 #pragma unroll 1
@@ -329,7 +373,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld32(tbase + c, g);
                     tmem_ld32(tbase + BN / 2 + c, u);
                     tmem_wait_ld();
-                    if (row < valid) {
+                    if (lane < nvalid) {
                         uint4 *oh = reinterpret_cast<uint4 *>(out_hi + c);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
@@ -340,52 +384,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 const float a0 = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]));
                                 const float a1 = silu_mul(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1]));
                                 __nv_bfloat162 hi = __floats2bfloat162_rn(a0, a1);
-                                __nv_bfloat162 lo = __floats2bfloat162_rn(a0 - __low2float(hi),
-                                                                          a1 - __high2float(hi));
                                 wh[h] = *reinterpret_cast<uint32_t *>(&hi);
-                                wl[h] = *reinterpret_cast<uint32_t *>(&lo);
+                                wl[h] = pack_bf16x2(a0 - __low2float(hi), a1 - __high2float(hi));
                             }
                             oh[v] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-                            if (a.out2) reinterpret_cast<uint4 *>(out_lo + c)[v] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                            if (out_lo) reinterpret_cast<uint4 *>(out_lo + c)[v] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
                         }
                     }
                 }
             } else if (a.out_bf16) {
-                __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) + orow * a.out_ld + (int64_t)nbk * a.bn;
+                char *out = reinterpret_cast<char *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + orow0 * a.out_ld +
+                                                     (int64_t)nbk * a.bn);
 #pragma unroll 1
-                for (int c = 0; c < a.bn; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tbase + c, v);
-                    tmem_wait_ld();
-                    if (row < valid) {
-                        uint4 *o = reinterpret_cast<uint4 *>(out + c);
+                for (int c = 0; c < a.bn; c += 64) {
+                    uint32_t w[32];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t w[4];
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t v[32];
+                        tmem_ld32(tbase + c + 32 * h, v);
+                        tmem_wait_ld();
 #pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * h]),
-                                                                         __uint_as_float(v[8 * q + 2 * h + 1]));
-                                w[h] = *reinterpret_cast<uint32_t *>(&b);
-                            }
-                            o[q] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
+                        for (int i = 0; i < 16; ++i)
+                            w[16 * h + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
                     }
+                    warp_store_rows(stg, w, out + (int64_t)c * 2, a.out_ld * 2, nvalid, lane);
                 }
             } else {
-                float *out = reinterpret_cast<float *>(a.out) + orow * a.out_ld + (int64_t)nbk * a.bn;
+                char *out = reinterpret_cast<char *>(reinterpret_cast<float *>(a.out) + orow0 * a.out_ld +
+                                                     (int64_t)nbk * a.bn);
 #pragma unroll 1
                 for (int c = 0; c < a.bn; c += 32) {
                     uint32_t v[32];
                     tmem_ld32(tbase + c, v);
                     tmem_wait_ld();
-                    if (row < valid) {
-                        float4 *o = reinterpret_cast<float4 *>(out + c);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            o[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-                    }
+                    warp_store_rows(stg, v, out + (int64_t)c * 4, a.out_ld * 4, nvalid, lane);
                 }
             }
             tc_fence_before();
