@@ -43,15 +43,21 @@ constexpr int kStageRowsBytes = 32 * 128;       // one epilogue warp's 32 rows x
 
 // Pipeline shape.  HILO: the A operand is a bf16 pair (two A tiles per stage).  PAIR: a
 // cluster of two CTAs on two SMs computes a 256-row tile with tcgen05.mma.cta_group::2;
-// each CTA stages its own 128 rows of A and half of the B tile.
-template <bool HILO, bool PAIR> struct Pipe {
+// each CTA stages its own 128 rows of A and half of the B tile.  TALL: one CTA computes a
+// 256-row tile as two M = 128 MMAs that share each staged B tile (a third fewer operand
+// bytes per FLOP than 128-row tiles); the two 128 x 256 accumulators fill the tensor
+// memory, so there is one accumulator buffer instead of two.
+template <bool HILO, bool PAIR, bool TALL> struct Pipe {
+    static_assert(!(TALL && (PAIR || HILO)), "TALL tiles take a single bf16 A operand on one SM");
     static constexpr int kATiles = HILO ? 2 : 1;
+    static constexpr int kABytes = TALL ? 2 * A_BYTES : A_BYTES;       // one A tile
     static constexpr int kBBytes = PAIR ? B_BYTES / 2 : B_BYTES;
-    static constexpr int kStageBytes = kATiles * A_BYTES + kBBytes;     // 32..64 KB
+    static constexpr int kStageBytes = kATiles * kABytes + kBBytes;     // 32..64 KB
     static constexpr int kStages = (192 * 1024) / kStageBytes;          // 3..6
     static constexpr int kSmemBytes =
         kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/ + 4 * kStageRowsBytes /*epilogue*/;
-    static constexpr int kMRows = PAIR ? 2 * BM : BM;                   // rows of one tile
+    static constexpr int kMRows = (PAIR || TALL) ? 2 * BM : BM;         // rows of one tile
+    static constexpr int kAccBufs = TALL ? 1 : 2;                       // accumulator buffers
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A bf16
@@ -183,6 +189,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&b);
 }
 
+// silu(g) * u of the SwiGLU epilogue.  TALL tiles drain both accumulators before the
+// next tile's MMAs can start (nothing overlaps their epilogue), so they take the fast
+// reciprocal divide (within 2 ulp of the IEEE quotient); the other tiles' epilogue runs
+// under the next mainloop and keeps the IEEE divide.
+template <bool FAST> __device__ __forceinline__ float silu_act(float g, float u) {
+    return FAST ? silu_mul_fast(g, u) : silu_mul(g, u);
+}
+
 // Tile index -> (expert, m-block, n-block).  Experts are laid out by the m-block prefix:
 // expert e owns tiles [mprefix[e]*nb, mprefix[e+1]*nb); inside, n-block-major.
 __device__ __forceinline__ void decode_tile(const FfnArgs &a, int tile, int &e, int &mb, int &nbk) {
@@ -201,17 +215,17 @@ __device__ __forceinline__ void decode_tile(const FfnArgs &a, int tile, int &e, 
     mb = local - nbk * mt;
 }
 
-template <bool HILO, bool PAIR>
+template <bool HILO, bool PAIR, bool TALL>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB, FfnArgs a) {
-    using P = Pipe<HILO, PAIR>;
+    using P = Pipe<HILO, PAIR, TALL>;
     constexpr int STAGES = P::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *sA = smem;                                   // [STAGES][kATiles] A tiles
-    uint8_t *sB = smem + STAGES * P::kATiles * A_BYTES;   // [STAGES] B tiles (or halves)
+    uint8_t *sA = smem;                                     // [STAGES][kATiles] A tiles
+    uint8_t *sB = smem + STAGES * P::kATiles * P::kABytes;  // [STAGES] B tiles (or halves)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * P::kStageBytes);
     // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
@@ -271,7 +285,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t phase = 0;
         bool ok = true;
         const int b_rows_cta = PAIR ? a.bn / 2 : a.bn;
-        const uint32_t tx_cta = (uint32_t)(P::kATiles * A_BYTES + b_rows_cta * BK * 2);
+        const uint32_t tx_cta = (uint32_t)(P::kATiles * P::kABytes + b_rows_cta * BK * 2);
         const uint32_t tx = PAIR ? 2 * tx_cta : tx_cta;   // the leader's barrier sees both CTAs
         for (int tile = first_tile; tile < total && ok; tile += tile_step) {
             int e, mb, nbk;
@@ -282,7 +296,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int kb = 0; kb < a.kb; ++kb) {
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, a.status)) { ok = false; break; }
                 const uint32_t fb = full0 + 8 * stage;
-                uint8_t *sa = sA + stage * P::kATiles * A_BYTES;
+                uint8_t *sa = sA + stage * P::kATiles * P::kABytes;
                 const uint32_t sb = smem_u32(sB + stage * P::kBBytes);
                 if (PAIR) {
                     if (leader) mbar_expect_tx(fb, tx);
@@ -306,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        const uint32_t idesc = make_idesc(P::kMRows, a.bn);
+        const uint32_t idesc = make_idesc(TALL ? BM : P::kMRows, a.bn);
         for (int tile = first_tile; tile < total && ok; tile += tile_step) {
             if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, a.status)) break;
             tc_fence_after();
@@ -314,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int kb = 0; kb < a.kb; ++kb) {
                 if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(sA + stage * P::kATiles * A_BYTES);
+                const uint32_t a0 = smem_u32(sA + stage * P::kATiles * P::kABytes);
                 const uint32_t b0 = smem_u32(sB + stage * P::kBBytes);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
@@ -327,6 +341,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     } else {
                         mma_bf16(d_tmem, ad, bd, idesc, accum);
                         if (HILO) mma_bf16(d_tmem, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc, 1u);
+                        // rows 128..255 of the tile: the second 16 KB of the A tile, the
+                        // second accumulator
+                        if (TALL) mma_bf16(d_tmem + BN, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc, accum);
                     }
                 }
                 // the stage is reusable (in both CTAs) once these MMAs finish
@@ -337,7 +354,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok) break;
             if (PAIR) mma_commit_pair(tfull0 + 8 * acc);   // accumulators ready in both CTAs
             else mma_commit(tfull0 + 8 * acc);
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            if (++acc == P::kAccBufs) { acc = 0; acc_phase ^= 1; }
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------------ epilogue
@@ -352,13 +369,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int tile = first_tile; tile < total; tile += tile_step) {
             int e, mb, nbk;
             decode_tile(a, tile, e, mb, nbk);
-            const int m0 = mb * P::kMRows + (int)rank * BM;   // first row of this CTA's half
-            const int nvalid = min(32, __ldg(a.counts + e) - m0 - quad * 32);   // rows this warp stores
-            const int64_t orow0 = (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) +
-                                  (int64_t)m0 + quad * 32;
+            const int count = __ldg(a.counts + e);
+            const int64_t obase = a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e);
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, a.status)) break;
             tc_fence_after();
-            const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
+            // TALL tiles hold rows 0..127 in the first accumulator and 128..255 in the second
+#pragma unroll 1
+            for (int half = 0; half < (TALL ? 2 : 1); ++half) {
+            // first row of this warp: PAIR tiles split rows by CTA, TALL tiles by accumulator
+            const int m0 = mb * P::kMRows + (int)rank * BM + half * BM + quad * 32;
+            const int nvalid = min(32, count - m0);   // rows this warp stores
+            const int64_t orow0 = obase + m0;
+            const uint32_t tbase = tmem_base + (uint32_t)((acc + half) * BN) + ((uint32_t)(quad * 32) << 16);
             if (nvalid <= 0) {
                 // every row of this warp is padding: nothing to store
             } else if (a.mode == 0) {
@@ -381,8 +403,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
                                 const int i = v * 8 + h * 2;
-                                const float a0 = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]));
-                                const float a1 = silu_mul(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1]));
+                                const float a0 = silu_act<TALL>(__uint_as_float(g[i]), __uint_as_float(u[i]));
+                                const float a1 = silu_act<TALL>(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1]));
                                 __nv_bfloat162 hi = __floats2bfloat162_rn(a0, a1);
                                 wh[h] = *reinterpret_cast<uint32_t *>(&hi);
                                 wl[h] = pack_bf16x2(a0 - __low2float(hi), a1 - __high2float(hi));
@@ -420,13 +442,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     warp_store_rows(stg, v, out + (int64_t)c * 4, a.out_ld * 4, nvalid, lane);
                 }
             }
+            }   // half
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {   // this warp is done with the accumulator
                 if (PAIR) mbar_arrive_cluster(map_to_rank(tempty0 + 8 * acc, 0));
                 else mbar_arrive(tempty0 + 8 * acc);
             }
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            if (++acc == P::kAccBufs) { acc = 0; acc_phase ^= 1; }
         }
     }
 
@@ -455,12 +478,12 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int 
     return make_map_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, cols, box_rows);
 }
 
-template <bool HILO, bool PAIR>
+template <bool HILO, bool PAIR, bool TALL = false>
 int launch_gemm(const CUtensorMap &ma, const CUtensorMap &ma2, const CUtensorMap &mb,
                 const FfnArgs &args, int64_t max_tiles, cudaStream_t s) {
     if (max_tiles <= 0) return MOE_OK;
-    constexpr int smem = Pipe<HILO, PAIR>::kSmemBytes;
-    auto kernel = ffn_gemm_kernel<HILO, PAIR>;
+    constexpr int smem = Pipe<HILO, PAIR, TALL>::kSmemBytes;
+    auto kernel = ffn_gemm_kernel<HILO, PAIR, TALL>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;
@@ -520,6 +543,14 @@ bool use_pair(const Plan &p, int64_t K, int64_t N) {
     return p.P >= 192 * p.E && K <= 2048 && N <= 2048;
 }
 
+// One-CTA 256-row tiles: for experts with four 128-row blocks or more on average and a
+// long K loop (>= 4096), which amortises the unoverlapped epilogue.  Measured on GB300
+// (A/B, same build): DeepSeek-like prefill GEMM1 (K 7168, ~1024 rows per expert) -10%
+// clock for clock; on the Mixtral-like decode (~256 rows per expert, three of eight
+// experts a few rows over 256) GEMM1 +9% and GEMM2 +50%, since a 256-row block holding
+// a few tail rows streams the whole weight tile again and nothing hides its epilogue.
+bool use_tall(const Plan &p, int64_t K) { return p.P >= 512 * p.E && K >= 4096; }
+
 // upper bound of the row blocks over all experts: sum ceil(n_e/rows) <= P/rows + E
 int64_t max_mblocks(const Plan &p, int rows) { return p.P / rows + p.E; }
 
@@ -539,18 +570,20 @@ int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s) {
     if (p.P == 0) return MOE_OK;
     const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
     const bool pair = use_pair(p, p.H, 2 * p.I);
+    const bool tall = !pair && use_tall(p, p.H);
     CUtensorMap mA, mB;
     const void *a1 = em ? (const void *)r.recv_x : (const void *)r.apick;
     const int64_t a1_rows = em ? p.E * p.cap : p.P;
-    if (!make_map(&mA, a1, a1_rows, p.H, BM) ||
+    if (!make_map(&mA, a1, a1_rows, p.H, tall ? 2 * BM : BM) ||
         !make_map(&mB, w1p, p.E * 2 * p.I, p.H, pair ? BN / 2 : BN))
         return MOE_ERR_CUDA;
-    FfnArgs g = base_args(r, pair);
+    FfnArgs g = base_args(r, pair || tall);
     g.bn = BN; g.nb = (int)(2 * p.I / BN); g.kb = (int)(p.H / BK);
     g.a_mode = em ? 0 : 1; g.a_cap = p.cap; g.b_rows = 2 * p.I;
     g.mode = 0; g.out = r.act; g.out2 = p.act_pair ? r.act_lo : nullptr; g.out_ld = p.I; g.out_mode = 1;
     g.out_cap = 0;
     if (pair) return launch_gemm<false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
+    if (tall) return launch_gemm<false, false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
     return launch_gemm<false, false>(mA, mA, mB, g, max_mblocks(p, BM) * g.nb, s);
 }
 
@@ -559,13 +592,14 @@ int launch_gemm2(const Routing &r, const uint16_t *w2, void *expert_out, cudaStr
     if (p.P == 0) return MOE_OK;
     const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
     const bool pair = use_pair(p, p.I, p.H);
+    const bool tall = !pair && !p.act_pair && use_tall(p, p.I);
     const int bn = (p.H % 256 == 0) ? 256 : 128;
     CUtensorMap mA, mA2, mB;
-    if (!make_map(&mA, r.act, p.P, p.I, BM) ||
+    if (!make_map(&mA, r.act, p.P, p.I, tall ? 2 * BM : BM) ||
         (p.act_pair && !make_map(&mA2, r.act_lo, p.P, p.I, BM)) ||
         !make_map(&mB, w2, p.E * p.H, p.I, pair ? bn / 2 : bn))
         return MOE_ERR_CUDA;
-    FfnArgs g = base_args(r, pair);
+    FfnArgs g = base_args(r, pair || tall);
     g.bn = bn; g.nb = (int)(p.H / bn); g.kb = (int)(p.I / BK);
     g.a_mode = 1; g.a_cap = 0; g.b_rows = p.H; g.mode = 1; g.out_ld = p.H; g.out_bf16 = p.eo_bf16;
     if (em) { g.out = expert_out; g.out_mode = 0; g.out_cap = p.cap; }
@@ -575,6 +609,7 @@ int launch_gemm2(const Routing &r, const uint16_t *w2, void *expert_out, cudaStr
         return launch_gemm<true, false>(mA, mA2, mB, g, max_mblocks(p, BM) * g.nb, s);
     }
     if (pair) return launch_gemm<false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
+    if (tall) return launch_gemm<false, false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
     return launch_gemm<false, false>(mA, mA, mB, g, max_mblocks(p, BM) * g.nb, s);
 }
 

@@ -86,6 +86,19 @@ SMALL.update({
                            layout="FLAT", algo="HT", routing="uniform", T=700),
 })
 
+# Shapes with a long K loop (>= 4096: hidden for the first GEMM, intermediate for the
+# second) and >= 512 rows per expert on average, which take the one-CTA 256-row GEMM
+# tiles; ragged tails in every expert; H 384 gives 128-wide second-GEMM tiles.  The other
+# dimension stays small so that the oracle finishes in seconds.
+SMALL.update({
+    "tall_em": MoeConfig("tall_em", W=2, Tr=560, H=4096, E=4, k=2, I=512,
+                         layout="EM", algo="LL", routing="uniform", T=1100),
+    "tall_rm": MoeConfig("tall_rm", W=2, Tr=560, H=384, E=4, k=2, I=4096,
+                         layout="RM", algo="LL", routing="zipf", T=1100),
+    "tall_flat": MoeConfig("tall_flat", W=2, Tr=560, H=512, E=4, k=2, I=4096,
+                           layout="FLAT", algo="HT", routing="uniform", T=1100),
+})
+
 # Batches above the single-CTA routing limit (16384 picks), which take the three-kernel
 # multi-block routing path; narrow H and I keep the oracle fast.
 SMALL.update({

@@ -23,7 +23,7 @@ def built():
     moe.build()
 
 
-@pytest.mark.parametrize("name", ["small_em", "small_rm", "small_flat", "pair_em"])
+@pytest.mark.parametrize("name", ["small_em", "small_rm", "small_flat", "pair_em", "tall_em"])
 def test_graph_replay_matches_eager(name):
     base = gen.SMALL[name]
     cases = [make_case(base.with_(seed=40 + i, routing=r), "cuda")

@@ -29,6 +29,12 @@ SMALL_CASES = {
     "pair_rm_h384": gen.SMALL["pair_rm"],
     "pair_flat": gen.SMALL["pair_flat"],
     "pair_em_masked_i32": gen.SMALL["pair_em"].with_(mask_frac=0.2, ids_dtype="int32", seed=9),
+    # one-CTA 256-row GEMM tiles (long K loops, many rows per expert)
+    "tall_em": gen.SMALL["tall_em"],
+    "tall_rm_h384": gen.SMALL["tall_rm"],
+    "tall_flat": gen.SMALL["tall_flat"],
+    "tall_flat_h4096": gen.SMALL["tall_flat"].with_(H=4096, I=512, seed=17),
+    "tall_em_masked_i32": gen.SMALL["tall_em"].with_(mask_frac=0.2, ids_dtype="int32", seed=16),
     # multi-block routing (more than 16384 picks)
     "blocks_em": gen.SMALL["blocks_em"],
     "blocks_rm": gen.SMALL["blocks_rm"],
