@@ -81,9 +81,8 @@ def algorithmic_work(cfg, rt):
     w = {}
     w["routing"] = dict(bytes=2 * T * k * ids_b + T * k * 4 * (3 if em else 2) +
                         (0 if em else T * k * 4 + nrecv * (4 + 8 * k) + T * cfg.W * 4), flops=0)
-    w["dispatch_copy"] = dict(bytes=T * H * 2 + (R if em else nrecv) * H * (eb + rs), flops=0)
-    if not em:
-        w["gather_picks"] = dict(bytes=2 * R * H * (eb + rs), flops=0)
+    # RM/FLAT: the row scatter also writes every kept pick's row in pick-list order
+    w["dispatch_copy"] = dict(bytes=T * H * 2 + (R if em else nrecv + R) * H * (eb + rs), flops=0)
     w["gemm1_swiglu"] = dict(bytes=active * 2 * I * H * (eb + ws) + R * H * (eb + rs) + R * I * (eb + rs),
                              flops=4 * R * H * I)
     w["gemm2"] = dict(bytes=active * H * I * (eb + ws) + R * I * (eb + rs) + R * H * ob, flops=2 * R * H * I)

@@ -286,7 +286,6 @@ class MoELayer1GPU:
              "gemm2": t(EV_GEMM1_END, EV_GEMM2_END),
              "combine": t(EV_COMBINE_BEGIN, EV_COMBINE_END)}
         if not em:
-            d["gather_picks"] = t(EV_FFN_BEGIN, EV_GATHER_END)
             d["reduce_ranks"] = t(EV_GEMM2_END, EV_FFN_END)
         d["dispatch"] = t(EV_DISPATCH_BEGIN, EV_DISPATCH_END)
         d["ffn"] = t(EV_FFN_BEGIN, EV_FFN_END)

@@ -1,6 +1,7 @@
 // Data-movement kernels of the layer: the dispatch row scatter (bf16, or quantised to FP8
-// on the way), the RANK_MAJOR / FLAT pick gather and weighted local-pick reduction, the
-// combine gather-reduce, and the one-time weight preparations (gate/up interleave of w1,
+// on the way; for RANK_MAJOR / FLAT it also writes the rows in pick-list order for the
+// first GEMM), the RANK_MAJOR / FLAT weighted local-pick reduction, the combine
+// gather-reduce, and the one-time weight preparations (gate/up interleave of w1,
 // FP8 block quantisation).  All are HBM-bound copies or reductions: one warp per
 // (row, column chunk), 16-byte vector loads and stores, several loads in flight per lane.
 //
@@ -71,45 +72,63 @@ __device__ __forceinline__ void st_row4(void *base, int64_t elem, float4 v) {
 }
 
 // ---------------------------------------------------------------- dispatch row scatter
-// x[t] is read once and written to each of its receive rows
-// (EM: the slot of every kept pick; RM/FLAT: the row in every destination that got it).
-// Rows are split into chunks of 32 lanes x kCopyU 16-byte vectors (1024 bf16 or 512 fp32
-// columns); one warp handles one (row, chunk) so that even a 1024-token batch keeps
-// thousands of warps and many loads in flight.
+// x[t] is read once and written to each of its receive rows (EM: the slot of every kept
+// pick; RM/FLAT: the row in every destination that got it, and the pick-ordered row of
+// every kept pick, apick[pick_pos[t, j]], which the first GEMM reads contiguously per
+// expert).  Rows are split into chunks of 32 lanes x kCopyU 16-byte vectors (1024 bf16 or
+// 512 fp32 columns); one warp handles one (row, chunk) so that even a 1024-token batch
+// keeps thousands of warps and many loads in flight.
 constexpr int kCopyU = 4;
+constexpr int kMaxDst = MOE_MAX_WORLD + MOE_MAX_TOPK;   // receive rows + pick rows of a token
 
 struct CopyArgs {
     const uint16_t *x;
     uint16_t *recv;
-    const int32_t *slot, *recv_row;
+    uint16_t *apick;   // RM/FLAT: [P, H] rows in pick-list order
+    const int32_t *slot, *recv_row, *pick_pos;
     int T, k, W, H, layout, nchunk;
     int64_t cap;
 };
 
+// Appends to list[n..] the row indices of token t's destinations that pass `pick`: lanes
+// scan q in [0, count), row_of(q) < 0 means none.  Returns the new length.
+template <typename RowOf>
+__device__ __forceinline__ int collect_rows(int64_t *list, int n, int count, int lane, RowOf row_of) {
+    for (int q0 = 0; q0 < count; q0 += 32) {
+        const int q = q0 + lane;
+        const int64_t row = q < count ? row_of(q) : -1;
+        const unsigned bal = __ballot_sync(0xffffffffu, row >= 0);
+        if (row >= 0) list[n + __popc(bal & ((1u << lane) - 1u))] = row;
+        n += __popc(bal);
+    }
+    return n;
+}
+
 __global__ void __launch_bounds__(kCopyThreads) dispatch_copy_kernel(CopyArgs a) {
-    __shared__ int64_t dst[kWarpsPerBlock][MOE_MAX_WORLD > MOE_MAX_TOPK ? MOE_MAX_WORLD : MOE_MAX_TOPK];
+    __shared__ int64_t dst[kWarpsPerBlock][kMaxDst];   // element offset of each target row
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (token, chunk)
     const int64_t t = gw / a.nchunk;
     const int chunk = (int)(gw - t * a.nchunk);
     if (t >= a.T) return;
-    const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
-    const int n = em ? a.k : a.W;
-    int nd = 0;
-    for (int q0 = 0; q0 < n; q0 += 32) {
-        int q = q0 + lane;
-        int64_t row = -1;
-        if (q < n) {
-            if (em) {
-                row = a.slot[t * a.k + q];
-            } else {
-                int r = a.recv_row[t * a.W + q];
-                row = r >= 0 ? (int64_t)q * a.cap + r : -1;
-            }
-        }
-        unsigned bal = __ballot_sync(0xffffffffu, row >= 0);
-        if (row >= 0) dst[warp][nd + __popc(bal & ((1u << lane) - 1u))] = row;
-        nd += __popc(bal);
+    int nd;
+    int np = 0;   // the last np entries are rows of apick
+    if (a.layout == MOE_LAYOUT_EXPERT_MAJOR) {
+        nd = collect_rows(dst[warp], 0, a.k, lane, [&](int q) -> int64_t {
+            const int s = a.slot[t * a.k + q];
+            return s >= 0 ? (int64_t)s * a.H : -1;
+        });
+    } else {
+        nd = collect_rows(dst[warp], 0, a.W, lane, [&](int q) -> int64_t {
+            const int r = a.recv_row[t * a.W + q];
+            return r >= 0 ? ((int64_t)q * a.cap + r) * a.H : -1;
+        });
+        const int n0 = nd;
+        nd = collect_rows(dst[warp], nd, a.k, lane, [&](int q) -> int64_t {
+            const int p = a.pick_pos[t * a.k + q];
+            return p >= 0 ? (int64_t)p * a.H : -1;
+        });
+        np = nd - n0;
     }
     __syncwarp();
     const int nv = a.H / 8;   // uint4 per row
@@ -120,55 +139,11 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_copy_kernel(CopyArgs a)
     for (int u = 0; u < kCopyU; ++u)
         if (c0 + 32 * u < nv) v[u] = ld_nc_v4(src + c0 + 32 * u);
     for (int d = 0; d < nd; ++d) {
-        uint4 *o = reinterpret_cast<uint4 *>(a.recv + dst[warp][d] * a.H);
+        uint4 *o = reinterpret_cast<uint4 *>((d < nd - np ? a.recv : a.apick) + dst[warp][d]);
 #pragma unroll
         for (int u = 0; u < kCopyU; ++u)
             if (c0 + 32 * u < nv) o[c0 + 32 * u] = v[u];
     }
-}
-
-// -------------------------------------------- RANK_MAJOR / FLAT: gather rows of the picks
-// apick[p] = recv row of pick p (destination d = e / Le, row recv_row[t, d]), so the first
-// GEMM reads the expert-grouped rows contiguously.
-struct GatherArgs {
-    const uint16_t *recv;
-    uint16_t *apick;
-    const int32_t *offsets, *pick_src, *recv_row;
-    int E, Le, k, W, H, nchunk;
-    int64_t P, cap;
-};
-
-__device__ __forceinline__ int expert_of_pick(const int32_t *offsets, int E, int p) {
-    int lo = 0, hi = E - 1;   // largest e with offsets[e] <= p
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (offsets[mid] <= p) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
-__global__ void __launch_bounds__(kCopyThreads) gather_picks_kernel(GatherArgs a) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (pick, chunk)
-    const int64_t p = gw / a.nchunk;
-    const int chunk = (int)(gw - p * a.nchunk);
-    if (p >= a.P || p >= a.offsets[a.E]) return;
-    const int e = expert_of_pick(a.offsets, a.E, (int)p);
-    const int i = a.pick_src[p];
-    const int t = i / a.k, d = e / a.Le;
-    const int64_t row = (int64_t)d * a.cap + a.recv_row[(int64_t)t * a.W + d];
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.recv + row * a.H);
-    uint4 *dst = reinterpret_cast<uint4 *>(a.apick + p * a.H);
-    const int nv = a.H / 8;
-    const int c0 = chunk * 32 * kCopyU + lane;
-    uint4 v[kCopyU];
-#pragma unroll
-    for (int u = 0; u < kCopyU; ++u)
-        if (c0 + 32 * u < nv) v[u] = ld_nc_v4(src + c0 + 32 * u);
-#pragma unroll
-    for (int u = 0; u < kCopyU; ++u)
-        if (c0 + 32 * u < nv) dst[c0 + 32 * u] = v[u];
 }
 
 // ------------------------- RANK_MAJOR / FLAT: weighted reduction over a row's local picks
@@ -365,40 +340,38 @@ __device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v
 
 // FP8 dispatch: like dispatch_copy_kernel, but each 128-column block of x[t] is quantised
 // once (16 lanes x 8 columns: the half-warp reduces amax) and the e4m3 codes plus the
-// block scale are written to every receive row of the token.
+// block scale are written to every receive row of the token (and for RM/FLAT to its
+// pick-ordered rows).
 struct QuantCopyArgs {
     const uint16_t *x;
     uint8_t *recv;          // [nrecv, H] codes
     float *recv_scales;     // [H/128][nrecv]
-    const int32_t *slot, *recv_row;
+    uint8_t *apick;         // RM/FLAT: [P, H] codes in pick-list order
+    float *apick_scales;    // RM/FLAT: [H/128][P]
+    const int32_t *slot, *recv_row, *pick_pos;
     int T, k, W, H, layout, nchunk;
-    int64_t cap, nrecv;
+    int64_t cap, nrecv, P;
 };
 
 __global__ void __launch_bounds__(kCopyThreads) dispatch_quant_kernel(QuantCopyArgs a) {
-    __shared__ int64_t dst[kWarpsPerBlock][MOE_MAX_WORLD > MOE_MAX_TOPK ? MOE_MAX_WORLD : MOE_MAX_TOPK];
+    __shared__ int64_t dst[kWarpsPerBlock][kMaxDst];   // row index of each target row
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (token, chunk)
     const int64_t t = gw / a.nchunk;
     const int chunk = (int)(gw - t * a.nchunk);
     if (t >= a.T) return;
-    const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
-    const int n = em ? a.k : a.W;
-    int nd = 0;
-    for (int q0 = 0; q0 < n; q0 += 32) {
-        int q = q0 + lane;
-        int64_t row = -1;
-        if (q < n) {
-            if (em) {
-                row = a.slot[t * a.k + q];
-            } else {
-                int r = a.recv_row[t * a.W + q];
-                row = r >= 0 ? (int64_t)q * a.cap + r : -1;
-            }
-        }
-        unsigned bal = __ballot_sync(0xffffffffu, row >= 0);
-        if (row >= 0) dst[warp][nd + __popc(bal & ((1u << lane) - 1u))] = row;
-        nd += __popc(bal);
+    int nd;
+    int np = 0;   // the last np entries are rows of apick
+    if (a.layout == MOE_LAYOUT_EXPERT_MAJOR) {
+        nd = collect_rows(dst[warp], 0, a.k, lane, [&](int q) -> int64_t { return a.slot[t * a.k + q]; });
+    } else {
+        nd = collect_rows(dst[warp], 0, a.W, lane, [&](int q) -> int64_t {
+            const int r = a.recv_row[t * a.W + q];
+            return r >= 0 ? (int64_t)q * a.cap + r : -1;
+        });
+        const int n0 = nd;
+        nd = collect_rows(dst[warp], nd, a.k, lane, [&](int q) -> int64_t { return a.pick_pos[t * a.k + q]; });
+        np = nd - n0;
     }
     __syncwarp();
     const int nv = a.H / 8;   // 8-column vectors per row; a 128-column block is 16 of them
@@ -425,53 +398,19 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_quant_kernel(QuantCopyA
     }
     for (int d = 0; d < nd; ++d) {
         const int64_t row = dst[warp][d];
-        uint2 *o = reinterpret_cast<uint2 *>(a.recv + row * a.H);
+        const bool pick = d >= nd - np;
+        uint2 *o = reinterpret_cast<uint2 *>((pick ? a.apick : a.recv) + row * a.H);
+        float *so = (pick ? a.apick_scales : a.recv_scales) + row;
+        const int64_t sstride = pick ? a.P : a.nrecv;
 #pragma unroll
         for (int u = 0; u < kCopyU; ++u) {
             const int c = c0 + 32 * u;
             if (c < nv) {
                 o[c] = q[u];
-                if ((lane & 15) == 0) a.recv_scales[(int64_t)(c >> 4) * a.nrecv + row] = sc[u];
+                if ((lane & 15) == 0) so[(int64_t)(c >> 4) * sstride] = sc[u];
             }
         }
     }
-}
-
-// RANK_MAJOR / FLAT, FP8: apick[p] = codes of the pick's receive row, and its scales.
-struct GatherF8Args {
-    const uint8_t *recv;
-    const float *recv_scales;   // [H/128][nrecv]
-    uint8_t *apick;
-    float *apick_scales;        // [H/128][P]
-    const int32_t *offsets, *pick_src, *recv_row;
-    int E, Le, k, W, H, nchunk;
-    int64_t P, cap, nrecv;
-};
-
-__global__ void __launch_bounds__(kCopyThreads) gather_picks_fp8_kernel(GatherF8Args a) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (pick, chunk)
-    const int64_t p = gw / a.nchunk;
-    const int chunk = (int)(gw - p * a.nchunk);
-    if (p >= a.P || p >= a.offsets[a.E]) return;
-    const int e = expert_of_pick(a.offsets, a.E, (int)p);
-    const int i = a.pick_src[p];
-    const int t = i / a.k, d = e / a.Le;
-    const int64_t row = (int64_t)d * a.cap + a.recv_row[(int64_t)t * a.W + d];
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.recv + row * a.H);
-    uint4 *dst = reinterpret_cast<uint4 *>(a.apick + p * a.H);
-    const int nv = a.H / 16;
-    const int c0 = chunk * 32 * kCopyU + lane;
-    uint4 v[kCopyU];
-#pragma unroll
-    for (int u = 0; u < kCopyU; ++u)
-        if (c0 + 32 * u < nv) v[u] = ld_nc_v4(src + c0 + 32 * u);
-#pragma unroll
-    for (int u = 0; u < kCopyU; ++u)
-        if (c0 + 32 * u < nv) dst[c0 + 32 * u] = v[u];
-    if (chunk == 0)
-        for (int b = lane; b < a.H / 128; b += 32)
-            a.apick_scales[(int64_t)b * a.P + p] = a.recv_scales[(int64_t)b * a.nrecv + row];
 }
 
 // 128x128-block quantisation of bf16 weights [E, R, C]: one CTA per block, thread
@@ -557,19 +496,9 @@ cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream
     const Plan &p = *r.p;
     if (p.T == 0) return cudaSuccess;
     const int nchunk = (int)((p.H / 8 + 32 * kCopyU - 1) / (32 * kCopyU));
-    CopyArgs a{x, r.recv_x, r.slot, r.recv_row, (int)p.T, (int)p.k, (int)p.W, (int)p.H,
-               p.layout, nchunk, p.cap};
+    CopyArgs a{x, r.recv_x, r.apick, r.slot, r.recv_row, r.pick_pos, (int)p.T, (int)p.k, (int)p.W,
+               (int)p.H, p.layout, nchunk, p.cap};
     dispatch_copy_kernel<<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_gather_picks(const Routing &r, cudaStream_t s) {
-    const Plan &p = *r.p;
-    if (p.P == 0) return cudaSuccess;
-    const int nchunk = (int)((p.H / 8 + 32 * kCopyU - 1) / (32 * kCopyU));
-    GatherArgs a{r.recv_x, r.apick, r.offsets, r.pick_src, r.recv_row,
-                 (int)p.E, (int)(p.E / p.W), (int)p.k, (int)p.W, (int)p.H, nchunk, p.P, p.cap};
-    gather_picks_kernel<<<blocks_for(p.P * nchunk), kCopyThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -609,21 +538,10 @@ cudaError_t launch_dispatch_quant(const Routing &r, const uint16_t *x, cudaStrea
     const Plan &p = *r.p;
     if (p.T == 0) return cudaSuccess;
     const int nchunk = (int)((p.H / 8 + 32 * kCopyU - 1) / (32 * kCopyU));
-    QuantCopyArgs a{x, reinterpret_cast<uint8_t *>(r.recv_x), r.recv_scales, r.slot, r.recv_row,
-                    (int)p.T, (int)p.k, (int)p.W, (int)p.H, p.layout, nchunk, p.cap, p.nrecv};
+    QuantCopyArgs a{x, reinterpret_cast<uint8_t *>(r.recv_x), r.recv_scales, reinterpret_cast<uint8_t *>(r.apick),
+                    r.apick_scales, r.slot, r.recv_row, r.pick_pos, (int)p.T, (int)p.k, (int)p.W, (int)p.H,
+                    p.layout, nchunk, p.cap, p.nrecv, p.P};
     dispatch_quant_kernel<<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_gather_picks_fp8(const Routing &r, cudaStream_t s) {
-    const Plan &p = *r.p;
-    if (p.P == 0) return cudaSuccess;
-    const int nchunk = (int)((p.H / 16 + 32 * kCopyU - 1) / (32 * kCopyU));
-    GatherF8Args a{reinterpret_cast<const uint8_t *>(r.recv_x), r.recv_scales,
-                   reinterpret_cast<uint8_t *>(r.apick), r.apick_scales, r.offsets, r.pick_src,
-                   r.recv_row, (int)p.E, (int)(p.E / p.W), (int)p.k, (int)p.W, (int)p.H, nchunk,
-                   p.P, p.cap, p.nrecv};
-    gather_picks_fp8_kernel<<<blocks_for(p.P * nchunk), kCopyThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

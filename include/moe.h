@@ -125,7 +125,8 @@ typedef enum {
 #define MOE_EV_ROUTING_END 1   /* after the three routing kernels                         */
 #define MOE_EV_DISPATCH_END 2  /* after the row scatter                                   */
 #define MOE_EV_FFN_BEGIN 3
-#define MOE_EV_GATHER_END 4    /* RANK_MAJOR / FLAT: after gathering the picks' rows       */
+#define MOE_EV_GATHER_END 4    /* recorded right after MOE_EV_FFN_BEGIN (the pick-ordered
+                                  RANK_MAJOR / FLAT rows are written by moe_dispatch)      */
 #define MOE_EV_GEMM1_END 5     /* after GEMM1 + SwiGLU                                    */
 #define MOE_EV_GEMM2_END 6     /* after GEMM2                                             */
 #define MOE_EV_FFN_END 7       /* after the RANK_MAJOR / FLAT local-pick reduction        */
@@ -244,7 +245,10 @@ int moe_expert_out_size(const moe_geom *g, size_t *bytes);
  * Computes (deterministically; atomics decide no position): per-expert counts and
  * offsets, the position of every pick in its expert's rows in ascending (token, pick)
  * order, the EM slots and layout ranges or the RM/FLAT per-destination rows, local
- * ids and weights, then copies each token row to every place it is received.  With
+ * ids and weights, then copies each token row to every place it is received.  For RM/FLAT
+ * it also writes every kept pick's row in pick-list order into the workspace, the operand
+ * moe_expert_ffn reads (so the FFN sees the rows as dispatched: later writes to recv_x do
+ * not reach an RM/FLAT FFN).  With
  * g->quant = MOE_QUANT_FP8_E4M3 each token row is quantised once (e4m3 codes plus one
  * scale per 128 columns, moe_quant rule) as it is copied: recv_x holds the codes and
  * recv_scales the scales.
