@@ -283,8 +283,7 @@ int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void 
     Routing r = carve(p, h->workspace);
     const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
     record(h, MOE_EV_FFN_BEGIN, s);
-    if (!em && launch_gather_picks(r, s) != cudaSuccess) return MOE_ERR_CUDA;
-    record(h, MOE_EV_GATHER_END, s);
+    record(h, MOE_EV_GATHER_END, s);   // RM/FLAT pick rows were written by moe_dispatch
     if ((rc = launch_gemm1(r, static_cast<const uint16_t *>(w1_prepared_dev), s)) != MOE_OK) return rc;
     record(h, MOE_EV_GEMM1_END, s);
     if ((rc = launch_gemm2(r, static_cast<const uint16_t *>(w2_dev), expert_out_dev, s)) != MOE_OK)
@@ -312,8 +311,7 @@ int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
     Routing r = carve(p, h->workspace);
     const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
     record(h, MOE_EV_FFN_BEGIN, s);
-    if (!em && launch_gather_picks_fp8(r, s) != cudaSuccess) return MOE_ERR_CUDA;
-    record(h, MOE_EV_GATHER_END, s);
+    record(h, MOE_EV_GATHER_END, s);   // RM/FLAT pick rows were written by moe_dispatch
     if ((rc = launch_gemm1_fp8(r, static_cast<const uint8_t *>(w1q_prepared_dev), w1_scales_prepared_dev,
                                s)) != MOE_OK)
         return rc;
@@ -449,9 +447,8 @@ int moe_launches_per_layer(const moe_geom *g, int32_t *n) {
         return MOE_OK;
     }
     const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
-    // routing, row scatter, (RM/FLAT pick gather), GEMM1, GEMM2, (RM/FLAT local-pick
-    // reduction), combine
-    *n = routing_launches(p) + 1 + (em ? 0 : 1) + 2 + (em ? 0 : 1) + 1;
+    // routing, row scatter, GEMM1, GEMM2, (RM/FLAT local-pick reduction), combine
+    *n = routing_launches(p) + 1 + 2 + (em ? 0 : 1) + 1;
     return MOE_OK;
 }
 

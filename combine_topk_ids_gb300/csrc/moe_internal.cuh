@@ -56,7 +56,6 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
                            const int32_t *active, cudaStream_t s);
 int routing_launches(const Plan &p);   // kernels launch_routing queues for this geometry
 cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream_t s);
-cudaError_t launch_gather_picks(const Routing &r, cudaStream_t s);
 // expert_out: float32, or bf16 when the plan's eo_bf16 is set
 cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, cudaStream_t s);
 cudaError_t launch_combine(const Routing &r, const void *expert_out, const float *topk_w,
@@ -70,7 +69,6 @@ int launch_gemm2(const Routing &r, const uint16_t *w2, void *expert_out, cudaStr
 
 // ---- FP8 (moe_quant MOE_QUANT_FP8_E4M3) -----------------------------------------------
 cudaError_t launch_dispatch_quant(const Routing &r, const uint16_t *x, cudaStream_t s);
-cudaError_t launch_gather_picks_fp8(const Routing &r, cudaStream_t s);
 // 128x128-block quantisation of bf16 [E, rows, cols] weights; w1_inter = I interleaves the
 // gate/up row blocks of W1 (0: keep the order)
 cudaError_t launch_quantize_weights_fp8(const uint16_t *w, int64_t E, int64_t rows, int64_t cols,
