@@ -86,9 +86,34 @@ struct CopyArgs {
     uint16_t *recv;
     uint16_t *apick;   // RM/FLAT: [P, H] rows in pick-list order
     const int32_t *slot, *recv_row, *pick_pos;
+    // RM/FLAT: received local ids and weights (read), the per-pick direct rows (written)
+    const int32_t *recv_topk_idx;
+    const float *recv_topk_w;
+    int32_t *direct_row;
+    float *direct_w;
     int T, k, W, H, layout, nchunk;
     int64_t cap;
 };
+
+// RM/FLAT: for every kept pick of token t, direct_row[p] = the received row d*cap + r
+// when the pick is the only local pick of that row (its expert_out row is then
+// weight * y, written by the second GEMM), else -1; direct_w[p] = its weight.  One warp
+// (lane j = pick j) per token.
+__device__ __forceinline__ void mark_direct_picks(const CopyArgs &a, int64_t t, int lane) {
+    for (int d = 0; d < a.W; ++d) {
+        const int r = a.recv_row[t * a.W + d];
+        if (r < 0) continue;
+        const int64_t gr = (int64_t)d * a.cap + r;
+        const bool local = lane < a.k && a.recv_topk_idx[gr * a.k + lane] >= 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, local);
+        if (!local) continue;
+        const int p = a.pick_pos[t * a.k + lane];
+        if (p < 0) continue;
+        const bool single = __popc(bal) == 1;
+        a.direct_row[p] = single ? (int32_t)gr : -1;
+        if (single) a.direct_w[p] = a.recv_topk_w[gr * a.k + lane];
+    }
+}
 
 // Appends to list[n..] the row indices of token t's destinations that pass `pick`: lanes
 // scan q in [0, count), row_of(q) < 0 means none.  Returns the new length.
@@ -129,6 +154,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_copy_kernel(CopyArgs a)
             return p >= 0 ? (int64_t)p * a.H : -1;
         });
         np = nd - n0;
+        if (chunk == 0 && a.direct_row) mark_direct_picks(a, t, lane);
     }
     __syncwarp();
     const int nv = a.H / 8;   // uint4 per row
@@ -152,6 +178,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_copy_kernel(CopyArgs a)
 struct ReduceArgs {
     const void *ypick;   // float32 or bf16 rows (the kernel's BF16 parameter)
     void *out;
+    int skip_single;     // rows with one local pick were written by the second GEMM
     const int32_t *recv_count, *num_recv, *recv_src, *recv_topk_idx, *pick_pos;
     const float *recv_topk_w;
     int W, Tr, k, H, layout, nchunk;
@@ -191,6 +218,7 @@ __global__ void __launch_bounds__(kCopyThreads) reduce_ranks_kernel(ReduceArgs a
         }
         n = __popc(bal);
     }
+    if (n == 1 && a.skip_single) return;   // warp-uniform
     __syncwarp();
     const int nv = a.H / 4;
     const int c0 = chunk * 32 * kCopyU + lane;
@@ -496,17 +524,17 @@ cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream
     const Plan &p = *r.p;
     if (p.T == 0) return cudaSuccess;
     const int nchunk = (int)((p.H / 8 + 32 * kCopyU - 1) / (32 * kCopyU));
-    CopyArgs a{x, r.recv_x, r.apick, r.slot, r.recv_row, r.pick_pos, (int)p.T, (int)p.k, (int)p.W,
-               (int)p.H, p.layout, nchunk, p.cap};
+    CopyArgs a{x, r.recv_x, r.apick, r.slot, r.recv_row, r.pick_pos, r.recv_topk_idx, r.recv_topk_w,
+               r.direct_row, r.direct_w, (int)p.T, (int)p.k, (int)p.W, (int)p.H, p.layout, nchunk, p.cap};
     dispatch_copy_kernel<<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, cudaStream_t s) {
+cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, bool skip_single, cudaStream_t s) {
     const Plan &p = *r.p;
     if (p.T == 0) return cudaSuccess;
     const int nchunk = (int)((p.H / 4 + 32 * kCopyU - 1) / (32 * kCopyU));
-    ReduceArgs a{r.ypick, expert_out, r.recv_count, r.num_recv, r.recv_src, r.recv_topk_idx,
+    ReduceArgs a{r.ypick, expert_out, skip_single ? 1 : 0, r.recv_count, r.num_recv, r.recv_src, r.recv_topk_idx,
                  r.pick_pos, r.recv_topk_w, (int)p.W, (int)p.Tr, (int)p.k, (int)p.H, p.layout,
                  nchunk, p.cap};
     if (p.eo_bf16) reduce_ranks_kernel<true><<<blocks_for(p.W * p.cap * nchunk), kCopyThreads, 0, s>>>(a);

@@ -85,6 +85,13 @@ struct FfnArgs {
     int64_t out_ld;   // elements per output row
     int out_mode;  // 0: row = e*out_cap + m; 1: row = offsets[e] + m
     int64_t out_cap;
+    // mode 1, out_mode 1 (RANK_MAJOR / FLAT per-pick rows), or NULL: a pick p with
+    // direct_row[p] >= 0 is the only local pick of its received row, so the row
+    // direct_row[p] of out_direct gets direct_w[p] * y (the local-pick sum) instead of
+    // out getting y
+    const int32_t *direct_row;
+    const float *direct_w;
+    void *out_direct;
     int32_t *status;
 };
 
@@ -161,8 +168,11 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
 // warp's 4 KB shared-memory buffer (16-byte chunk q of row r at chunk q ^ (r & 7), so that
 // neither the row-per-lane writes nor the segment-per-8-lanes reads conflict on banks),
 // then each store instruction writes four whole rows' 128-byte segments.
+// With dbase set, row r goes to dbase + drow_r * row_bytes instead when the drow of lane r
+// is >= 0.
 __device__ __forceinline__ void warp_store_rows(uint32_t stg, const uint32_t (&w)[32], char *gbase,
-                                                int64_t row_bytes, int nvalid, int lane) {
+                                                int64_t row_bytes, int nvalid, int lane,
+                                                int64_t drow = -1, char *dbase = nullptr) {
     const uint32_t mine = stg + (uint32_t)lane * 128u;
 #pragma unroll
     for (int q = 0; q < 8; ++q)
@@ -179,7 +189,12 @@ __device__ __forceinline__ void warp_store_rows(uint32_t stg, const uint32_t (&w
                      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                      : "r"(stg + (uint32_t)r * 128u + (uint32_t)((ch ^ (r & 7)) << 4))
                      : "memory");
-        if (r < nvalid) *reinterpret_cast<uint4 *>(gbase + (int64_t)r * row_bytes + ch * 16) = v;
+        char *dst = gbase + (int64_t)r * row_bytes;
+        if (dbase) {
+            const int64_t dr = __shfl_sync(0xffffffffu, drow, r);
+            if (dr >= 0) dst = dbase + dr * row_bytes;
+        }
+        if (r < nvalid) *reinterpret_cast<uint4 *>(dst + ch * 16) = v;
     }
     __syncwarp();   // the buffer is reused by the next call
 }
@@ -414,32 +429,56 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 }
-            } else if (a.out_bf16) {
-                char *out = reinterpret_cast<char *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + orow0 * a.out_ld +
-                                                     (int64_t)nbk * a.bn);
-#pragma unroll 1
-                for (int c = 0; c < a.bn; c += 64) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t v[32];
-                        tmem_ld32(tbase + c + 32 * h, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            w[16 * h + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                    }
-                    warp_store_rows(stg, w, out + (int64_t)c * 2, a.out_ld * 2, nvalid, lane);
-                }
             } else {
-                char *out = reinterpret_cast<char *>(reinterpret_cast<float *>(a.out) + orow0 * a.out_ld +
-                                                     (int64_t)nbk * a.bn);
+                // the direct row of this lane's pick (RANK_MAJOR / FLAT), or -1
+                int64_t drow = -1;
+                float dw = 0.f;
+                if (a.direct_row && lane < nvalid) {
+                    drow = __ldg(a.direct_row + orow0 + lane);
+                    if (drow >= 0) dw = __ldg(a.direct_w + orow0 + lane);
+                }
+                const int esz = a.out_bf16 ? 2 : 4;
+                char *out = reinterpret_cast<char *>(a.out) + (orow0 * a.out_ld + (int64_t)nbk * a.bn) * esz;
+                char *dout = a.direct_row ? reinterpret_cast<char *>(a.out_direct) + (int64_t)nbk * a.bn * esz
+                                          : nullptr;
+                if (a.out_bf16) {
 #pragma unroll 1
-                for (int c = 0; c < a.bn; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tbase + c, v);
-                    tmem_wait_ld();
-                    warp_store_rows(stg, v, out + (int64_t)c * 4, a.out_ld * 4, nvalid, lane);
+                    for (int c = 0; c < a.bn; c += 64) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t v[32];
+                            tmem_ld32(tbase + c + 32 * h, v);
+                            tmem_wait_ld();
+                            if (drow >= 0) {
+                                // the same roundings as the local-pick reduction of a
+                                // one-pick row: bf16(y), then bf16(w * y)
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    v[i] = __float_as_uint(__fmaf_rn(
+                                        dw, __bfloat162float(__float2bfloat16_rn(__uint_as_float(v[i]))), 0.0f));
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                w[16 * h + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                        }
+                        warp_store_rows(stg, w, out + (int64_t)c * 2, a.out_ld * 2, nvalid, lane, drow,
+                                        dout ? dout + (int64_t)c * 2 : nullptr);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < a.bn; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tbase + c, v);
+                        tmem_wait_ld();
+                        if (drow >= 0) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v[i] = __float_as_uint(__fmaf_rn(dw, __uint_as_float(v[i]), 0.0f));
+                        }
+                        warp_store_rows(stg, v, out + (int64_t)c * 4, a.out_ld * 4, nvalid, lane, drow,
+                                        dout ? dout + (int64_t)c * 4 : nullptr);
+                    }
                 }
             }
             }   // half
@@ -603,7 +642,10 @@ int launch_gemm2(const Routing &r, const uint16_t *w2, void *expert_out, cudaStr
     g.bn = bn; g.nb = (int)(p.H / bn); g.kb = (int)(p.I / BK);
     g.a_mode = 1; g.a_cap = 0; g.b_rows = p.H; g.mode = 1; g.out_ld = p.H; g.out_bf16 = p.eo_bf16;
     if (em) { g.out = expert_out; g.out_mode = 0; g.out_cap = p.cap; }
-    else { g.out = r.ypick; g.out_mode = 1; g.out_cap = 0; }
+    else {
+        g.out = r.ypick; g.out_mode = 1; g.out_cap = 0;
+        g.direct_row = r.direct_row; g.direct_w = r.direct_w; g.out_direct = expert_out;
+    }
     if (p.act_pair) {
         if (pair) return launch_gemm<true, true>(mA, mA2, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
         return launch_gemm<true, false>(mA, mA2, mB, g, max_mblocks(p, BM) * g.nb, s);

@@ -121,6 +121,8 @@ int make_plan(const moe_geom &g, Plan *p) {
     q.apick = take(em ? 0 : eb * P * H);
     q.apick_scales = take(em || !f8 ? 0 : 4 * P * (H / 128));
     q.ypick = take(em ? 0 : (q.eo_bf16 ? 2 : 4) * P * H);
+    q.direct_row = take(em ? 0 : 4 * P);
+    q.direct_w = take(em ? 0 : 4 * P);
     q.total = off;
     return MOE_OK;
 }
@@ -143,6 +145,8 @@ Routing carve(const Plan &p, void *ws) {
     r.act_lo = p.act_pair ? reinterpret_cast<uint16_t *>(b + p.act_lo) : nullptr;
     r.apick = reinterpret_cast<uint16_t *>(b + p.apick);
     r.ypick = b + p.ypick;
+    r.direct_row = p.layout != MOE_LAYOUT_EXPERT_MAJOR ? i32(p.direct_row) : nullptr;
+    r.direct_w = p.layout != MOE_LAYOUT_EXPERT_MAJOR ? reinterpret_cast<float *>(b + p.direct_w) : nullptr;
     const bool f8 = p.quant == MOE_QUANT_FP8_E4M3;
     r.recv_scales = f8 ? reinterpret_cast<float *>(b + p.recv_scales) : nullptr;
     r.act_scales = f8 ? reinterpret_cast<float *>(b + p.act_scales) : nullptr;
@@ -289,7 +293,7 @@ int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void 
     if ((rc = launch_gemm2(r, static_cast<const uint16_t *>(w2_dev), expert_out_dev, s)) != MOE_OK)
         return rc;
     record(h, MOE_EV_GEMM2_END, s);
-    if (!em && launch_reduce_ranks(r, expert_out_dev, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!em && launch_reduce_ranks(r, expert_out_dev, true, s) != cudaSuccess) return MOE_ERR_CUDA;
     record(h, MOE_EV_FFN_END, s);
     return MOE_OK;
 }
@@ -320,7 +324,7 @@ int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
                                s)) != MOE_OK)
         return rc;
     record(h, MOE_EV_GEMM2_END, s);
-    if (!em && launch_reduce_ranks(r, expert_out_dev, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!em && launch_reduce_ranks(r, expert_out_dev, false, s) != cudaSuccess) return MOE_ERR_CUDA;
     record(h, MOE_EV_FFN_END, s);
     return MOE_OK;
 }

@@ -29,7 +29,7 @@ struct Plan {
     size_t status, counts, offsets, mprefix, mprefix2, pick_pos, pick_src, slot, layout_range,
         blk_hist, blk_base, recv_row, recv_count, num_recv, recv_src, recv_topk_idx,
         recv_topk_w, blk_dhist, blk_dbase, recv_x, recv_scales, act, act_lo, act_scales, apick,
-        apick_scales, ypick, total;
+        apick_scales, ypick, direct_row, direct_w, total;
 };
 
 // Returns MOE_OK or a moe_error for an invalid geometry.
@@ -44,6 +44,12 @@ struct Routing {
     float *recv_topk_w;
     uint16_t *recv_x, *act, *act_lo, *apick;   // act (and act_lo for the pair): SwiGLU output
     void *ypick;    // RM/FLAT per-pick GEMM2 rows: float32, or bf16 with eo_bf16
+    // RM/FLAT, per pick in pick-list order: the expert_out row (d*cap + r) when the pick is
+    // the only local pick of its received row, else -1; and that pick's routing weight.
+    // Written by the dispatch row scatter; the bf16 second GEMM then stores weight * y
+    // straight into expert_out for such picks, and the local-pick reduction skips the row.
+    int32_t *direct_row;
+    float *direct_w;
     // FP8 geometry: recv_x / act / apick hold e4m3 codes (one byte per element); their
     // scales are column-block major ([cols/128][rows]); act_lo is unused
     float *recv_scales, *act_scales, *apick_scales;
@@ -56,8 +62,9 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
                            const int32_t *active, cudaStream_t s);
 int routing_launches(const Plan &p);   // kernels launch_routing queues for this geometry
 cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream_t s);
-// expert_out: float32, or bf16 when the plan's eo_bf16 is set
-cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, cudaStream_t s);
+// expert_out: float32, or bf16 when the plan's eo_bf16 is set.  skip_single: rows with one
+// local pick were already written by the second GEMM (direct_row)
+cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, bool skip_single, cudaStream_t s);
 cudaError_t launch_combine(const Routing &r, const void *expert_out, const float *topk_w,
                            uint16_t *out, cudaStream_t s);
 cudaError_t launch_prepare_w1(const moe_geom &g, const uint16_t *w1, uint16_t *w1p,
