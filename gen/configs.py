@@ -121,11 +121,15 @@ ACTPAIR = {name + "_actpair": cfg.with_(name=name + "_actpair", act="pair") for 
 
 ALL = {**CONFIGS, **SMALL, **FP8, **EO16, **ACTPAIR}
 
-# A smaller EXPERT_MAJOR case for detailed (multi-pass) profiler captures of the same
-# kernels: 4 experts, weights 0.7 GB (larger than L2), about 1.3 GB on the device.
+# Smaller cases for detailed (multi-pass) profiler captures of the same kernels: 4
+# experts, weights 0.7 GB (larger than L2), about 1.3 GB on the device.  ncu_em_small
+# (512 rows per expert) takes the one-CTA 256-row bf16 tiles and is the FP8 profile case.
 PROFILE = {
     "ncu_em_small": MoeConfig("ncu_em_small", W=4, Tr=256, H=4096, E=4, k=2, I=7168,
                               layout="EM", algo="LL", routing="uniform"),
+    # 384 rows per expert: the 128-row tiles of the Mixtral-like decode workload
+    "ncu_em_mid": MoeConfig("ncu_em_mid", W=4, Tr=192, H=4096, E=4, k=2, I=7168,
+                            layout="EM", algo="LL", routing="uniform"),
     "ncu_flat_small": MoeConfig("ncu_flat_small", W=8, Tr=512, H=7168, E=32, k=8, I=2048,
                                 layout="FLAT", algo="HT", routing="uniform"),
 }
