@@ -185,64 +185,114 @@ struct ReduceArgs {
     int64_t cap;
 };
 
+// G consecutive elements (16 bytes: 4 float32 or 8 bf16) of a row as fp32, and back.
 template <bool BF16>
-__global__ void __launch_bounds__(kCopyThreads) reduce_ranks_kernel(ReduceArgs a) {
+__device__ __forceinline__ void ld_group(const void *base, int64_t elem, float (&f)[BF16 ? 8 : 4]) {
+    if (BF16) {
+        const uint4 v = ld_nc_v4(reinterpret_cast<const uint16_t *>(base) + elem);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = bf16_lo(w[i]);
+            f[2 * i + 1] = bf16_hi(w[i]);
+        }
+    } else {
+        const float4 v = ld_nc_f4(reinterpret_cast<const float *>(base) + elem);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void st_group(void *base, int64_t elem, const float (&f)[BF16 ? 8 : 4]) {
+    if (BF16) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&b);
+        }
+        *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(base) + elem) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(base) + elem) = make_float4(f[0], f[1], f[2], f[3]);
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kCopyThreads, 3) reduce_ranks_kernel(ReduceArgs a) {
+    constexpr int G = BF16 ? 8 : 4;   // elements per 16-byte group
+    constexpr int U = BF16 ? 2 : 4;   // groups per lane and pick in flight (<= 85 registers)
     __shared__ int64_t src[kWarpsPerBlock][MOE_MAX_TOPK];
     __shared__ float wt[kWarpsPerBlock][MOE_MAX_TOPK];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (row, chunk)
-    const int64_t gr = gw / a.nchunk;                                 // d*cap + r
-    const int chunk = (int)(gw - gr * a.nchunk);
-    if (gr >= (int64_t)a.W * a.cap) return;
-    const int d = (int)(gr / a.cap);
-    const int r = (int)(gr % a.cap);
-    bool used = a.layout == MOE_LAYOUT_RANK_MAJOR
-                    ? (r % a.Tr) < a.recv_count[d * a.W + r / a.Tr]
-                    : r < a.num_recv[d];
-    if (!used) return;
-    const int t = a.recv_src[gr];
-    int n = 0;
-    {
-        int j = lane;
+    const int64_t rows = (int64_t)a.W * a.cap;
+    const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerBlock;
+    const int ng = a.H / G;   // groups per row
+    // grid-stride over received rows d*cap + r, one warp per row: a row's routing is read
+    // once, unused rows and rows the second GEMM already wrote cost a few loads
+    for (int64_t gr = (int64_t)blockIdx.x * kWarpsPerBlock + warp; gr < rows; gr += nwarps) {
+        const int d = (int)(gr / a.cap);
+        const int r = (int)(gr - (int64_t)d * a.cap);
+        const bool used = a.layout == MOE_LAYOUT_RANK_MAJOR
+                              ? (r % a.Tr) < a.recv_count[d * a.W + r / a.Tr]
+                              : r < a.num_recv[d];
+        if (!used) continue;   // warp-uniform
+        const int t = a.recv_src[gr];
         int64_t s = -1;
         float w = 0.f;
-        if (j < a.k && a.recv_topk_idx[gr * a.k + j] >= 0) {
-            s = a.pick_pos[(int64_t)t * a.k + j];
-            w = a.recv_topk_w[gr * a.k + j];
+        if (lane < a.k && a.recv_topk_idx[gr * a.k + lane] >= 0) {
+            s = a.pick_pos[(int64_t)t * a.k + lane];
+            w = a.recv_topk_w[gr * a.k + lane];
         }
-        unsigned bal = __ballot_sync(0xffffffffu, s >= 0);
+        const unsigned bal = __ballot_sync(0xffffffffu, s >= 0);
+        const int n = __popc(bal);
+        if (n == 1 && a.skip_single) continue;   // warp-uniform
+        __syncwarp();   // the previous row's readers are done with src / wt
         if (s >= 0) {
-            int q = __popc(bal & ((1u << lane) - 1u));
+            const int q = __popc(bal & ((1u << lane) - 1u));
             src[warp][q] = s;
             wt[warp][q] = w;
         }
-        n = __popc(bal);
-    }
-    if (n == 1 && a.skip_single) return;   // warp-uniform
-    __syncwarp();
-    const int nv = a.H / 4;
-    const int c0 = chunk * 32 * kCopyU + lane;
-    float4 acc[kCopyU];
+        __syncwarp();
+        for (int g0 = lane; g0 < ng; g0 += 32 * U) {
+            float acc[U][G];
 #pragma unroll
-    for (int u = 0; u < kCopyU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < n; ++q) {
-        const int64_t row = src[warp][q] * a.H;
-        const float w = wt[warp][q];
-        float4 y[kCopyU];
+            for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int u = 0; u < kCopyU; ++u)
-            if (c0 + 32 * u < nv) y[u] = ld_row4<BF16>(a.ypick, row + 4 * (c0 + 32 * u));
+                for (int i = 0; i < G; ++i) acc[u][i] = 0.f;
+            // two picks' rows in flight at a time; the sum stays in ascending pick order
+            for (int q = 0; q < n; q += 2) {
+                const bool two = q + 1 < n;
+                const int64_t row0 = src[warp][q] * a.H;
+                const int64_t row1 = two ? src[warp][q + 1] * a.H : row0;
+                float y0[U][G], y1[U][G];
 #pragma unroll
-        for (int u = 0; u < kCopyU; ++u) {
-            acc[u].x = fmaf(w, y[u].x, acc[u].x);
-            acc[u].y = fmaf(w, y[u].y, acc[u].y);
-            acc[u].z = fmaf(w, y[u].z, acc[u].z);
-            acc[u].w = fmaf(w, y[u].w, acc[u].w);
+                for (int u = 0; u < U; ++u) {
+                    const int g = g0 + 32 * u;
+                    if (g < ng) {
+                        ld_group<BF16>(a.ypick, row0 + (int64_t)G * g, y0[u]);
+                        if (two) ld_group<BF16>(a.ypick, row1 + (int64_t)G * g, y1[u]);
+                    }
+                }
+                const float w0 = wt[warp][q];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int i = 0; i < G; ++i) acc[u][i] = fmaf(w0, y0[u][i], acc[u][i]);
+                if (two) {
+                    const float w1 = wt[warp][q + 1];
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+#pragma unroll
+                        for (int i = 0; i < G; ++i) acc[u][i] = fmaf(w1, y1[u][i], acc[u][i]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int g = g0 + 32 * u;
+                if (g < ng) st_group<BF16>(a.out, gr * a.H + (int64_t)G * g, acc[u]);
+            }
         }
     }
-#pragma unroll
-    for (int u = 0; u < kCopyU; ++u)
-        if (c0 + 32 * u < nv) st_row4<BF16>(a.out, gr * a.H + 4 * (c0 + 32 * u), acc[u]);
 }
 
 // ----------------------------------------------------------------------------- combine
@@ -537,8 +587,22 @@ cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, bool skip_si
     ReduceArgs a{r.ypick, expert_out, skip_single ? 1 : 0, r.recv_count, r.num_recv, r.recv_src, r.recv_topk_idx,
                  r.pick_pos, r.recv_topk_w, (int)p.W, (int)p.Tr, (int)p.k, (int)p.H, p.layout,
                  nchunk, p.cap};
-    if (p.eo_bf16) reduce_ranks_kernel<true><<<blocks_for(p.W * p.cap * nchunk), kCopyThreads, 0, s>>>(a);
-    else reduce_ranks_kernel<false><<<blocks_for(p.W * p.cap * nchunk), kCopyThreads, 0, s>>>(a);
+    // grid-stride over rows: no more blocks than can be resident at once, so that no block
+    // starts its rows after the others have finished theirs
+    static int resident[2] = {0, 0};
+    const int bi = p.eo_bf16 ? 1 : 0;
+    if (resident[bi] == 0) {
+        int nb = 0;
+        const cudaError_t e = p.eo_bf16
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, reduce_ranks_kernel<true>, kCopyThreads, 0)
+            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, reduce_ranks_kernel<false>, kCopyThreads, 0);
+        if (e != cudaSuccess) return e;
+        resident[bi] = nb > 0 ? nb : 1;
+    }
+    int64_t blocks = blocks_for(p.W * p.cap);
+    if (blocks > (int64_t)num_sms() * resident[bi]) blocks = (int64_t)num_sms() * resident[bi];
+    if (p.eo_bf16) reduce_ranks_kernel<true><<<(unsigned)blocks, kCopyThreads, 0, s>>>(a);
+    else reduce_ranks_kernel<false><<<(unsigned)blocks, kCopyThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -245,7 +245,7 @@ int moe_dispatch(const moe_geom *g, const void *x_dev, const void *topk_ids_dev,
     h->workspace_bytes = workspace_bytes;
 
     record(h, MOE_EV_DISPATCH_BEGIN, s);
-    if (cudaMemsetAsync(r.status, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    // launch_routing clears the status word before any kernel can set a bit
     if (launch_routing(r, topk_ids_dev, ids_dtype == MOE_IDS_INT64, topk_weights_dev,
                        active_ranks_dev, s) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -58,6 +58,7 @@ struct Routing {
 Routing carve(const Plan &p, void *ws);
 
 // ---- launchers (return cudaGetLastError of the launch) -------------------------------
+// Also clears the status word (before any routing kernel can set a bit).
 cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const float *topk_w,
                            const int32_t *active, cudaStream_t s);
 int routing_launches(const Plan &p);   // kernels launch_routing queues for this geometry

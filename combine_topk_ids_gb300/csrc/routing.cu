@@ -29,6 +29,7 @@ struct RouteArgs {
     const float *topk_w;
     const int32_t *active;          // EP rank-health mask [W] (NULL: all ranks active)
     int T, W, Tr, E, k, Le, layout, tb, nbpr, nb;
+    int zero_status;                // the single-CTA kernel clears the status word first
     int64_t cap;
     int32_t *status, *counts, *offsets, *mprefix, *mprefix2, *pick_pos, *pick_src, *slot, *layout_range;
     int32_t *blk_hist, *blk_base;   // [E][nb]
@@ -413,7 +414,10 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a)
     int *off = dw + W * W;                  // [E]     expert offsets
     int *cnt = off + E;                     // [E]     kept counts
     __shared__ unsigned long long s_act;
-    if (threadIdx.x == 0) s_act = load_active_mask(a);
+    if (threadIdx.x == 0) {
+        s_act = load_active_mask(a);
+        if (a.zero_status) *a.status = 0;   // before the barrier below, so before any bit is set
+    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
     const int total_sm = kFusedWarps * (E + W) + E * W + W * W + 2 * E;
@@ -618,9 +622,12 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
     a.recv_row = r.recv_row; a.recv_count = r.recv_count; a.num_recv = r.num_recv;
     a.recv_src = r.recv_src; a.recv_topk_idx = r.recv_topk_idx; a.recv_topk_w = r.recv_topk_w;
     a.blk_dhist = r.blk_dhist; a.blk_dbase = r.blk_dbase;
+    a.zero_status = 0;
 
-    // one fused CTA for small batches with few experts (bounded shared memory)
+    // one fused CTA for small batches with few experts (bounded shared memory); it clears
+    // the status word itself (one launch less in a latency-bound step)
     if (routing_launches(p) == 1) {
+        a.zero_status = 1;
         const size_t smf = (size_t)(kFusedWarps * (a.E + a.W) + a.E * a.W + a.W * a.W + 2 * a.E) *
                            sizeof(int);
         if (smf > 48 * 1024) {
@@ -632,6 +639,8 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
         return cudaGetLastError();
     }
 
+    // several blocks may raise status bits: clear the word before the first of them runs
+    if (cudaMemsetAsync(a.status, 0, sizeof(int32_t), s) != cudaSuccess) return cudaGetLastError();
     size_t sm1 = (size_t)(a.E + a.W) * sizeof(int);
     route_count_kernel<<<a.nb, kRouteThreads, sm1, s>>>(a);
     route_scan_kernel<<<1, 1024, 0, s>>>(a);
