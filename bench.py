@@ -159,8 +159,9 @@ class ClockSampler:
 
 
 # sources that define the grouped-GEMM kernels whose ncu counters are committed (the bf16
-# kernels, or the FP8 ones for FP8 workloads), plus the compiler flags they are built with
-TRAFFIC_COMMON = ("combine_topk_ids_gb300/csrc/tc_common.cuh", "combine_topk_ids_gb300/csrc/moe_internal.cuh")
+# kernels, or the FP8 ones for FP8 workloads, and their shared device helpers), plus the
+# compiler flags they are built with; the library's plumbing headers are not part of it
+TRAFFIC_COMMON = ("combine_topk_ids_gb300/csrc/tc_common.cuh",)
 TRAFFIC_SOURCES = {"bf16": ("combine_topk_ids_gb300/csrc/ffn_tc.cu",) + TRAFFIC_COMMON,
                    "fp8": ("combine_topk_ids_gb300/csrc/ffn_fp8.cu",) + TRAFFIC_COMMON}
 
