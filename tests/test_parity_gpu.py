@@ -24,6 +24,10 @@ SMALL_CASES = {
     "small_em_h384": gen.SMALL["small_em"].with_(H=384, seed=6),          # 128-wide GEMM2 tiles
     "small_flat_w1": gen.SMALL["small_flat"].with_(W=1, Tr=350, seed=7),  # one logical rank
     "small_rm_w8": gen.SMALL["small_rm"].with_(W=8, Tr=48, T=380, E=16, seed=8),
+    # top-1: every received row has one local pick, so the second GEMM writes every
+    # expert_out row itself and the local-pick reduction has nothing left to add
+    "small_flat_k1": gen.SMALL["small_flat"].with_(k=1, seed=18),
+    "small_rm_k1_masked": gen.SMALL["small_rm"].with_(k=1, mask_frac=0.2, seed=19),
     # two-SM GEMM tiles (many rows per expert)
     "pair_em": gen.SMALL["pair_em"],
     "pair_rm_h384": gen.SMALL["pair_rm"],
