@@ -10,16 +10,17 @@
 //     GEMM2   y   = act W2[e]^T, or act_hi W2[e]^T + act_lo W2[e]^T   [n_e, H], fp32
 // The pair carries act to about 16 significant bits (GEMM2 then runs two MMAs per k-step).
 //
-// One persistent kernel per GEMM, one CTA per SM, 256 threads:
+// One persistent kernel per GEMM, one CTA per SM, 384 threads:
 //   warp 0      TMA producer: 128x64 A tile(s) + 256x64 B tile per stage (SWIZZLE_128B),
 //               a 4-stage (GEMM1) or 3-stage (GEMM2: A_hi, A_lo, B) mbarrier ring
 //   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16, M=128,
 //               N=256, K=16, bf16 x bf16 -> fp32 into one of two 256-column TMEM
 //               accumulators, tcgen05.commit frees smem stages and hands tiles over
 //   warp 2      TMEM allocator (512 columns)
-//   warps 4-7   epilogue: tcgen05.ld 32x32b rows -> registers -> SwiGLU / fp32 or bf16
-//               -> a 4 KB shared-memory buffer per warp -> whole 128-byte row segments
-//               in global memory, overlapped with the next tile's mainloop
+//   warps 4-11  epilogue, two warps per TMEM lane quarter, each on half of the tile's
+//               columns: tcgen05.ld 32x32b rows -> registers -> SwiGLU / fp32 or bf16
+//               -> (GEMM2) a 4 KB shared-memory buffer per warp -> whole 128-byte row
+//               segments in global memory, overlapped with the next tile's mainloop
 //               (double-buffered accumulator)
 // Tiles: per expert ceil(n_e/128) m-blocks x (N/256) n-blocks, enumerated expert by expert,
 // n-block-major with the m-blocks of one weight tile adjacent (they run on neighbouring
@@ -37,7 +38,8 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 64;   // BN: widest n-tile (GEMM2 may use 128)
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
-constexpr int THREADS = 256;
+constexpr int THREADS = 384;                    // 4 control warps + 8 epilogue warps
+constexpr int EPI_WARPS = 8;
 constexpr int TMEM_COLS = 2 * BN;               // two fp32 accumulators of 128 x 256
 constexpr int kStageRowsBytes = 32 * 128;       // one epilogue warp's 32 rows x 128 B
 
@@ -55,7 +57,7 @@ template <bool HILO, bool PAIR, bool TALL> struct Pipe {
     static constexpr int kStageBytes = kATiles * kABytes + kBBytes;     // 32..64 KB
     static constexpr int kStages = (192 * 1024) / kStageBytes;          // 3..6
     static constexpr int kSmemBytes =
-        kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/ + 4 * kStageRowsBytes /*epilogue*/;
+        kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/ + EPI_WARPS * kStageRowsBytes /*epilogue*/;
     static constexpr int kMRows = (PAIR || TALL) ? 2 * BM : BM;         // rows of one tile
     static constexpr int kAccBufs = TALL ? 1 : 2;                       // accumulator buffers
 };
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(tfull0 + 8 * s, 1);
-            mbar_init(tempty0 + 8 * s, PAIR ? 8 : 4);   // one arrival per epilogue warp
+            mbar_init(tempty0 + 8 * s, PAIR ? 2 * EPI_WARPS : EPI_WARPS);   // one arrival per epilogue warp
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -377,8 +379,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // 32*quad + i).  GEMM2 rows go through the warp's shared-memory buffer and leave as
         // whole 128-byte row segments (32 fp32 or 64 bf16 columns at a time); GEMM1's
         // SwiGLU activation is stored from registers (staging it measured slower).
+        // Warps 4-7 and 8-11 read the same TMEM lane quarters (warp % 4) and split the
+        // tile's columns in halves.
         const int quad = warp & 3;
-        const uint32_t stg = smem_u32(smem + STAGES * P::kStageBytes + 256) + (uint32_t)(quad * kStageRowsBytes);
+        const int chalf = (warp - 4) >> 2;   // 0: first half of the columns, 1: second
+        const uint32_t stg = smem_u32(smem + STAGES * P::kStageBytes + 256) + (uint32_t)((warp - 4) * kStageRowsBytes);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = first_tile; tile < total; tile += tile_step) {
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __nv_bfloat16 *out_hi = reinterpret_cast<__nv_bfloat16 *>(a.out) + o0;
                 __nv_bfloat16 *out_lo = a.out2 ? reinterpret_cast<__nv_bfloat16 *>(a.out2) + o0 : nullptr;
 #pragma unroll 1
-                for (int c = 0; c < BN / 2; c += 32) {
+                for (int c = chalf * (BN / 4); c < (chalf + 1) * (BN / 4); c += 32) {
                     uint32_t g[32], u[32];
                     tmem_ld32(tbase + c, g);
                     tmem_ld32(tbase + BN / 2 + c, u);
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                           : nullptr;
                 if (a.out_bf16) {
 #pragma unroll 1
-                    for (int c = 0; c < a.bn; c += 64) {
+                    for (int c = chalf * (a.bn / 2); c < (chalf + 1) * (a.bn / 2); c += 64) {
                         uint32_t w[32];
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
@@ -467,7 +472,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 } else {
 #pragma unroll 1
-                    for (int c = 0; c < a.bn; c += 32) {
+                    for (int c = chalf * (a.bn / 2); c < (chalf + 1) * (a.bn / 2); c += 32) {
                         uint32_t v[32];
                         tmem_ld32(tbase + c, v);
                         tmem_wait_ld();
