@@ -130,6 +130,7 @@ __device__ __forceinline__ int collect_rows(int64_t *list, int n, int count, int
 }
 
 __global__ void __launch_bounds__(kCopyThreads) dispatch_copy_kernel(CopyArgs a) {
+    pdl_begin();   // after the previous kernel in the stream (programmatic launch)
     __shared__ int64_t dst[kWarpsPerBlock][kMaxDst];   // element offset of each target row
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (token, chunk)
@@ -219,6 +220,7 @@ __device__ __forceinline__ void st_group(void *base, int64_t elem, const float (
 
 template <bool BF16>
 __global__ void __launch_bounds__(kCopyThreads, 3) reduce_ranks_kernel(ReduceArgs a) {
+    pdl_begin();   // after the previous kernel in the stream (programmatic launch)
     constexpr int G = BF16 ? 8 : 4;   // elements per 16-byte group
     constexpr int U = BF16 ? 2 : 4;   // groups per lane and pick in flight (<= 85 registers)
     __shared__ int64_t src[kWarpsPerBlock][MOE_MAX_TOPK];
@@ -309,6 +311,7 @@ struct CombineArgs {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
+    pdl_begin();   // after the previous kernel in the stream (programmatic launch)
     __shared__ int64_t src[kWarpsPerBlock][MOE_MAX_WORLD > MOE_MAX_TOPK ? MOE_MAX_WORLD : MOE_MAX_TOPK];
     __shared__ float wt[kWarpsPerBlock][MOE_MAX_WORLD > MOE_MAX_TOPK ? MOE_MAX_WORLD : MOE_MAX_TOPK];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -432,6 +435,7 @@ struct QuantCopyArgs {
 };
 
 __global__ void __launch_bounds__(kCopyThreads) dispatch_quant_kernel(QuantCopyArgs a) {
+    pdl_begin();   // after the previous kernel in the stream (programmatic launch)
     __shared__ int64_t dst[kWarpsPerBlock][kMaxDst];   // row index of each target row
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (token, chunk)
@@ -576,8 +580,7 @@ cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream
     const int nchunk = (int)((p.H / 8 + 32 * kCopyU - 1) / (32 * kCopyU));
     CopyArgs a{x, r.recv_x, r.apick, r.slot, r.recv_row, r.pick_pos, r.recv_topk_idx, r.recv_topk_w,
                r.direct_row, r.direct_w, (int)p.T, (int)p.k, (int)p.W, (int)p.H, p.layout, nchunk, p.cap};
-    dispatch_copy_kernel<<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_copy_kernel, dim3(blocks_for(p.T * nchunk)), dim3(kCopyThreads), 0, s, a);
 }
 
 cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, bool skip_single, cudaStream_t s) {
@@ -601,9 +604,8 @@ cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, bool skip_si
     }
     int64_t blocks = blocks_for(p.W * p.cap);
     if (blocks > (int64_t)num_sms() * resident[bi]) blocks = (int64_t)num_sms() * resident[bi];
-    if (p.eo_bf16) reduce_ranks_kernel<true><<<(unsigned)blocks, kCopyThreads, 0, s>>>(a);
-    else reduce_ranks_kernel<false><<<(unsigned)blocks, kCopyThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    if (p.eo_bf16) return launch_pdl(reduce_ranks_kernel<true>, dim3((unsigned)blocks), dim3(kCopyThreads), 0, s, a);
+    return launch_pdl(reduce_ranks_kernel<false>, dim3((unsigned)blocks), dim3(kCopyThreads), 0, s, a);
 }
 
 cudaError_t launch_combine(const Routing &r, const void *expert_out, const float *topk_w,
@@ -613,9 +615,8 @@ cudaError_t launch_combine(const Routing &r, const void *expert_out, const float
     const int nchunk = (int)((p.H / 4 + 32 * kCopyU - 1) / (32 * kCopyU));
     CombineArgs a{expert_out, topk_w, r.slot, r.recv_row, out, (int)p.T, (int)p.k, (int)p.W,
                   (int)p.H, p.layout, nchunk, p.cap};
-    if (p.eo_bf16) combine_kernel<true><<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
-    else combine_kernel<false><<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    if (p.eo_bf16) return launch_pdl(combine_kernel<true>, dim3(blocks_for(p.T * nchunk)), dim3(kCopyThreads), 0, s, a);
+    return launch_pdl(combine_kernel<false>, dim3(blocks_for(p.T * nchunk)), dim3(kCopyThreads), 0, s, a);
 }
 
 cudaError_t launch_prepare_w1(const moe_geom &g, const uint16_t *w1, uint16_t *w1p,
@@ -633,8 +634,7 @@ cudaError_t launch_dispatch_quant(const Routing &r, const uint16_t *x, cudaStrea
     QuantCopyArgs a{x, reinterpret_cast<uint8_t *>(r.recv_x), r.recv_scales, reinterpret_cast<uint8_t *>(r.apick),
                     r.apick_scales, r.slot, r.recv_row, r.pick_pos, (int)p.T, (int)p.k, (int)p.W, (int)p.H,
                     p.layout, nchunk, p.cap, p.nrecv, p.P};
-    dispatch_quant_kernel<<<blocks_for(p.T * nchunk), kCopyThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_quant_kernel, dim3(blocks_for(p.T * nchunk)), dim3(kCopyThreads), 0, s, a);
 }
 
 cudaError_t launch_quantize_weights_fp8(const uint16_t *w, int64_t E, int64_t rows, int64_t cols,

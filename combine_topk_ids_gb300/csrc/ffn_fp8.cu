@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     ffn_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         F8Args a) {
     constexpr int F_STAGES = F8Smem<MODE>::kStages;
+    // the set-up below touches no global memory; pdl_wait() follows it
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -210,6 +211,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();   // the previous kernel in the stream has completed: its outputs are visible
     const int total = __ldg(a.mprefix + a.E) * a.nb;
     // GEMM2 stages 256-column tiles of at least three k-blocks: then a promotion warp that
     // stages a half is never two phases of that half's barrier ahead of the storing warps
@@ -492,8 +494,8 @@ int launch_gemm_fp8(const CUtensorMap &ma, const CUtensorMap &mb, const F8Args &
     if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
     int grid = num_sms();
     if ((int64_t)grid > max_tiles) grid = (int)max_tiles;
-    kernel<<<grid, F_THREADS, smem, s>>>(ma, mb, args);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return launch_pdl(kernel, dim3(grid), dim3(F_THREADS), smem, s, ma, mb, args) == cudaSuccess ? MOE_OK
+                                                                                            : MOE_ERR_CUDA;
 }
 
 bool make_map_u8(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows) {

@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __grid_constant__ CUtensorMap tmB, FfnArgs a) {
     using P = Pipe<HILO, PAIR, TALL>;
     constexpr int STAGES = P::kStages;
+    // the set-up below touches no global memory; pdl_wait() follows it
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (PAIR) cluster_sync();   // the peer's barriers exist before anyone signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();   // the previous kernel in the stream has completed: its outputs are visible
     const int total = __ldg(a.mprefix + a.E) * a.nb;
 
     if (warp == 0 && lane == 0) {
@@ -554,25 +556,28 @@ int launch_gemm(const CUtensorMap &ma, const CUtensorMap &ma2, const CUtensorMap
     if (!PAIR) {
         int grid = num_sms();
         if ((int64_t)grid > max_tiles) grid = (int)max_tiles;
-        kernel<<<grid, THREADS, smem, s>>>(ma, ma2, mb, args);
-        return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+        return launch_pdl(kernel, dim3(grid), dim3(THREADS), smem, s, ma, ma2, mb, args) == cudaSuccess
+                   ? MOE_OK
+                   : MOE_ERR_CUDA;
     }
     // persistent clusters of two CTAs: never more than can be resident at once
     int clusters = max_clusters > 0 ? max_clusters : num_sms() / 2;
     if ((int64_t)clusters > max_tiles) clusters = (int)max_tiles;
     if (clusters < 1) return MOE_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, ma, ma2, mb, args) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

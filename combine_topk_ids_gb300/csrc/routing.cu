@@ -95,6 +95,7 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 }
 
 __global__ void __launch_bounds__(kRouteThreads) route_count_kernel(RouteArgs a) {
+    pdl_begin();   // after the previous kernel in the stream (programmatic launch)
     extern __shared__ int sm[];
     int *hist = sm;          // [E]
     int *dhist = sm + a.E;   // [W]
@@ -176,6 +177,7 @@ __device__ __forceinline__ int scan_row(const RouteArgs &a, const int32_t *hist,
 }
 
 __global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
+    pdl_begin();   // after the previous kernel in the stream (programmatic launch)
     __shared__ int wsum[3][32];
     __shared__ int carry[3];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -246,6 +248,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a) {
 }
 
 __global__ void __launch_bounds__(kRouteThreads) route_assign_kernel(RouteArgs a) {
+    pdl_begin();   // after the previous kernel in the stream (programmatic launch)
     extern __shared__ int sm[];
     int *cur = sm;                          // [warps][E] running position inside expert
     int *dcur = sm + kRouteWarps * a.E;     // [warps][W] running row inside destination
@@ -404,6 +407,7 @@ __device__ __forceinline__ void block_excl_scan3(const int (&v)[3], int (&ex)[3]
 }
 
 __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a) {
+    pdl_begin();   // after the previous kernel in the stream (programmatic launch)
     extern __shared__ int sm[];
     __shared__ int wsum[3][32];
     const int E = a.E, W = a.W;
@@ -635,23 +639,23 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf);
             if (e != cudaSuccess) return e;
         }
-        route_fused_kernel<<<1, kFusedThreads, smf, s>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(route_fused_kernel, dim3(1), dim3(kFusedThreads), smf, s, a);
     }
 
     // several blocks may raise status bits: clear the word before the first of them runs
     if (cudaMemsetAsync(a.status, 0, sizeof(int32_t), s) != cudaSuccess) return cudaGetLastError();
     size_t sm1 = (size_t)(a.E + a.W) * sizeof(int);
-    route_count_kernel<<<a.nb, kRouteThreads, sm1, s>>>(a);
-    route_scan_kernel<<<1, 1024, 0, s>>>(a);
+    cudaError_t e = launch_pdl(route_count_kernel, dim3(a.nb), dim3(kRouteThreads), sm1, s, a);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, a);
+    if (e != cudaSuccess) return e;
     size_t sm3 = (size_t)kRouteWarps * (a.E + a.W) * sizeof(int);
     if (sm3 > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(route_assign_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3);
         if (e != cudaSuccess) return e;
     }
-    route_assign_kernel<<<a.nb, kRouteThreads, sm3, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(route_assign_kernel, dim3(a.nb), dim3(kRouteThreads), sm3, s, a);
 }
 
 }  // namespace moe
