@@ -186,7 +186,9 @@ def moe_combine(h, expert_out, topk_weights, out, stream=None):
 
 def moe_forward_host(g, x_host, ids_host, w_host, out_host, x_dev, ids_dev, w_dev, out_dev,
                      w1_prepared, w2, expert_out, workspace, handle, stream=None):
-    """The whole layer from host buffers (pinned torch CPU tensors), one C call."""
+    """The whole layer from host buffers (torch CPU tensors), one C call.  With pinned
+    (page-locked) host tensors the kernels read and write them directly and the device
+    staging tensors may be None; otherwise they stage the copies."""
     _check(lib().moe_forward_host(
         ctypes.byref(g), _ptr(x_host), _ptr(ids_host), _ids_dtype(ids_host), _ptr(w_host),
         _ptr(out_host), _ptr(x_dev), _ptr(ids_dev), _ptr(w_dev), _ptr(out_dev), _ptr(w1_prepared),

@@ -161,6 +161,16 @@ inline void record(const moe_handle *h, int slot, cudaStream_t s) {
         cudaEventRecord(static_cast<cudaEvent_t>(h->events[slot]), s);
 }
 
+// Device address of a page-locked host buffer, or NULL for any other pointer.
+const void *mapped_host(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();   // clear the error of an unknown pointer
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 int handle_plan(const moe_handle *h, Plan *p) {
     if (!h || h->magic != kHandleMagic || !h->workspace) return MOE_ERR_BAD_HANDLE;
     int rc = make_plan(h->geom, p);
@@ -405,10 +415,27 @@ int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids
     if (rc != MOE_OK) return rc;
     if (p.quant != MOE_QUANT_NONE) return MOE_ERR_INVALID_ARGUMENT;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.T > 0 && (!x_host || !topk_ids_host || !topk_weights_host || !out_host))
+        return MOE_ERR_INVALID_ARGUMENT;
+    // Page-locked host buffers are addressable by the kernels (one address space, and on
+    // GB300 a coherent NVLink-C2C link to the Grace memory): the row scatter and the
+    // routing then read the batch straight from host memory and the combine writes the
+    // result straight into it, instead of staging copies through the device buffers.
     if (p.T > 0) {
-        if (!x_host || !topk_ids_host || !topk_weights_host || !out_host || !x_dev ||
-            !topk_ids_dev || !topk_weights_dev)
-            return MOE_ERR_INVALID_ARGUMENT;
+        const void *xm = mapped_host(x_host), *im = mapped_host(topk_ids_host),
+                   *wm = mapped_host(topk_weights_host);
+        void *om = const_cast<void *>(mapped_host(out_host));
+        if (xm && im && wm && om && aligned(xm, 16) && aligned(om, 16) &&
+            aligned(im, ids_dtype == MOE_IDS_INT64 ? 8 : 4) && aligned(wm, 4)) {
+            int rc2 = moe_dispatch(g, xm, im, ids_dtype, static_cast<const float *>(wm), nullptr, workspace_dev,
+                                   workspace_bytes, h, stream);
+            if (rc2 == MOE_OK) rc2 = moe_expert_ffn(h, w1_prepared_dev, w2_dev, expert_out_dev, stream);
+            if (rc2 == MOE_OK) rc2 = moe_combine(h, expert_out_dev, static_cast<const float *>(wm), om, stream);
+            return rc2;
+        }
+    }
+    if (p.T > 0) {
+        if (!x_dev || !topk_ids_dev || !topk_weights_dev) return MOE_ERR_INVALID_ARGUMENT;
         const size_t xb = (size_t)p.T * p.H * 2, pb = (size_t)p.P;
         if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
             cudaMemcpyAsync(topk_ids_dev, topk_ids_host, pb * (ids_dtype == MOE_IDS_INT64 ? 8 : 4),

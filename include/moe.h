@@ -338,14 +338,17 @@ int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
 
 /*
  * moe_forward_host - the whole layer end to end from HOST buffers, on one stream:
- * copy x_host / topk_ids_host / topk_weights_host into the caller's device buffers
- * (x_dev, topk_ids_dev, topk_weights_dev, same shapes as in moe_dispatch), then
- * moe_dispatch (all ranks active) -> moe_expert_ffn -> moe_combine into out_dev, then copy out_dev to
- * out_host (bf16 [T, H]).  bf16 geometries only (MOE_ERR_INVALID_ARGUMENT for FP8).
- * Asynchronous like the other calls: out_host is valid once the
- * stream has been synchronised.  Host buffers should be page-locked for the copies to
- * overlap; pageable memory works but the copies then synchronise.  Returns the first
- * error of the sequence.
+ * moe_dispatch (all ranks active) -> moe_expert_ffn -> moe_combine of x_host /
+ * topk_ids_host / topk_weights_host (same shapes as in moe_dispatch) into out_host (bf16
+ * [T, H]).  When all four host buffers are page-locked (cudaHostAlloc / registered), the
+ * kernels read the inputs from host memory and the combine writes out_host directly
+ * (over NVLink-C2C on GB300); x_dev, topk_ids_dev, topk_weights_dev and out_dev are then
+ * not used and may be NULL.  Otherwise the inputs are copied into those device buffers
+ * first and out_dev is copied to out_host last (the copies of pageable memory
+ * synchronise).  bf16 geometries only (MOE_ERR_INVALID_ARGUMENT for FP8).  Asynchronous
+ * like the other calls: out_host is valid once the stream has been synchronised; the
+ * host inputs must stay unchanged until then.  Returns the first error of the
+ * sequence.
  */
 int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids_host,
                      int ids_dtype, const float *topk_weights_host, void *out_host,
