@@ -5,7 +5,7 @@ import torch
 import combine_topk_ids_gb300 as moe
 import oracle
 
-# spec tolerance on floating outputs: |d| <= 2e-2 * |ref| + 1e-3, elementwise
+# output tolerance on floating outputs: |d| <= 2e-2 * |ref| + 1e-3, elementwise
 RTOL, ATOL = 2e-2, 1e-3
 
 

@@ -6,7 +6,7 @@ rounding can land on the other side of a bf16 tie: each held bf16 value may diff
 bf16 ulp beyond the plain tolerance.  The checks: routing bit-exact; expert_out rows within
 |d| <= 2e-2 |ref| + 1e-3 + the ulps of the roundings that produced the row; out within the
 same bound carried through the routing weights.  The fraction of outputs that fall outside
-the plain spec bound against the full-precision (float32 expert_out) oracle is the
+the plain output bound (|d| <= 2e-2*|ref| + 1e-3) against the full-precision (float32 expert_out) oracle is the
 cost of the option; it is checked to stay small and printed."""
 import numpy as np
 import pytest
@@ -95,7 +95,7 @@ def test_bf16_expert_out_parity(name):
     # the option's cost against the full-precision expert_out oracle
     _, out_full = oracle.layer(g, case.x_bits, case.ids_np, case.w_np, case.w1_host, case.w2_host)
     fail = float((np.abs(got_out - out_full) > RTOL * np.abs(out_full) + ATOL + allow).mean())
-    print("%s: fraction of outputs outside the north-star bound vs the float32 expert_out "
+    print("%s: fraction of outputs outside the output bound vs the float32 expert_out "
           "oracle: %.2e" % (name, fail))
     assert fail < 2e-2
 
