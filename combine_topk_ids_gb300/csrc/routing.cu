@@ -142,12 +142,21 @@ __device__ __forceinline__ int scan_row(const RouteArgs &a, const int32_t *hist,
                                         bool restart_per_rank, RankFn on_rank) {
     const int lane = threadIdx.x & 31;
     int run = 0;
-    for (int b0 = 0; b0 < a.nb; b0 += 32) {
-        const int b = b0 + lane;
-        const int v = b < a.nb ? hist[b] : 0;
-        const int incl = warp_incl_scan(v);
-        if (b < a.nb) base[b] = run + incl - v;
-        run += __shfl_sync(kFull, incl, 31);
+    // 256 chunks per round: all eight loads are issued before the first scan step
+    for (int b00 = 0; b00 < a.nb; b00 += 256) {
+        int v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int b = b00 + 32 * i + lane;
+            v[i] = b < a.nb ? hist[b] : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int b = b00 + 32 * i + lane;
+            const int incl = warp_incl_scan(v[i]);
+            if (b < a.nb) base[b] = run + incl - v[i];
+            run += __shfl_sync(kFull, incl, 31);
+        }
     }
     __syncwarp();
     // per-rank begin (= exclusive prefix at the rank's first block) and count
