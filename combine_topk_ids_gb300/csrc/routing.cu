@@ -606,11 +606,12 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a)
 }  // namespace
 
 #ifndef MOE_FUSED_ROUTING_MAX_PICKS
-#define MOE_FUSED_ROUTING_MAX_PICKS 16384
+#define MOE_FUSED_ROUTING_MAX_PICKS 3072
 #endif
-// The single-CTA path wins for few experts (one launch instead of three: 10 vs ~15 us on
-// the 8-expert decode batch) and loses for many (82 vs 36 us with 256 experts, where its
-// per-expert work runs on one SM), so it is kept for E <= 64.
+// The single-CTA path wins for small batches over few experts (one launch instead of
+// three: 9-12 vs 14-15 us for 128-2048 picks) and loses for larger ones (44.6 vs 15.9 us
+// on 16384 picks over 16 experts; 82 vs 36 us with 256 experts, where its per-expert work
+// runs on one SM), so it is kept for at most 3072 picks and E <= 64.
 int routing_launches(const Plan &p) {
     return (p.P <= MOE_FUSED_ROUTING_MAX_PICKS && p.E <= 64 && p.E * p.W <= 4096) ? 1 : 3;
 }

@@ -99,7 +99,7 @@ SMALL.update({
                            layout="FLAT", algo="HT", routing="uniform", T=1100),
 })
 
-# Batches above the single-CTA routing limit (16384 picks), which take the three-kernel
+# Batches of more than 16384 picks, far above the single-CTA routing limit, which take the three-kernel
 # multi-block routing path; narrow H and I keep the oracle fast.
 SMALL.update({
     "blocks_em": MoeConfig("blocks_em", W=4, Tr=1100, H=256, E=16, k=4, I=128,
@@ -130,6 +130,10 @@ PROFILE = {
     # 384 rows per expert: the 128-row tiles of the Mixtral-like decode workload
     "ncu_em_mid": MoeConfig("ncu_em_mid", W=4, Tr=192, H=4096, E=4, k=2, I=7168,
                             layout="EM", algo="LL", routing="uniform"),
+    # >= 192 rows per expert with K, N <= 2048: the two-SM (cta_group::2) tiles of the
+    # ragged workload; weights 201 MB, about 1.3 GB on the device
+    "ncu_pair_small": MoeConfig("ncu_pair_small", W=4, Tr=1024, H=2048, E=16, k=4, I=1024,
+                                layout="EM", algo="LL", routing="dirichlet"),
     "ncu_flat_small": MoeConfig("ncu_flat_small", W=8, Tr=512, H=7168, E=32, k=8, I=2048,
                                 layout="FLAT", algo="HT", routing="uniform"),
 }

@@ -393,7 +393,7 @@ int moe_route_noalloc(const moe_geom *g, const void *topk_ids_dev, int ids_dtype
 
 /*
  * moe_launches_per_layer - number of kernels one moe_dispatch + moe_expert_ffn +
- * moe_combine of geometry *g queues (routing is one kernel for batches of at most 16384
+ * moe_combine of geometry *g queues (routing is one kernel for batches of at most 3072
  * picks over at most 64 experts and three otherwise; RANK_MAJOR / FLAT add the
  * local-pick reduction).  Written to *n.
  */

@@ -39,7 +39,7 @@ SMALL_CASES = {
     "tall_flat": gen.SMALL["tall_flat"],
     "tall_flat_h4096": gen.SMALL["tall_flat"].with_(H=4096, I=512, seed=17),
     "tall_em_masked_i32": gen.SMALL["tall_em"].with_(mask_frac=0.2, ids_dtype="int32", seed=16),
-    # multi-block routing (more than 16384 picks)
+    # multi-block routing (more than 3072 picks; these hold more than 16384)
     "blocks_em": gen.SMALL["blocks_em"],
     "blocks_rm": gen.SMALL["blocks_rm"],
     "blocks_flat": gen.SMALL["blocks_flat"],
