@@ -13,6 +13,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -592,18 +594,21 @@ cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, bool skip_si
                  nchunk, p.cap};
     // grid-stride over rows: no more blocks than can be resident at once, so that no block
     // starts its rows after the others have finished theirs
-    static int resident[2] = {0, 0};
+    // (the kernels' occupancy depends on the architecture only; cached once per variant)
+    static std::atomic<int> resident[2] = {{0}, {0}};
     const int bi = p.eo_bf16 ? 1 : 0;
-    if (resident[bi] == 0) {
+    int per_sm = resident[bi].load(std::memory_order_relaxed);
+    if (per_sm == 0) {
         int nb = 0;
         const cudaError_t e = p.eo_bf16
             ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, reduce_ranks_kernel<true>, kCopyThreads, 0)
             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, reduce_ranks_kernel<false>, kCopyThreads, 0);
         if (e != cudaSuccess) return e;
-        resident[bi] = nb > 0 ? nb : 1;
+        per_sm = nb > 0 ? nb : 1;
+        resident[bi].store(per_sm, std::memory_order_relaxed);
     }
     int64_t blocks = blocks_for(p.W * p.cap);
-    if (blocks > (int64_t)num_sms() * resident[bi]) blocks = (int64_t)num_sms() * resident[bi];
+    if (blocks > (int64_t)num_sms() * per_sm) blocks = (int64_t)num_sms() * per_sm;
     if (p.eo_bf16) return launch_pdl(reduce_ranks_kernel<true>, dim3((unsigned)blocks), dim3(kCopyThreads), 0, s, a);
     return launch_pdl(reduce_ranks_kernel<false>, dim3((unsigned)blocks), dim3(kCopyThreads), 0, s, a);
 }
