@@ -12,7 +12,8 @@
 //
 // One persistent kernel per GEMM, one CTA per SM, 384 threads:
 //   warp 0      TMA producer: 128x64 A tile(s) + 256x64 B tile per stage (SWIZZLE_128B),
-//               a 4-stage (GEMM1) or 3-stage (GEMM2: A_hi, A_lo, B) mbarrier ring
+//               a 192 KB mbarrier ring: 4 stages of 48 KB (128-row tiles), 3 of 64 KB
+//               (256-row tiles, or the bf16-pair A operand), 6 of 32 KB (two-SM tiles)
 //   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16, M=128,
 //               N=256, K=16, bf16 x bf16 -> fp32 into one of two 256-column TMEM
 //               accumulators, tcgen05.commit frees smem stages and hands tiles over
