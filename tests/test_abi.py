@@ -114,3 +114,16 @@ def test_calls_reject_an_unfilled_handle(lib):
     assert lib.moe_combine(ctypes.byref(h), p, p, p, None) == -10
     v = ctypes.c_int32()
     assert lib.moe_get_status(ctypes.byref(h), ctypes.byref(v), None) == -10
+
+
+@pytest.mark.parametrize("W,Tr,T,E,k,layout,want", [
+    (2, 32, 64, 8, 2, "EM", 5),          # 128 picks, 8 experts: one routing CTA
+    (8, 128, 1024, 8, 2, "EM", 5),       # 2048 picks
+    (4, 1024, 4096, 16, 4, "EM", 7),     # 16384 picks: three routing kernels
+    (8, 128, 1024, 256, 8, "RM", 8),     # 256 experts: three routing kernels, plus the reduction
+    (4, 96, 350, 16, 4, "FLAT", 6),      # 1400 picks: one routing CTA, plus the reduction
+])
+def test_launches_per_layer(lib, W, Tr, T, E, k, layout, want):
+    # routing (1 or 3), row scatter, GEMM1, GEMM2, RANK_MAJOR / FLAT reduction, combine
+    g = moe.make_geom(W, Tr, T, 512, E, k, 256, layout, "LL")
+    assert moe.moe_launches_per_layer(g) == want
