@@ -43,6 +43,16 @@ SMALL_CASES = {
     "blocks_em": gen.SMALL["blocks_em"],
     "blocks_rm": gen.SMALL["blocks_rm"],
     "blocks_flat": gen.SMALL["blocks_flat"],
+    # limits: top_k = 32 (every lane of the warp-level routing busy), world = 64 (64-bit
+    # destination masks, ranks lane and lane + 32 in the scans), one local expert per rank
+    "topk32_em": gen.MoeConfig("topk32_em", W=2, Tr=32, H=256, E=64, k=32, I=128,
+                               layout="EM", algo="LL", routing="uniform", T=64),
+    "topk32_flat": gen.MoeConfig("topk32_flat", W=4, Tr=16, H=256, E=64, k=32, I=128,
+                                 layout="FLAT", algo="HT", routing="uniform", T=64),
+    "world64_rm": gen.MoeConfig("world64_rm", W=64, Tr=4, H=256, E=64, k=4, I=128,
+                                layout="RM", algo="LL", routing="zipf", T=250),
+    "world64_flat": gen.MoeConfig("world64_flat", W=64, Tr=4, H=256, E=128, k=4, I=128,
+                                  layout="FLAT", algo="HT", routing="uniform", T=256),
     # the bf16-pair activation (hi + lo operand of the second GEMM)
     "actpair_em": gen.SMALL["small_em"].with_(act="pair", seed=13),
     "actpair_rm_h384": gen.SMALL["small_rm"].with_(act="pair", H=384, seed=14),
@@ -199,4 +209,21 @@ def test_expert_major_region_overflow():
     rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
     assert rt["n_over"] > 0
     check_routing(layer, rt, cfg)
+    check_out(layer, case)
+
+
+@pytest.mark.parametrize("layout,T", [("EM", 350), ("EM", 256), ("FLAT", 350)])
+def test_every_pick_on_one_expert(layout, T):
+    """All tokens pick expert 2 (top-1): one expert holds every row (several full 128-row
+    blocks, or an exact multiple of 128), the others none, so most experts issue no tiles."""
+    cfg = gen.MoeConfig("onehot", W=2, Tr=200, H=512, E=4, k=1, I=384, layout=layout,
+                        algo="LL", routing="uniform", T=T)
+    ids = np.full((T, 1), 2, np.int64)
+    case = make_case(cfg, "cuda", ids_override=ids)
+    layer = run_layer(case)
+    assert layer.status() == 0
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    check_routing(layer, rt, cfg)
+    check_dispatch_rows(layer, rt, case)
+    check_expert_out(layer, rt, case)
     check_out(layer, case)
