@@ -27,6 +27,8 @@ CASES = {
     "eo16_pair_flat": gen.SMALL["pair_flat"],
     "eo16_tall_rm_h384": gen.SMALL["tall_rm"],
     "eo16_small_flat_k1": gen.SMALL["small_flat"].with_(k=1, seed=20),
+    "eo16_world64_flat": gen.MoeConfig("eo16_world64_flat", W=64, Tr=4, H=256, E=128, k=4, I=128,
+                                       layout="FLAT", algo="HT", routing="uniform", T=256),
     "eo16_small_em_h384": gen.SMALL["small_em"].with_(H=384, seed=6),
     "eo16_blocks_rm": gen.SMALL["blocks_rm"],
 }

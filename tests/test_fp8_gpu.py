@@ -32,6 +32,11 @@ CASES = {
     # 128-column tiles; many routing blocks
     "f8_blocks_flat": gen.SMALL["blocks_flat"].with_(quant="fp8"),
     "f8_pair_rm": gen.SMALL["pair_rm"].with_(quant="fp8"),
+    # limits: top_k 32 and world 64 (the row scatter writes up to 64 + 32 destinations)
+    "f8_topk32_flat": gen.MoeConfig("f8_topk32_flat", W=4, Tr=16, H=256, E=64, k=32, I=128,
+                                    layout="FLAT", algo="HT", routing="uniform", T=64, quant="fp8"),
+    "f8_world64_rm": gen.MoeConfig("f8_world64_rm", W=64, Tr=4, H=256, E=64, k=4, I=128,
+                                   layout="RM", algo="LL", routing="zipf", T=250, quant="fp8"),
 }
 
 
