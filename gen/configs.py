@@ -119,7 +119,21 @@ EO16 = {name + "_eo16": cfg.with_(name=name + "_eo16", expert_out="bf16") for na
 # The same workloads with the bf16-pair activation (hi + lo operand of the second GEMM).
 ACTPAIR = {name + "_actpair": cfg.with_(name=name + "_actpair", act="pair") for name, cfg in CONFIGS.items()}
 
-ALL = {**CONFIGS, **SMALL, **FP8, **EO16, **ACTPAIR}
+# The shapes of the FlashInfer MoE-EP page's accuracy check ("MoE-EP implementation &
+# usage", section 4 "Usage walkthrough" and section 5 "Correctness status"): 16 experts,
+# top-8, hidden 8192, intermediate 2048, world 8; 128 tokens per rank for the two LL
+# layouts, 4096 for HT FLAT.  The page does not state the routing; uniform distinct top-k
+# is the plainest reading.  H = 8192 is the widest hidden of any test shape.
+ACCURACY = {
+    "fi_ll_em": MoeConfig("fi_ll_em", W=8, Tr=128, H=8192, E=16, k=8, I=2048,
+                          layout="EM", algo="LL", routing="uniform"),
+    "fi_ll_rm": MoeConfig("fi_ll_rm", W=8, Tr=128, H=8192, E=16, k=8, I=2048,
+                          layout="RM", algo="LL", routing="uniform"),
+    "fi_ht_flat": MoeConfig("fi_ht_flat", W=8, Tr=4096, H=8192, E=16, k=8, I=2048,
+                            layout="FLAT", algo="HT", routing="uniform"),
+}
+
+ALL = {**CONFIGS, **SMALL, **FP8, **EO16, **ACTPAIR, **ACCURACY}
 
 # Smaller cases for detailed (multi-pass) profiler captures of the same kernels: 4
 # experts, weights 0.7 GB (larger than L2), about 1.3 GB on the device.  ncu_em_small
