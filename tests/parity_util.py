@@ -95,7 +95,11 @@ def act_flip_allowance(layer, rt, case, picks):
     allow, n_bad, n_flip = oracle.bf16_act_allowance(geom_dict(cfg), rt, case.x_bits, case.w1_host,
                                                      case.w2_host, picks, gpu)
     assert n_bad == 0, "%d activation codes outside the oracle's band" % n_bad
-    assert n_flip <= 0.02 * len(picks) * cfg.I, "%d of %d activation codes differ" % (n_flip, len(picks) * cfg.I)
+    # a guard on how many codes may sit on the other side of a midpoint: 2% up to a
+    # 16384-long first-GEMM K loop, then in proportion to K (the tensor-core sum's distance
+    # from the exact sum grows with the number of terms it accumulates)
+    cap = 0.02 * max(1.0, cfg.H / 16384.0)
+    assert n_flip <= cap * len(picks) * cfg.I, "%d of %d activation codes differ" % (n_flip, len(picks) * cfg.I)
     return allow
 
 

@@ -53,6 +53,12 @@ SMALL_CASES = {
                                 layout="RM", algo="LL", routing="zipf", T=250),
     "world64_flat": gen.MoeConfig("world64_flat", W=64, Tr=4, H=256, E=128, k=4, I=128,
                                   layout="FLAT", algo="HT", routing="uniform", T=256),
+    # the widest hidden the library accepts (MOE_MAX_HIDDEN = 65536): a 65536-long K loop
+    # in the first GEMM (1024 k-blocks), 256 n-tiles in the second, 64 copy chunks per row
+    "hmax_em": gen.MoeConfig("hmax_em", W=2, Tr=8, H=65536, E=4, k=2, I=128,
+                             layout="EM", algo="LL", routing="uniform", T=13),
+    "hmax_flat": gen.MoeConfig("hmax_flat", W=2, Tr=8, H=65536, E=4, k=2, I=128,
+                               layout="FLAT", algo="HT", routing="uniform", T=13),
     # the bf16-pair activation (hi + lo operand of the second GEMM)
     "actpair_em": gen.SMALL["small_em"].with_(act="pair", seed=13),
     "actpair_rm_h384": gen.SMALL["small_rm"].with_(act="pair", H=384, seed=14),
