@@ -236,6 +236,25 @@ def handle_view(h: MoeHandle, workspace, field: str, shape, dtype):
     return workspace.view(torch.uint8)[off:off + nbytes].view(dtype).view(*shape)
 
 
+def _require(t, name, dtypes, shape, device):
+    """Raise before any library call if `t` is not a contiguous tensor of one of `dtypes`
+    and of `shape`, on `device` or in page-locked host memory (which the kernels read over
+    the host link): the C ABI takes bare pointers and would read any other layout wrongly."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s: expected a torch.Tensor, got %s" % (name, type(t).__name__))
+    if t.dtype not in dtypes:
+        raise TypeError("%s: dtype %s, expected %s" % (name, t.dtype, " or ".join(str(d) for d in dtypes)))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s: shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    same = t.device.type == device.type and (device.index is None or t.device.index is None or
+                                              t.device.index == device.index)
+    if not same and not (t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError("%s is on %s; expected %s or page-locked host memory" % (name, t.device, device))
+
+
 class MoELayer1GPU:
     """One MoE EP layer of a fixed geometry with its buffers on the current CUDA device.
 
@@ -296,6 +315,10 @@ class MoELayer1GPU:
     def set_weights(self, w1, w2):
         """bf16 w1 [E, 2I, H] and w2 [E, H, I]; prepared (FP8: quantised) once here."""
         import torch
+        g = self.geom
+        E, H, I = g.num_experts, g.hidden, g.intermediate
+        _require(w1, "w1", (torch.bfloat16,), (E, 2 * I, H), self.device)
+        _require(w2, "w2", (torch.bfloat16,), (E, H, I), self.device)
         if self.quant == "fp8":
             E, I2, H = w1.shape
             dev = w1.device
@@ -309,12 +332,25 @@ class MoELayer1GPU:
         moe_prepare_weights(self.geom, w1, self.w1p)
         self.w2 = w2
 
+    def _check_routing(self, topk_ids, topk_weights):
+        import torch
+        T, k = self.geom.num_tokens, self.geom.top_k
+        _require(topk_ids, "topk_ids", (torch.int64, torch.int32), (T, k), self.device)
+        _require(topk_weights, "topk_weights", (torch.float32,), (T, k), self.device)
+
     def dispatch(self, x, topk_ids, topk_weights, active_ranks=None):
+        import torch
+        _require(x, "x", (torch.bfloat16,), (self.geom.num_tokens, self.geom.hidden), self.device)
+        self._check_routing(topk_ids, topk_weights)
+        if active_ranks is not None:
+            _require(active_ranks, "active_ranks", (torch.int32,), (self.geom.world,), self.device)
         moe_dispatch(self.geom, x, topk_ids, topk_weights, self.workspace, handle=self.handle,
                      active_ranks=active_ranks)
         return self.handle
 
     def expert_ffn(self):
+        if self.w1p is None:
+            raise RuntimeError("set_weights() has not been called")
         if self.quant == "fp8":
             moe_expert_ffn_fp8(self.handle, self.w1p, self.w1s, self.w2, self.w2s, self.expert_out)
         else:
@@ -322,6 +358,9 @@ class MoELayer1GPU:
         return self.expert_out
 
     def combine(self, topk_weights):
+        import torch
+        _require(topk_weights, "topk_weights", (torch.float32,),
+                 (self.geom.num_tokens, self.geom.top_k), self.device)
         moe_combine(self.handle, self.expert_out, topk_weights, self.out)
         return self.out
 

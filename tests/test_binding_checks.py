@@ -1,0 +1,76 @@
+"""The Python layer object checks every tensor it hands to the C ABI (dtype, shape,
+contiguity, device) and raises before any library call; the C ABI takes bare pointers.
+CPU only: the layer's buffers live in host memory here, so a call that passes the checks
+reaches the library, which then refuses to launch without a GB300."""
+import pytest
+import torch
+
+import combine_topk_ids_gb300 as moe
+
+W, Tr, T, H, E, k, I = 2, 8, 12, 256, 4, 2, 128
+
+
+@pytest.fixture(scope="module")
+def layer():
+    try:
+        moe.lib()
+    except RuntimeError:
+        moe.build()
+    return moe.MoELayer1GPU(W, Tr, T, H, E, k, I, "EM", "LL", device="cpu")
+
+
+def good():
+    return (torch.zeros((T, H), dtype=torch.bfloat16), torch.zeros((T, k), dtype=torch.int64),
+            torch.zeros((T, k), dtype=torch.float32))
+
+
+@pytest.mark.parametrize("which,bad,err", [
+    (0, lambda: torch.zeros((T, H), dtype=torch.float32), TypeError),           # x not bf16
+    (0, lambda: torch.zeros((T, H + 128), dtype=torch.bfloat16), ValueError),   # x of another width
+    (0, lambda: torch.zeros((H, T), dtype=torch.bfloat16).t(), ValueError),     # x not contiguous
+    (1, lambda: torch.zeros((T, k), dtype=torch.int16), TypeError),             # ids int16
+    (1, lambda: torch.zeros((T, k + 1), dtype=torch.int64), ValueError),        # ids of another top_k
+    (2, lambda: torch.zeros((T, k), dtype=torch.float64), TypeError),           # weights float64
+    (2, lambda: [[0.5] * k] * T, TypeError),                                    # not a tensor
+])
+def test_forward_rejects_bad_inputs(layer, which, bad, err):
+    args = list(good())
+    args[which] = bad()
+    with pytest.raises(err):
+        layer.forward(*args)
+
+
+def test_active_ranks_checked(layer):
+    with pytest.raises(ValueError):
+        layer.dispatch(*good(), active_ranks=torch.ones(W + 1, dtype=torch.int32))
+    with pytest.raises(TypeError):
+        layer.dispatch(*good(), active_ranks=torch.ones(W, dtype=torch.int64))
+
+
+def test_set_weights_checks_shapes_and_dtypes(layer):
+    w1 = torch.zeros((E, 2 * I, H), dtype=torch.bfloat16)
+    w2 = torch.zeros((E, H, I), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        layer.set_weights(w1, torch.zeros((E, I, H), dtype=torch.bfloat16))   # w2 transposed
+    with pytest.raises(TypeError):
+        layer.set_weights(w1.float(), w2)
+    with pytest.raises(ValueError):
+        layer.set_weights(torch.zeros((E, 2 * I, H), dtype=torch.bfloat16)[:, ::2], w2)
+
+
+def test_combine_checks_weights(layer):
+    with pytest.raises(ValueError):
+        layer.combine(torch.zeros((T + 1, k), dtype=torch.float32))
+
+
+def test_expert_ffn_requires_weights():
+    fresh = moe.MoELayer1GPU(W, Tr, T, H, E, k, I, "EM", "LL", device="cpu")
+    with pytest.raises(RuntimeError, match="set_weights"):
+        fresh.expert_ffn()
+
+
+def test_valid_inputs_pass_the_checks(layer):
+    # the checks pass; what stops the call here is the missing GPU (no CUDA stream on this
+    # host, or the library's MoeError on a host without a GB300), not a TypeError/ValueError
+    with pytest.raises(RuntimeError):
+        layer.dispatch(*good())
