@@ -189,6 +189,19 @@ def moe_forward_host(g, x_host, ids_host, w_host, out_host, x_dev, ids_dev, w_de
     """The whole layer from host buffers (torch CPU tensors), one C call.  With pinned
     (page-locked) host tensors the kernels read and write them directly and the device
     staging tensors may be None; otherwise they stage the copies."""
+    import torch
+    T, H, k = g.num_tokens, g.hidden, g.top_k
+    cpu, cuda = torch.device("cpu"), torch.device("cuda")
+    for t, name, dts, shape, dev in ((x_host, "x_host", (torch.bfloat16,), (T, H), cpu),
+                                     (ids_host, "ids_host", (torch.int64, torch.int32), (T, k), cpu),
+                                     (w_host, "w_host", (torch.float32,), (T, k), cpu),
+                                     (out_host, "out_host", (torch.bfloat16,), (T, H), cpu),
+                                     (x_dev, "x_dev", (torch.bfloat16,), (T, H), cuda),
+                                     (ids_dev, "ids_dev", (getattr(ids_host, "dtype", torch.int64),), (T, k), cuda),
+                                     (w_dev, "w_dev", (torch.float32,), (T, k), cuda),
+                                     (out_dev, "out_dev", (torch.bfloat16,), (T, H), cuda)):
+        if t is not None or dev is cpu:
+            _require(t, name, dts, shape, dev)
     _check(lib().moe_forward_host(
         ctypes.byref(g), _ptr(x_host), _ptr(ids_host), _ids_dtype(ids_host), _ptr(w_host),
         _ptr(out_host), _ptr(x_dev), _ptr(ids_dev), _ptr(w_dev), _ptr(out_dev), _ptr(w1_prepared),

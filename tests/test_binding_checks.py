@@ -74,3 +74,18 @@ def test_valid_inputs_pass_the_checks(layer):
     # host, or the library's MoeError on a host without a GB300), not a TypeError/ValueError
     with pytest.raises(RuntimeError):
         layer.dispatch(*good())
+
+
+def test_forward_host_checks_host_and_staging_tensors(layer):
+    x, ids, w = good()
+    out = torch.zeros((T, H), dtype=torch.bfloat16)
+    rest = (layer.w1p, layer.w2, layer.expert_out, layer.workspace, moe.MoeHandle())
+    with pytest.raises(TypeError):   # float32 rows
+        moe.moe_forward_host(layer.geom, x.float(), ids, w, out, None, None, None, None, *rest)
+    with pytest.raises(ValueError):  # output of another width
+        moe.moe_forward_host(layer.geom, x, ids, w, out[:, :128], None, None, None, None, *rest)
+    with pytest.raises(ValueError):  # a staging tensor of the wrong shape
+        moe.moe_forward_host(layer.geom, x, ids, w, out, torch.zeros((T + 1, H), dtype=torch.bfloat16),
+                             None, None, None, *rest)
+    with pytest.raises(TypeError):   # ids missing
+        moe.moe_forward_host(layer.geom, x, None, w, out, None, None, None, None, *rest)
