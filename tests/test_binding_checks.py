@@ -89,3 +89,28 @@ def test_forward_host_checks_host_and_staging_tensors(layer):
                              None, None, None, *rest)
     with pytest.raises(TypeError):   # ids missing
         moe.moe_forward_host(layer.geom, x, None, w, out, None, None, None, None, *rest)
+
+
+def _cases():
+    import gen
+    names = list(gen.SMALL) + ["tiny_ll_em"]
+    cfgs = [gen.ALL[n] for n in names]
+    cfgs += [gen.SMALL["small_em"].with_(quant="fp8"), gen.SMALL["small_flat"].with_(expert_out="bf16"),
+             gen.SMALL["small_rm"].with_(act="pair"), gen.SMALL["small_em"].with_(ids_dtype="int32", mask_frac=0.3)]
+    return cfgs
+
+
+@pytest.mark.parametrize("cfg", _cases(), ids=lambda c: "%s-%s-%s-%s" % (c.name, c.quant, c.expert_out, c.act))
+def test_checks_accept_what_the_gpu_tests_pass(cfg):
+    """The inputs the GPU tests build for each geometry (gen.device.make_case) pass every
+    check: the only error left on this GPU-less host is the missing device."""
+    from gen.device import make_case
+    case = make_case(cfg, "cpu")
+    layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout, cfg.algo,
+                             device="cpu", quant=cfg.quant, expert_out=cfg.expert_out, act=cfg.act)
+    for call in (lambda: layer.set_weights(case.w1, case.w2),
+                 lambda: layer.dispatch(case.x, case.ids, case.w,
+                                        torch.ones(cfg.W, dtype=torch.int32)),
+                 lambda: layer.combine(case.w)):
+        with pytest.raises(RuntimeError):
+            call()
