@@ -190,6 +190,87 @@ def test_route_hand_example():
                 assert rt_["recv_topk_idx"][d, r].tolist() == loc
 
 
+def _brute_dispatch_rows(W, Tr, T, E, k, ids, layout, b):
+    """(receive row, token) pairs counted from the brute-force routing: EXPERT_MAJOR one
+    row per kept pick at e*cap + (number of earlier kept picks of e); RANK_MAJOR / FLAT one
+    row per (token, destination) pair at d*cap + the token's row there."""
+    cap = W * Tr
+    ids = np.asarray(ids).reshape(T, k)
+    pairs = []
+    if layout == "EM":
+        for t in range(T):
+            for j in range(k):
+                if b["pos"][t, j] >= 0:
+                    e = int(ids[t, j])
+                    pairs.append((e * cap + int(b["pos"][t, j]) - b["offsets"][e], t))
+    else:
+        rr = b["rm"] if layout == "RM" else b["fl"]
+        pairs = [(d * cap + int(rr[t, d]), t) for t in range(T) for d in range(W) if rr[t, d] >= 0]
+    return sorted(pairs)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_dispatch_rows_match_brute_force(seed):
+    """oracle.dispatch_rows decides which received row the dispatch check compares with which
+    token: every row that should hold a token is listed, with that token, and nothing else."""
+    W, Tr, T, E, k, ids, w = _rand_case(seed)
+    for layout in ("EM", "RM", "FLAT"):
+        b = brute_route(W, Tr, T, E, k, ids, w, cap=W * Tr if layout == "EM" else None)
+        g = dict(W=W, Tr=Tr, T=T, E=E, k=k, layout=layout)
+        rows, toks = oracle.dispatch_rows(g, oracle.route(g, ids, w))
+        got = sorted(zip(np.asarray(rows).tolist(), np.asarray(toks).tolist()))
+        want = _brute_dispatch_rows(W, Tr, T, E, k, ids, layout, b)
+        assert got == want, layout
+        n_expected = sum(b["counts"]) if layout == "EM" else int(((b["rm"] if layout == "RM" else b["fl"]) >= 0).sum())
+        assert len(got) == n_expected
+
+
+def test_dispatch_rows_pins_catch_planted_mistakes():
+    """Plausible mistakes in dispatch_rows (a wrong region base, one destination per token,
+    a dropped pick) each fail the brute-force comparison on the tiny random cases."""
+    real = oracle.dispatch_rows
+
+    def wrong_cap(g, rt):
+        rows, toks = real(g, rt)
+        cap = g["W"] * g["Tr"]
+        return rows - (rows // cap) * cap + (rows // cap) * g["Tr"], toks
+
+    def one_dest(g, rt):
+        rows, toks = real(g, rt)
+        if g["layout"] == "EM":
+            return rows, toks
+        keep = np.ones(len(toks), bool)
+        keep[1:] = toks[1:] != toks[:-1]
+        return rows[keep], toks[keep]
+
+    def drop_last(g, rt):
+        rows, toks = real(g, rt)
+        return rows[:-1], toks[:-1]
+
+    for bad in (wrong_cap, one_dest, drop_last):
+        caught = False
+        for seed in range(40):
+            W, Tr, T, E, k, ids, w = _rand_case(seed)
+            for layout in ("EM", "RM", "FLAT"):
+                b = brute_route(W, Tr, T, E, k, ids, w, cap=W * Tr if layout == "EM" else None)
+                g = dict(W=W, Tr=Tr, T=T, E=E, k=k, layout=layout)
+                rows, toks = bad(g, oracle.route(g, ids, w))
+                got = sorted(zip(np.asarray(rows).tolist(), np.asarray(toks).tolist()))
+                caught |= got != _brute_dispatch_rows(W, Tr, T, E, k, ids, layout, b)
+        assert caught, bad.__name__
+
+
+def test_dispatch_rows_hand_example():
+    gd = json.load(open(os.path.join(GOLDEN, "route_hand_example.json")))
+    ids = np.array(gd["topk_ids"])
+    w = np.array(gd["topk_weights"], np.float32)
+    for layout in ("EM", "RM", "FLAT"):
+        g = dict(gd["geom"], layout=layout)
+        rows, toks = oracle.dispatch_rows(g, oracle.route(g, ids, w))
+        got = sorted(zip(np.asarray(rows).tolist(), np.asarray(toks).tolist()))
+        assert [list(p) for p in got] == gd["dispatch_rows"][layout], layout
+
+
 def test_route_flags_bad_ids():
     ids = np.array([[0, 5], [-2, 1]])
     rt = oracle.route(dict(W=1, Tr=2, T=2, E=4, k=2, layout="EM"), ids, np.ones((2, 2), np.float32))
