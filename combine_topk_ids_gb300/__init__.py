@@ -33,7 +33,8 @@ class MoeGeom(ctypes.Structure):
 _P = ctypes.c_void_p
 _HANDLE_PTRS = ("recv_x", "recv_scales", "counts", "offsets", "pick_pos", "pick_src", "slot",
                 "layout_range", "recv_row", "recv_count", "num_recv", "recv_src", "recv_topk_idx",
-                "recv_topk_weights", "status", "ffn_act", "ffn_act_scales", "workspace")
+                "recv_topk_weights", "status", "ffn_act", "ffn_act_scales", "pick_rows", "pick_row_scales",
+                "workspace")
 
 
 class MoeHandle(ctypes.Structure):

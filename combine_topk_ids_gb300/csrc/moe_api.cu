@@ -35,12 +35,19 @@ const DeviceInfo *device_info() {
     return &d;
 }
 
+}  // namespace
+
 int check_device() {
     const DeviceInfo *d = device_info();
     if (!d) return MOE_ERR_CUDA;
     return d->checked == 1 ? MOE_OK : MOE_ERR_NOT_BUILT_FOR_DEVICE;
 }
-}  // namespace
+
+int device_ordinal() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    return dev;
+}
 
 int num_sms() {
     const DeviceInfo *d = device_info();
@@ -236,6 +243,8 @@ int moe_dispatch(const moe_geom *g, const void *x_dev, const void *topk_ids_dev,
     h->recv_scales = r.recv_scales;
     h->ffn_act = r.act;
     h->ffn_act_scales = r.act_scales;
+    h->pick_rows = g->layout != MOE_LAYOUT_EXPERT_MAJOR ? (void *)r.apick : nullptr;
+    h->pick_row_scales = r.apick_scales;
     h->counts = r.counts;
     h->offsets = r.offsets;
     h->pick_pos = r.pick_pos;

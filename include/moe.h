@@ -199,6 +199,12 @@ typedef struct {
                                   e4m3 codes                                             */
     float *ffn_act_scales;     /* FP8 only (else NULL): scales of ffn_act, column-block
                                   major [I/128][T*k] (row p, block b at b*T*k + p)        */
+    void *pick_rows;           /* RM/FLAT (else NULL): [R, H] the row of every kept pick in
+                                  pick-list order, x[pick_src[p] / k] at row p, written by
+                                  moe_dispatch beside the receive buffer as the first
+                                  GEMM's operand (bf16, or FP8 e4m3 codes)               */
+    float *pick_row_scales;    /* RM/FLAT FP8 only (else NULL): scales of pick_rows,
+                                  column-block major [H/128][T*k]                        */
     void *workspace;           /* base of the workspace the handle lives in              */
     size_t workspace_bytes;
     /* Optional per-kernel timing, the analogue of FlashInfer's enable_timing stage events
@@ -378,12 +384,16 @@ int moe_get_status(const moe_handle *h, int32_t *status_host, void *stream);
  *   (2 * E * nb + 2 * E + 2) * 4 bytes of it, nb being the routing chunk count of the geometry
  *   (about 256 for large batches); a larger geometry returns MOE_ERR_LIMIT.
  *   The first call on each device looks the array's address up (cudaGetSymbolAddress)
- *   with that device current; make that first call before any stream capture.
+ *   with that device current; make that first call before any stream capture.  The
+ *   address is kept for that device until the process exits: after cudaDeviceReset (or
+ *   any other teardown of the device's primary context) this entry point must not be
+ *   called again in the same process.
  *   Every call shares the one array, so calls that overlap on the GPU (issued on different
  *   streams of one device without ordering between them) race on it and corrupt each
  *   other's results: order them on one stream.
  *   Errors: MOE_ERR_INVALID_ARGUMENT for a non-EXPERT_MAJOR geometry or a NULL buffer,
- *   the geometry errors of moe_workspace_size, MOE_ERR_LIMIT beyond the scratch size.
+ *   the geometry errors of moe_workspace_size, MOE_ERR_LIMIT beyond the scratch size,
+ *   MOE_ERR_NOT_BUILT_FOR_DEVICE on a device other than compute capability 10.3.
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
 int moe_route_noalloc(const moe_geom *g, const void *topk_ids_dev, int ids_dtype,

@@ -127,3 +127,49 @@ def test_launches_per_layer(lib, W, Tr, T, E, k, layout, want):
     # routing (1 or 3), row scatter, GEMM1, GEMM2, RANK_MAJOR / FLAT reduction, combine
     g = moe.make_geom(W, Tr, T, 512, E, k, 256, layout, "LL")
     assert moe.moe_launches_per_layer(g) == want
+
+
+def test_ctypes_structs_match_the_header(tmp_path):
+    """The binding's ctypes mirrors of moe_geom and moe_handle have the C layout: a small C
+    program built against include/moe.h prints sizeof and offsetof of every field."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = {"moe_geom": [n for n, _ in moe.MoeGeom._fields_],
+              "moe_handle": [n for n, _ in moe.MoeHandle._fields_]}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe.h"', "int main(void) {"]
+    for st, names in fields.items():
+        lines.append('printf("%s sizeof %%zu\\n", sizeof(%s));' % (st, st))
+        for n in names:
+            lines.append('printf("%s %s %%zu\\n", offsetof(%s, %s));' % (st, n, st, n))
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    got = {}
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        st, n, v = line.split()
+        got[(st, n)] = int(v)
+    for st, cls in (("moe_geom", moe.MoeGeom), ("moe_handle", moe.MoeHandle)):
+        assert got[(st, "sizeof")] == ctypes.sizeof(cls), st
+        for n in fields[st]:
+            assert got[(st, n)] == getattr(cls, n).offset, (st, n)
+
+
+def test_noalloc_validates_before_touching_a_device(lib):
+    """moe_route_noalloc's host checks come first; on a host without a GB300 a valid call
+    reports the device (MOE_ERR_CUDA without one, MOE_ERR_NOT_BUILT_FOR_DEVICE on another
+    GPU) and never succeeds."""
+    p = ctypes.c_void_p(1 << 20)
+    call = lambda g, dt=1: lib.moe_route_noalloc(ctypes.byref(g), p, dt, p, p, p, p, p, p, p, None)  # noqa: E731
+    assert call(_geom(layout="RM")) == -1
+    assert call(_geom(), dt=5) == -7
+    assert call(_geom(E=7)) == -2
+    assert call(moe.make_geom(8, 16384, 8, 128, 2048, 1, 128, "EM", "LL")) == -13
+    import torch
+    if not torch.cuda.is_available():
+        assert call(_geom()) in (-11, -12)

@@ -113,6 +113,14 @@ def test_fp8_dispatch_bit_exact(name):
     codes, sc, _ = fp8.quantize_rows(oracle.bf16_bits_to_f64(case.x_bits))
     np.testing.assert_array_equal(recv[rows], codes[toks])
     np.testing.assert_array_equal(scales[:, rows].T, sc[toks])
+    if cfg.layout != "EM":
+        # the kept picks' rows in pick-list order (the first GEMM's operand), codes and scales
+        R, P = rt["R"], cfg.tokens * cfg.k
+        src = rt["pick_src"].astype(np.int64) // cfg.k
+        prow = layer.view("pick_rows", (R, cfg.H), torch.uint8).cpu().numpy()
+        psc = layer.view("pick_row_scales", (cfg.H // 128, P), torch.float32).cpu().numpy()
+        np.testing.assert_array_equal(prow, codes[src])
+        np.testing.assert_array_equal(psc[:, :R].T, sc[src])
 
 
 def _check_layer(cfg, active=None, tokens=None, layer=None, case=None):

@@ -9,7 +9,8 @@ import combine_topk_ids_gb300 as moe
 import gen
 import oracle
 from gen.device import make_case
-from parity_util import check_dispatch_rows, check_expert_out, check_out, check_routing, geom_dict, run_layer
+from parity_util import (check_dispatch_rows, check_layer_tokens, check_routing, geom_dict, run_layer,
+                         targeted_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -30,6 +31,9 @@ def _sample(n_total, n, seed):
 
 @pytest.mark.parametrize("name", list(gen.CONFIGS))
 def test_full_size(name):
+    """Routing, every received row and (RANK_MAJOR / FLAT) every pick-ordered row bit for
+    bit; expert_out and out on the targeted tokens (every expert's tail row block, rows
+    128..255 of the 256-row tiles, the most loaded expert) plus random ones."""
     cfg = gen.CONFIGS[name]
     case = make_case(cfg, "cuda")
     layer = run_layer(case)
@@ -38,15 +42,11 @@ def test_full_size(name):
     rt = oracle.route(g, case.ids_np, case.w_np)
     check_routing(layer, rt, cfg)
     check_dispatch_rows(layer, rt, case)
-    ntok = 64 if cfg.E * cfg.H * cfg.I <= (1 << 30) else 6
-    toks = _sample(cfg.tokens, ntok, 1)
-    if cfg.layout == "EM":
-        picks = np.array([t * cfg.k + j for t in toks for j in range(cfg.k) if rt["pick_pos"][t, j] >= 0])
-        check_expert_out(layer, rt, case, picks_or_rows=picks)
-    else:
-        rows = [(d, int(rt["recv_row"][t, d])) for t in toks for d in range(cfg.W) if rt["recv_row"][t, d] >= 0]
-        check_expert_out(layer, rt, case, picks_or_rows=rows)
-    check_out(layer, case, tokens=toks)
+    small = cfg.E * cfg.H * cfg.I <= (1 << 30)
+    toks = targeted_tokens(cfg, rt, n_random=64 if small else 32, seed=1)
+    n_eo, n_out = check_layer_tokens(layer, rt, case, toks)
+    print("%s: %d tokens checked; elements outside the plain bound: expert_out %d, out %d"
+          % (name, len(toks), n_eo, n_out))
     del layer, case
     torch.cuda.empty_cache()
 
