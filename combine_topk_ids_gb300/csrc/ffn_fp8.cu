@@ -480,9 +480,17 @@ int launch_gemm_fp8(const CUtensorMap &ma, const CUtensorMap &mb, const F8Args &
     if (max_tiles <= 0) return MOE_OK;
     auto kernel = ffn_gemm_fp8_kernel<MODE>;
     constexpr int smem = F8Smem<MODE>::kBytes;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
+    // kernel attributes are set per device (with that device current), once each
+    struct PerDevice {
+        std::once_flag once;
+        cudaError_t attr_err = cudaSuccess;
+    };
+    static PerDevice per_device[64];
+    const int dev = device_ordinal();
+    if (dev < 0) return MOE_ERR_CUDA;
+    PerDevice &pd = per_device[dev];
+    cudaError_t &attr_err = pd.attr_err;
+    std::call_once(pd.once, [&] {
         attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         // setmaxnreg.inc waits until the registers it asks for are free in the CTA's launch
         // allocation: never launch a build whose register count makes the split too large

@@ -531,10 +531,19 @@ int launch_gemm(const CUtensorMap &ma, const CUtensorMap &ma2, const CUtensorMap
     if (max_tiles <= 0) return MOE_OK;
     constexpr int smem = Pipe<HILO, PAIR, TALL>::kSmemBytes;
     auto kernel = ffn_gemm_kernel<HILO, PAIR, TALL>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    static int max_clusters = 0;
-    std::call_once(once, [&] {
+    // kernel attributes are set per device (with that device current), once each
+    struct PerDevice {
+        std::once_flag once;
+        cudaError_t attr_err = cudaSuccess;
+        int max_clusters = 0;
+    };
+    static PerDevice per_device[64];
+    const int dev = device_ordinal();
+    if (dev < 0) return MOE_ERR_CUDA;
+    PerDevice &pd = per_device[dev];
+    cudaError_t &attr_err = pd.attr_err;
+    int &max_clusters = pd.max_clusters;
+    std::call_once(pd.once, [&] {
         attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (attr_err == cudaSuccess && PAIR) {
             attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);

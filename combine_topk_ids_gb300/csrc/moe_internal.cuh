@@ -88,6 +88,8 @@ int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, voi
                      cudaStream_t s);
 
 int num_sms();   // SM count of the current device (cached per device)
+int check_device();   // MOE_OK on a compute capability 10.3 device, else a moe_error
+int device_ordinal();   // the current device, or -1 (only ordinals below 64 are served)
 
 // ---- programmatic dependent launch -----------------------------------------------------
 // The layer's kernels are launched with programmatic stream serialization, so the launch of

@@ -64,6 +64,7 @@ extern "C" int moe_route_noalloc(const moe_geom *g, const void *topk_ids_dev, in
     const size_t hist_ints = (size_t)p.E * p.nb;
     const size_t need = 2 * hist_ints + 2 * ((size_t)p.E + 1);
     if (need * sizeof(int32_t) > kScratchBytes) return MOE_ERR_LIMIT;
+    if ((rc = check_device()) != MOE_OK) return rc;
 
     int err = MOE_OK;
     int32_t *scratch = scratch_on_current_device(&err);
@@ -83,9 +84,9 @@ extern "C" int moe_route_noalloc(const moe_geom *g, const void *topk_ids_dev, in
     r.mprefix = scratch + 2 * hist_ints;
     r.mprefix2 = r.mprefix + p.E + 1;
     // every scratch entry the kernels read is written earlier in the same call, so the
-    // previous call's contents never need clearing; only the status output starts at 0
+    // previous call's contents never need clearing; the status output starts at 0, which
+    // launch_routing sees to before any routing kernel can set a bit
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(status_dev, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
     return launch_routing(r, topk_ids_dev, ids_dtype == MOE_IDS_INT64, nullptr, nullptr, s) ==
                    cudaSuccess
                ? MOE_OK

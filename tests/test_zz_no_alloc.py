@@ -57,11 +57,14 @@ def _noalloc(cfg, case):
     return bufs
 
 
+@pytest.mark.parametrize("ids_dtype", ["int64", "int32"])
 @pytest.mark.parametrize("name", ["small_em", "ragged_em"])
-def test_noalloc_routing_matches_dispatch_on_consecutive_calls(name):
+def test_noalloc_routing_matches_dispatch_on_consecutive_calls(name, ids_dtype):
     base = gen.ALL[name]
-    cfgs = [base.with_(seed=seed, mask_frac=0.1) for seed in (21, 22)]
+    cfgs = [base.with_(seed=seed, mask_frac=0.1, ids_dtype=ids_dtype) for seed in (21, 22)]
     cases = [make_case(c, "cuda") for c in cfgs]
+    for c in cases:
+        assert c.ids.dtype == getattr(torch, ids_dtype)
     refs = [_reference(c, cs) for c, cs in zip(cfgs, cases)]
     # two calls in a row on different batches: the second reuses the scratch the first left
     gots = [_noalloc(c, cs) for c, cs in zip(cfgs, cases)]
