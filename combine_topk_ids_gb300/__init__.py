@@ -19,7 +19,7 @@ LAYOUT = {"EM": 0, "RM": 1, "FLAT": 2}
 ALGO = {"LL": 0, "HT": 1}
 QUANT = {"bf16": 0, "fp8": 1}
 EXPERT_OUT = {"fp32": 0, "bf16": 1}
-ACT = {"bf16": 0, "pair": 1}
+ACT = {"pair": 0, "bf16": 1}
 IDS_INT32, IDS_INT64 = 0, 1
 STATUS_BAD_EXPERT_ID, STATUS_EM_OVERFLOW, STATUS_TIMEOUT, STATUS_INACTIVE_RANK = 0x1, 0x2, 0x4, 0x8
 
@@ -106,7 +106,7 @@ def _check(rc, where):
 
 
 def make_geom(W, Tr, T, H, E, k, I, layout="EM", algo="LL", quant="bf16", expert_out="fp32",
-              act="bf16") -> MoeGeom:
+              act="pair") -> MoeGeom:
     return MoeGeom(W, Tr, T, H, E, k, I, LAYOUT[layout] if isinstance(layout, str) else layout,
                    ALGO[algo] if isinstance(algo, str) else algo,
                    QUANT[quant] if isinstance(quant, str) else quant,
@@ -275,12 +275,13 @@ class MoELayer1GPU:
     forward(x, topk_ids, topk_weights) = moe_dispatch -> moe_expert_ffn -> moe_combine,
     all on the current stream, no host synchronisation.  quant="fp8": FP8 dispatch and
     moe_expert_ffn_fp8 on weights quantised by set_weights.  expert_out="bf16": the expert
-    stage's output (and the RANK_MAJOR / FLAT per-pick rows) in bf16.  act="pair": the SwiGLU
-    activation as a bf16 (hi, lo) pair instead of one bf16 value.
+    stage's output (and the RANK_MAJOR / FLAT per-pick rows) in bf16.  act: the SwiGLU
+    activation as the second GEMM's operand, "pair" (default: a bf16 (hi, lo) pair) or
+    "bf16" (one bf16 value: faster, less accurate; see moe_act_precision in moe.h).
     """
 
     def __init__(self, W, Tr, T, H, E, k, I, layout="EM", algo="LL", device="cuda", quant="bf16",
-                 expert_out="fp32", act="bf16"):
+                 expert_out="fp32", act="pair"):
         import torch
         self.quant = quant
         self.geom = make_geom(W, Tr, T, H, E, k, I, layout, algo, quant, expert_out, act)

@@ -87,13 +87,21 @@ typedef enum { MOE_EXPERT_OUT_FLOAT32 = 0, MOE_EXPERT_OUT_BFLOAT16 = 1 } moe_exp
 
 /*
  * The SwiGLU activation as the second GEMM's operand (bf16 geometries; FP8 geometries
- * quantise it to e4m3 instead) [FI-4: the expert GEMMs take bf16 operands].
- *   MOE_ACT_BF16       act = bf16_rne(silu(g) * u), one bf16 x bf16 GEMM (default).
- *   MOE_ACT_BF16_PAIR  act carried as act_hi = bf16(act) plus act_lo = bf16(act - act_hi)
- *                      (about 16 significant bits): GEMM2 runs both halves, twice the
- *                      tensor work, for outputs that track an unrounded activation.
+ * quantise it to e4m3 instead).  The expert GEMMs take bf16 operands [FI-4 step 3]; the
+ * layer's output is checked against the expert FFN evaluated in full precision from the
+ * bf16 weights [FI-4 step 6], which only the pair reaches within the output tolerance.
+ *   MOE_ACT_BF16_PAIR  (default, 0) act carried as act_hi = bf16(act) plus
+ *                      act_lo = bf16(act - act_hi), about 16 significant bits: GEMM2 runs
+ *                      both halves (two bf16 MMAs per k-step), so y tracks the unrounded
+ *                      activation to about 2e-4.
+ *   MOE_ACT_BF16       act = bf16_rne(silu(g) * u), one bf16 x bf16 GEMM: faster (about
+ *                      20% of the layer on tensor-bound batches), but each bf16 code is a
+ *                      rounding decision on a tensor-core sum; codes that land on the other
+ *                      side of a midpoint move y by |W2| x one bf16 step, which on long
+ *                      GEMMs puts some outputs outside 2e-2*|ref| + 1e-3 of the
+ *                      full-precision FFN.
  */
-typedef enum { MOE_ACT_BF16 = 0, MOE_ACT_BF16_PAIR = 1 } moe_act_precision;
+typedef enum { MOE_ACT_BF16_PAIR = 0, MOE_ACT_BF16 = 1 } moe_act_precision;
 
 typedef enum {
     MOE_OK = 0,
@@ -194,8 +202,8 @@ typedef struct {
     int32_t *status;           /* device status word (MOE_STATUS_* bits)                 */
     void *ffn_act;             /* written by the FFN: the SwiGLU activation, [R, I] in
                                   pick-list order (row offsets[e] + position), the second
-                                  GEMM's operand.  bf16: the bf16 activation (with
-                                  MOE_ACT_BF16_PAIR, the high half of the pair); FP8:
+                                  GEMM's operand.  bf16: the high half of the pair
+                                  (MOE_ACT_BF16: the bf16 activation); FP8:
                                   e4m3 codes                                             */
     float *ffn_act_scales;     /* FP8 only (else NULL): scales of ffn_act, column-block
                                   major [I/128][T*k] (row p, block b at b*T*k + p)        */
@@ -276,7 +284,7 @@ int moe_prepare_weights(const moe_geom *g, const void *w1_dev, void *w1_prepared
 /*
  * moe_expert_ffn - per-expert grouped SwiGLU FFN on the received rows [FI-2; FI-3]:
  * for each expert e and each of its rows x: h = x W1[e]^T (fp32 accumulate),
- * act = bf16(silu(h[:I]) * h[I:]) (or the bf16 pair of MOE_ACT_BF16_PAIR),
+ * act = silu(h[:I]) * h[I:] as a bf16 pair (MOE_ACT_BF16_PAIR) or one bf16 (MOE_ACT_BF16),
  * y = act W2[e]^T (fp32).
  *   EM:      expert_out[e*cap + r] = y of row r (top_k = 1 per dispatched row)
  *   RM/FLAT: expert_out[d*cap + r] = sum over the row's LOCAL picks j (ascending) of

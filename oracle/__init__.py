@@ -5,9 +5,9 @@ CPU-baseline leg (bench.py --impl reference / cpu_baseline) may import this pack
 The product library never calls it and shares no code with it.
 
 Plain and slow on purpose: routing is the literal (t, j)-ordered loop in moe_oracle.c;
-the FFN and combine are numpy in float64, one expert at a time; the only roundings are
-the SwiGLU activation's and the final output's to bf16 (plus expert_out's with the bf16
-expert_out option).
+the FFN and combine are numpy in float64, one expert at a time; the only rounding is the
+final output's to bf16 (plus, for the library's options, the SwiGLU activation's to bf16
+and expert_out's to bf16 where those options round).
 
 Sources (page title, section):
   * FlashInfer "MoE-EP implementation & usage", section 2 "Call stack": dispatch ->
@@ -26,10 +26,12 @@ Readings where the pages are silent (each listed in the design notes):
   * gate = rows [0, I) of w1[e], up = rows [I, 2I); SwiGLU act = silu(gate) * up with
     silu(g) = g / (1 + exp(-g))  (parity unpinned by the pages: a fixed convention);
   * the expert FFN is evaluated in full precision (float64) from the bf16 weights and
-    inputs; the SwiGLU activation, the operand of the second bf16 GEMM, is rounded to bf16
-    (round to nearest even) unless geom["act"] == "pair" (the library's bf16-pair option,
-    which tracks the unrounded activation); expert_out is not rounded (float64 here); the
-    final combined output is rounded to bf16 (round-to-nearest-even);
+    inputs, the SwiGLU activation unrounded (FlashInfer page, section 4 step 6: the EP
+    layer is checked against a dense MoE evaluated in fp32); only with geom["act"] ==
+    "bf16" (the library's single-bf16 activation option) is the activation, the operand
+    of the second bf16 GEMM, rounded to bf16 (round to nearest even) first; expert_out is
+    not rounded (float64 here); the final combined output is rounded to bf16
+    (round-to-nearest-even);
   * RANK_MAJOR / FLAT apply topk_weights in the FFN stage's reduction over the local
     picks of a received row (ascending j), and combine sums over destinations without
     weights (ascending d).
@@ -37,7 +39,7 @@ Readings where the pages are silent (each listed in the design notes):
 Functions whose values the pages never print ("parity unpinned" by the pages; pinned in
 tests by brute force, closed forms, a library special case and exact invariants):
 route, pick_outputs, ffn_ranks, combine_em, combine_ranks, layer (swiglu_act_band and bf16_act_allowance
-are the tolerance helpers of the default bf16 activation).
+are the tolerance helpers of the single-bf16 activation option).
 """
 import ctypes
 import os
@@ -191,7 +193,7 @@ def swiglu_act_band(xrows, w1e, rel=2.0 ** -14):
 
 
 def bf16_act_allowance(geom, rt, x_bits, w1, w2, picks, gpu_act):
-    """For the default bf16 activation: which of a GPU's activation codes are correct
+    """For the single-bf16 activation option: which of a GPU's activation codes are correct
     results, and what their differences from the oracle's codes may do to y.
 
     gpu_act: float64 [len(picks), I], the GPU's bf16 activation of each pick.  A code is
@@ -245,12 +247,13 @@ def pick_outputs(geom, rt, x_bits, w1, w2, picks=None, expert_fn=None, acts=None
     This is EXPERT_MAJOR's expert stage (top_k = 1 per dispatched row) and the per-pick
     term of the RANK_MAJOR / FLAT stage.  Returns {pick index t*k+j: float64 [H]} for
     `picks` (default: all valid picks).  expert_fn(e, xrows) replaces the SwiGLU expert
-    (the identity-expert pin uses it).  The activation is rounded to bf16 unless
-    geom["act"] == "pair" (reading: the expert GEMMs take bf16 operands, FlashInfer
-    "MoE-EP implementation & usage" section 4 step 3, so the second one's is rounded).
+    (the identity-expert pin uses it).  The activation is unrounded (the FFN in full
+    precision) unless geom["act"] == "bf16", the library's single-bf16 activation option,
+    whose second GEMM takes the activation as one bf16 operand (FlashInfer "MoE-EP
+    implementation & usage" section 4 step 3: the expert GEMMs take bf16 operands).
     acts: optional dict that receives each pick's unrounded activation (float64 [I]).
     """
-    act_bf16 = geom.get("act", "bf16") == "bf16"
+    act_bf16 = geom.get("act", "pair") == "bf16"
     k = geom["k"]
     pp = rt["pick_pos"].reshape(-1)
     ids = rt["ids"].reshape(-1)
@@ -351,4 +354,4 @@ def layer(geom, x_bits, ids, topk_w, w1, w2, tokens=None, expert_fn=None, active
 def geom_of(cfg):
     """Geometry dict of a gen.configs.MoeConfig."""
     return dict(W=cfg.W, Tr=cfg.Tr, T=cfg.tokens, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I,
-                layout=cfg.layout, act=getattr(cfg, "act", "bf16"))
+                layout=cfg.layout, act=getattr(cfg, "act", "pair"))

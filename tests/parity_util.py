@@ -96,14 +96,14 @@ def check_dispatch_rows(layer, rt, case):
 
 
 def act_flip_allowance(layer, rt, case, picks):
-    """The default bf16 activation is a rounding decision taken on tensor-core sums: a GPU
+    """The single-bf16 activation option is a rounding decision taken on tensor-core sums: a GPU
     code may be the neighbour of the oracle's where the exact activation lies within the
     accumulation band of a bf16 midpoint.  Checks every GPU activation code of `picks` is
     a correct result (oracle.bf16_act_allowance) and returns {pick: [H] allowance}; zero
-    for the bf16-pair activation."""
+    for the default bf16-pair activation."""
     cfg = case.cfg
     picks = [int(i) for i in picks]
-    if getattr(cfg, "act", "bf16") != "bf16" or not picks:
+    if getattr(cfg, "act", "pair") != "bf16" or not picks:
         return {i: 0.0 for i in picks}
     pp = rt["pick_pos"].reshape(-1)
     pos = torch.as_tensor([int(pp[i]) for i in picks], dtype=torch.int64, device=layer.out.device)
@@ -111,11 +111,16 @@ def act_flip_allowance(layer, rt, case, picks):
     allow, n_bad, n_flip = oracle.bf16_act_allowance(geom_dict(cfg), rt, case.x_bits, case.w1_host,
                                                      case.w2_host, picks, gpu)
     assert n_bad == 0, "%d activation codes outside the oracle's band" % n_bad
-    # a guard on how many codes may sit on the other side of a midpoint: 2% up to a
-    # 16384-long first-GEMM K loop, then in proportion to K (the tensor-core sum's distance
-    # from the exact sum grows with the number of terms it accumulates)
-    cap = 0.02 * max(1.0, cfg.H / 16384.0)
-    assert n_flip <= cap * len(picks) * cfg.I, "%d of %d activation codes differ" % (n_flip, len(picks) * cfg.I)
+    # a guard on how many codes may sit on the other side of a midpoint: the tensor-core
+    # sum's distance from the exact sum grows with the number of terms it accumulates, and
+    # the measured rate is about 0.11% of the codes per 1024 terms of the first GEMM's K
+    # (0.05% at K 512, 0.41% at 4096, 0.72% at 7168, 7.0% at 65536); allow twice that
+    # rate plus 0.1%
+    cap = 0.001 + 0.0022 * cfg.H / 1024.0
+    n_codes = len(picks) * cfg.I
+    print("%s: %d of %d activation codes on the other side of a midpoint (%.3g%%)"
+          % (cfg.name, n_flip, n_codes, 100.0 * n_flip / max(n_codes, 1)))
+    assert n_flip <= cap * n_codes, "%d of %d activation codes differ" % (n_flip, n_codes)
     return allow
 
 
@@ -239,5 +244,4 @@ def check_out(layer, case, tokens=None, active=None):
     for i in picks:
         extra[row_of[i // k]] += wv[i] * allow[i]
     got = bf16_tensor_to_f64(layer.out if tokens is None else layer.out[torch.as_tensor(tokens)])
-    assert_close(got, ref, "out (%s)" % cfg.name, extra=extra)
-    return ref
+    return assert_close(got, ref, "out (%s)" % cfg.name, extra=extra)

@@ -27,19 +27,44 @@ def test_algorithmic_work_expert_major():
     assert w["gemm2"]["bytes"] == E * H * I * 2 + R * I * 2 + R * H * 4
     assert w["gemm2"]["flops"] == 2 * R * I * H
     assert "reduce_ranks" not in w
-    assert w["combine"]["bytes"] == R * H * 4 + T * k * 8 + T * H * 2
+    # combine: the expert_out rows, the routing weights, the bf16 output
+    assert w["combine"]["bytes"] == R * H * 4 + T * k * 4 + T * H * 2
 
 
-def test_algorithmic_work_flat_counts_pick_rows_in_dispatch():
-    cfg = gen.CONFIGS["dsv3_ht_flat"]
-    T, k, H = cfg.tokens, cfg.k, cfg.H
+@pytest.mark.parametrize("layout", ["RM", "FLAT"])
+def test_algorithmic_work_rank_layouts(layout):
+    """RANK_MAJOR / FLAT: dispatch writes each received row once, the FFN's output is one row
+    per received row (N_recv), combine reads those; the pick-ordered rows, the per-pick GEMM2
+    rows and the local-pick reduction are this design's, not the layer's, and count nothing."""
+    cfg = gen.CONFIGS["dsv3_ht_flat"].with_(layout=layout)
+    T, k, H, I, E = cfg.tokens, cfg.k, cfg.H, cfg.I, cfg.E
     R, n_recv = T * k, 173743
-    w = bench.algorithmic_work(cfg, {"R": R, "active_experts": cfg.E, "n_recv": n_recv})
-    # the row scatter writes every received row and every kept pick's row
-    assert w["dispatch_copy"]["bytes"] == T * H * 2 + (n_recv + R) * H * 2
+    w = bench.algorithmic_work(cfg, {"R": R, "active_experts": E, "n_recv": n_recv})
+    assert w["dispatch_copy"]["bytes"] == T * H * 2 + n_recv * H * 2
     assert "gather_picks" not in w
-    assert w["reduce_ranks"]["bytes"] == R * H * 4 + n_recv * H * 4 + R * 8
+    assert w["gemm1_swiglu"]["bytes"] == E * 2 * I * H * 2 + R * H * 2 + R * I * 2
+    assert w["gemm2"]["bytes"] == E * H * I * 2 + R * I * 2 + n_recv * H * 4
+    assert w["reduce_ranks"]["bytes"] == 0 and w["reduce_ranks"]["flops"] == 0
     assert w["combine"]["bytes"] == n_recv * H * 4 + T * H * 2
+    layer = sum(v["bytes"] for v in w.values()) - w["routing"]["bytes"]
+    # dispatch + FFN + combine as one closed form: x in, received rows out, weights once,
+    # rows into the FFN, the activation out and back in, expert_out out and back in, output
+    assert layer == (T * H * 2 + n_recv * H * 2 + E * 3 * I * H * 2 + R * H * 2 + 2 * R * I * 2 +
+                     2 * n_recv * H * 4 + T * H * 2)
+    extra = bench.moved_beyond_algorithmic(cfg, {"R": R, "n_recv": n_recv})
+    assert extra["dispatch_copy"] == R * H * 2
+    assert extra["gemm1_swiglu"] == R * I * 2      # the low half of the bf16-pair activation
+    assert extra["gemm2"] == R * I * 2 + (R - n_recv) * H * 4
+
+
+def test_kernel_roofline_picks_the_bound_and_the_peak():
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+    mem = bench.kernel_roofline({"bytes": 6e9, "flops": 1e9}, 2e-3, peaks)
+    assert mem["bound"] == "hbm" and mem["frac"] == pytest.approx(0.5)
+    assert mem["frac_of_nominal"] == pytest.approx(3000.0 / bench.NOMINAL_PEAKS["hbm_gbs"])
+    tc = bench.kernel_roofline({"bytes": 1e9, "flops": 1.6e13}, 10e-3, peaks, sustained=True)
+    assert tc["bound"] == "tensor" and tc["peak_kind"] == "sustained" and tc["frac"] == pytest.approx(1.0)
+    assert bench.kernel_roofline({"bytes": 1e9, "flops": 1.6e13}, 10e-3, peaks)["frac"] == pytest.approx(0.8)
 
 
 def test_traffic_key_does_not_depend_on_the_checkout_path(monkeypatch):

@@ -96,7 +96,7 @@ def _cases():
     names = list(gen.SMALL) + ["tiny_ll_em"]
     cfgs = [gen.ALL[n] for n in names]
     cfgs += [gen.SMALL["small_em"].with_(quant="fp8"), gen.SMALL["small_flat"].with_(expert_out="bf16"),
-             gen.SMALL["small_rm"].with_(act="pair"), gen.SMALL["small_em"].with_(ids_dtype="int32", mask_frac=0.3)]
+             gen.SMALL["small_rm"].with_(act="bf16"), gen.SMALL["small_em"].with_(ids_dtype="int32", mask_frac=0.3)]
     return cfgs
 
 

@@ -74,3 +74,31 @@ def test_full_size_bf16_expert_out(name):
     assert fail < 2e-2
     del layer, case
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["mixtral_ll_em_act16", "dsv3_ll_rm_act16", "dsv3_ht_flat_act16", "ragged_em_act16"])
+def test_full_size_single_bf16_act(name):
+    """The single-bf16 activation option at full size: every activation code of the
+    sampled picks inside the oracle's band and the outputs within the bound plus the
+    allowance of the differing codes (against the oracle that rounds the activation the
+    same way), and the fraction of outputs outside the plain bound |d| <= 2e-2*|ref| + 1e-3
+    against the default full-precision oracle, reported (the cost of the option)."""
+    cfg = gen.ALL[name]
+    case = make_case(cfg, "cuda")
+    layer = run_layer(case)
+    assert layer.status() == 0
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    toks = targeted_tokens(cfg, rt, n_random=16, seed=3)
+    check_layer_tokens(layer, rt, case, toks)
+    _, ref = oracle.layer(geom_dict(cfg.with_(act="pair")), case.x_bits, case.ids_np, case.w_np,
+                          case.w1_host, case.w2_host, tokens=toks)
+    got = oracle.bf16_bits_to_f64(layer.out[torch.as_tensor(toks)].contiguous().view(torch.int16)
+                                  .cpu().numpy().view(np.uint16))
+    fail = float((np.abs(got - ref) > 2e-2 * np.abs(ref) + 1e-3).mean())
+    print("%s: %d tokens; fraction of outputs outside the plain bound against the full-precision "
+          "oracle: %.2e" % (name, len(toks), fail))
+    # a reported cost, not a bound: measured 3.5e-2 on the Mixtral-like batch (K 14336 in
+    # the second GEMM), 1.7e-2 on the DeepSeek-like ones, 6e-5 on the ragged one
+    assert fail < 5e-2
+    del layer, case
+    torch.cuda.empty_cache()
