@@ -96,7 +96,12 @@ struct FfnArgs {
     const float *direct_w;
     void *out_direct;
     int32_t *status;
+    // TALL tiles in dynamic order (NULL: the static order): sched[0] counts the tiles
+    // handed out after each CTA's first one, sched[1] the CTAs that finished; both are zero
+    // when the kernel starts, and the last CTA to finish zeroes them again
+    int32_t *sched;
 };
+constexpr int kRing = 4;   // tiles in flight from the producer to the MMA and epilogue warps
 
 // --- two-SM (cluster of two CTAs) variants
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -246,9 +251,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *sA = smem;                                     // [STAGES][kATiles] A tiles
     uint8_t *sB = smem + STAGES * P::kATiles * P::kABytes;  // [STAGES] B tiles (or halves)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * P::kStageBytes);
-    // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
+    // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], then (dynamic tile order)
+    // rfull[kRing], rempty[kRing]; then the TMEM address, the abort flag, the ring's tiles
+    // and their short-tile flags
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4 + 2 * kRing);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *ring_tile = reinterpret_cast<volatile int *>(tmem_slot + 2);
+    volatile int *ring_short = ring_tile + kRing;
+    const bool dyn = TALL && a.sched != nullptr;
+    const uint32_t rfull0 = smem_u32(bars + 2 * STAGES + 4), rempty0 = rfull0 + 8 * kRing;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
@@ -269,10 +280,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(tfull0 + 8 * s, 1);
             mbar_init(tempty0 + 8 * s, PAIR ? 2 * EPI_WARPS : EPI_WARPS);   // one arrival per epilogue warp
         }
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(rfull0 + 8 * s, 1);                 // the producer publishes a tile
+            mbar_init(rempty0 + 8 * s, 1 + EPI_WARPS);    // the MMA thread and every epilogue warp took it
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-        if (HILO)
+        if (HILO || dyn)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA2)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
     }
@@ -307,9 +322,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int b_rows_cta = PAIR ? a.bn / 2 : a.bn;
         const uint32_t tx_cta = (uint32_t)(P::kATiles * P::kABytes + b_rows_cta * BK * 2);
         const uint32_t tx = PAIR ? 2 * tx_cta : tx_cta;   // the leader's barrier sees both CTAs
-        for (int tile = first_tile; tile < total && ok; tile += tile_step) {
-            int e, mb, nbk;
-            decode_tile(a, tile, e, mb, nbk);
+        int seq = 0;
+        for (int tile = first_tile; ok;) {
+            bool short_tile = false;
+            int e = 0, mb = 0, nbk = 0;
+            if (tile < total) {
+                decode_tile(a, tile, e, mb, nbk);
+                // a tile whose rows end in its first 128 loads only those, through the
+                // 128-row box of tmA2, and the MMA issuer skips the second half
+                short_tile = dyn && __ldg(a.counts + e) - mb * P::kMRows <= BM;
+            }
+            if (dyn) {   // publish the tile (or the end) to the MMA and epilogue warps
+                const int slot = seq & (kRing - 1);
+                if (!mbar_wait(rempty0 + 8 * slot, ((seq / kRing) & 1) ^ 1, abort_flag, a.status)) break;
+                ring_tile[slot] = tile < total ? tile : -1;
+                ring_short[slot] = short_tile ? 1 : 0;
+                mbar_arrive(rfull0 + 8 * slot);
+                ++seq;
+            }
+            if (tile >= total) break;
             const int64_t arow = (a.a_mode == 0 ? (int64_t)e * a.a_cap : (int64_t)__ldg(a.offsets + e)) +
                                  (int64_t)mb * P::kMRows + (int64_t)rank * BM;
             const int64_t brow = (int64_t)e * a.b_rows + (int64_t)nbk * a.bn + (int64_t)rank * b_rows_cta;
@@ -324,6 +355,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tma_load_2d_pair(smem_u32(sa), &tmA, kb * BK, (int)arow, fbl);
                     if (HILO) tma_load_2d_pair(smem_u32(sa + A_BYTES), &tmA2, kb * BK, (int)arow, fbl);
                     tma_load_2d_pair(sb, &tmB, kb * BK, (int)brow, fbl);
+                } else if (short_tile) {
+                    mbar_expect_tx(fb, (uint32_t)(A_BYTES + a.bn * BK * 2));
+                    tma_load_2d(smem_u32(sa), &tmA2, kb * BK, (int)arow, fb);
+                    tma_load_2d(sb, &tmB, kb * BK, (int)brow, fb);
                 } else {
                     mbar_expect_tx(fb, tx);
                     tma_load_2d(smem_u32(sa), &tmA, kb * BK, (int)arow, fb);
@@ -332,6 +367,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
+            // dynamic order: a CTA takes its next tile from a device counter once it has
+            // queued this one's loads, so tiles start in increasing order, the tiles in flight
+            // stay a contiguous window and the m-blocks that share a weight tile run at the
+            // same time even when some tiles are shorter than others
+            tile = dyn ? (int)gridDim.x + atomicAdd(a.sched, 1) : tile + tile_step;
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ---------------------------------------------------------------- MMA issuer
@@ -341,7 +381,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t acc_phase = 0;
         bool ok = true;
         const uint32_t idesc = make_idesc(TALL ? BM : P::kMRows, a.bn);
-        for (int tile = first_tile; tile < total && ok; tile += tile_step) {
+        int seq = 0;
+        for (int tile = first_tile; ok; tile += tile_step) {
+            bool second_half = TALL;   // TALL: rows 128..255 of the tile hold data
+            if (dyn) {
+                const int slot = seq & (kRing - 1);
+                if (!mbar_wait(rfull0 + 8 * slot, (seq / kRing) & 1, abort_flag, a.status)) break;
+                tile = ring_tile[slot];
+                second_half = ring_short[slot] == 0;
+                mbar_arrive(rempty0 + 8 * slot);
+                ++seq;
+                if (tile < 0) break;
+            } else if (tile >= total) {
+                break;
+            }
             if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -363,7 +416,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (HILO) mma_bf16(d_tmem, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc, 1u);
                         // rows 128..255 of the tile: the second 16 KB of the A tile, the
                         // second accumulator
-                        if (TALL) mma_bf16(d_tmem + BN, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc, accum);
+                        if (TALL && second_half)
+                            mma_bf16(d_tmem + BN, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc, accum);
                     }
                 }
                 // the stage is reusable (in both CTAs) once these MMAs finish
@@ -389,7 +443,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t stg = smem_u32(smem + STAGES * P::kStageBytes + 256) + (uint32_t)((warp - 4) * kStageRowsBytes);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = first_tile; tile < total; tile += tile_step) {
+        int seq = 0;
+        for (int tile = first_tile;; tile += tile_step) {
+            if (dyn) {
+                const int slot = seq & (kRing - 1);
+                if (!mbar_wait(rfull0 + 8 * slot, (seq / kRing) & 1, abort_flag, a.status)) break;
+                tile = ring_tile[slot];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rempty0 + 8 * slot);
+                ++seq;
+                if (tile < 0) break;
+            } else if (tile >= total) {
+                break;
+            }
             int e, mb, nbk;
             decode_tile(a, tile, e, mb, nbk);
             const int count = __ldg(a.counts + e);
@@ -502,6 +568,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     __syncthreads();
     if (PAIR) cluster_sync();   // no signal from the peer can still be on its way here
+    if (dyn && threadIdx.x == 0) {
+        // every tile this CTA took was taken before the barrier above; the last CTA to get
+        // here zeroes the counters for the next launch
+        __threadfence();
+        if (atomicAdd(a.sched + 1, 1) == (int)gridDim.x - 1) {
+            a.sched[0] = 0;
+            a.sched[1] = 0;
+        }
+    }
     if (*abort_flag) {
         // Give in-flight TMA copies and MMAs time to land before the memory is released.
         unsigned long long t0 = globaltimer();
@@ -630,10 +705,11 @@ int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s) {
     const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
     const bool pair = use_pair(p, p.H, 2 * p.I);
     const bool tall = !pair && use_tall(p, p.H);
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mA2, mB;
     const void *a1 = em ? (const void *)r.recv_x : (const void *)r.apick;
     const int64_t a1_rows = em ? p.E * p.cap : p.P;
     if (!make_map(&mA, a1, a1_rows, p.H, tall ? 2 * BM : BM) ||
+        (tall && !make_map(&mA2, a1, a1_rows, p.H, BM)) ||   // short tail tiles of TALL
         !make_map(&mB, w1p, p.E * 2 * p.I, p.H, pair ? BN / 2 : BN))
         return MOE_ERR_CUDA;
     FfnArgs g = base_args(r, pair || tall);
@@ -642,7 +718,10 @@ int launch_gemm1(const Routing &r, const uint16_t *w1p, cudaStream_t s) {
     g.mode = 0; g.out = r.act; g.out2 = p.act_pair ? r.act_lo : nullptr; g.out_ld = p.I; g.out_mode = 1;
     g.out_cap = 0;
     if (pair) return launch_gemm<false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
-    if (tall) return launch_gemm<false, false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
+    if (tall) {
+        g.sched = r.sched;
+        return launch_gemm<false, false, true>(mA, mA2, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
+    }
     return launch_gemm<false, false>(mA, mA, mB, g, max_mblocks(p, BM) * g.nb, s);
 }
 
@@ -656,6 +735,7 @@ int launch_gemm2(const Routing &r, const uint16_t *w2, void *expert_out, cudaStr
     CUtensorMap mA, mA2, mB;
     if (!make_map(&mA, r.act, p.P, p.I, tall ? 2 * BM : BM) ||
         (p.act_pair && !make_map(&mA2, r.act_lo, p.P, p.I, BM)) ||
+        (tall && !make_map(&mA2, r.act, p.P, p.I, BM)) ||   // short tail tiles of TALL
         !make_map(&mB, w2, p.E * p.H, p.I, pair ? bn / 2 : bn))
         return MOE_ERR_CUDA;
     FfnArgs g = base_args(r, pair || tall);
@@ -671,7 +751,10 @@ int launch_gemm2(const Routing &r, const uint16_t *w2, void *expert_out, cudaStr
         return launch_gemm<true, false>(mA, mA2, mB, g, max_mblocks(p, BM) * g.nb, s);
     }
     if (pair) return launch_gemm<false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
-    if (tall) return launch_gemm<false, false, true>(mA, mA, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
+    if (tall) {
+        g.sched = r.sched + 2;
+        return launch_gemm<false, false, true>(mA, mA2, mB, g, max_mblocks(p, 2 * BM) * g.nb, s);
+    }
     return launch_gemm<false, false>(mA, mA, mB, g, max_mblocks(p, BM) * g.nb, s);
 }
 

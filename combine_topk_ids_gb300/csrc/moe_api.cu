@@ -101,7 +101,7 @@ int make_plan(const moe_geom &g, Plan *p) {
         off = align_up(off + bytes, 256);
         return o;
     };
-    q.status = take(4);
+    q.status = take(4 * 5);   // status word, then the GEMMs' four tile counters
     q.counts = take(4 * E);
     q.offsets = take(4 * (E + 1));
     q.mprefix = take(4 * (E + 1));
@@ -139,7 +139,7 @@ Routing carve(const Plan &p, void *ws) {
     Routing r;
     r.p = &p;
     auto i32 = [&](size_t o) { return reinterpret_cast<int32_t *>(b + o); };
-    r.status = i32(p.status); r.counts = i32(p.counts); r.offsets = i32(p.offsets);
+    r.status = i32(p.status); r.sched = r.status + 1; r.counts = i32(p.counts); r.offsets = i32(p.offsets);
     r.mprefix = i32(p.mprefix); r.mprefix2 = i32(p.mprefix2); r.pick_pos = i32(p.pick_pos); r.pick_src = i32(p.pick_src);
     r.slot = i32(p.slot); r.layout_range = i32(p.layout_range); r.blk_hist = i32(p.blk_hist);
     r.blk_base = i32(p.blk_base); r.recv_row = i32(p.recv_row); r.recv_count = i32(p.recv_count);

@@ -50,6 +50,10 @@ struct Routing {
     // straight into expert_out for such picks, and the local-pick reduction skips the row.
     int32_t *direct_row;
     float *direct_w;
+    // the two GEMMs' tile counters for the dynamic tile order ([0..1] first GEMM, [2..3]
+    // second), right after the status word; zeroed with it by the routing launch, and by
+    // each GEMM for its next launch; NULL when the routing runs without a workspace
+    int32_t *sched;
     // FP8 geometry: recv_x / act / apick hold e4m3 codes (one byte per element); their
     // scales are column-block major ([cols/128][rows]); act_lo is unused
     float *recv_scales, *act_scales, *apick_scales;

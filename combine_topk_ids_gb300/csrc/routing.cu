@@ -30,6 +30,7 @@ struct RouteArgs {
     const int32_t *active;          // EP rank-health mask [W] (NULL: all ranks active)
     int T, W, Tr, E, k, Le, layout, tb, nbpr, nb;
     int zero_status;                // the single-CTA kernel clears the status word first
+    int32_t *sched;                 // and the GEMMs' tile counters (NULL: none)
     int64_t cap;
     int32_t *status, *counts, *offsets, *mprefix, *mprefix2, *pick_pos, *pick_src, *slot, *layout_range;
     int32_t *blk_hist, *blk_base;   // [E][nb]
@@ -429,7 +430,11 @@ __global__ void __launch_bounds__(kFusedThreads) route_fused_kernel(RouteArgs a)
     __shared__ unsigned long long s_act;
     if (threadIdx.x == 0) {
         s_act = load_active_mask(a);
-        if (a.zero_status) *a.status = 0;   // before the barrier below, so before any bit is set
+        if (a.zero_status) {
+            *a.status = 0;   // before the barrier below, so before any bit is set
+            if (a.sched)
+                for (int i = 0; i < 4; ++i) a.sched[i] = 0;
+        }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool em = a.layout == MOE_LAYOUT_EXPERT_MAJOR;
@@ -637,6 +642,7 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
     a.recv_src = r.recv_src; a.recv_topk_idx = r.recv_topk_idx; a.recv_topk_w = r.recv_topk_w;
     a.blk_dhist = r.blk_dhist; a.blk_dbase = r.blk_dbase;
     a.zero_status = 0;
+    a.sched = r.sched;
 
     // one fused CTA for small batches with few experts (bounded shared memory); it clears
     // the status word itself (one launch less in a latency-bound step)
@@ -653,7 +659,9 @@ cudaError_t launch_routing(const Routing &r, const void *ids, int ids64, const f
     }
 
     // several blocks may raise status bits: clear the word before the first of them runs
-    if (cudaMemsetAsync(a.status, 0, sizeof(int32_t), s) != cudaSuccess) return cudaGetLastError();
+    // (the GEMMs' tile counters follow the status word when there is a workspace)
+    if (cudaMemsetAsync(a.status, 0, (r.sched ? 5 : 1) * sizeof(int32_t), s) != cudaSuccess)
+        return cudaGetLastError();
     size_t sm1 = (size_t)(a.E + a.W) * sizeof(int);
     cudaError_t e = launch_pdl(route_count_kernel, dim3(a.nb), dim3(kRouteThreads), sm1, s, a);
     if (e != cudaSuccess) return e;
