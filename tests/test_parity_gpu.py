@@ -39,6 +39,10 @@ SMALL_CASES = {
     "tall_flat": gen.SMALL["tall_flat"],
     "tall_flat_h4096": gen.SMALL["tall_flat"].with_(H=4096, I=512, seed=17),
     "tall_em_masked_i32": gen.SMALL["tall_em"].with_(mask_frac=0.2, ids_dtype="int32", seed=16),
+    # the 256-row tiles in dynamic order with fewer tiles than CTAs (one expert, 600 rows:
+    # three row blocks, the last a short 88-row tail, one n-block)
+    "tall_few_tiles": gen.MoeConfig("tall_few_tiles", W=1, Tr=600, H=4096, E=1, k=1, I=128,
+                                    layout="EM", algo="LL", routing="uniform", T=600),
     # multi-block routing (more than 3072 picks; these hold more than 16384)
     "blocks_em": gen.SMALL["blocks_em"],
     "blocks_rm": gen.SMALL["blocks_rm"],
@@ -162,6 +166,35 @@ def test_identity_expert_via_recv_buffer():
     ws = np.where(case.ids_np >= 0, case.w_np.astype(np.float64), 0.0).sum(axis=1)
     ref = oracle.round_bf16(oracle.bf16_bits_to_f64(case.x_bits) * ws[:, None])
     np.testing.assert_allclose(bf16_tensor_to_f64(layer.out), ref, rtol=2 ** -7, atol=1e-30)
+
+
+@pytest.mark.parametrize("name", ["small_em", "tall_em", "tall_flat", "tall_few_tiles"])
+def test_ffn_twice_on_one_dispatch(name):
+    """moe_expert_ffn run twice on the same dispatch gives the same expert_out bit for bit:
+    the first GEMM's dynamic tile order (256-row tiles) leaves its tile counter at zero for
+    the next launch, which here is not preceded by a dispatch that would zero it."""
+    cfg = SMALL_CASES[name]
+    case = make_case(cfg, "cuda")
+    layer = run_layer(case)
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    H, cap = cfg.H, cfg.W * cfg.Tr
+    if cfg.layout == "EM":
+        rows = rt["slot"].reshape(-1)
+        rows = rows[rows >= 0]
+    else:
+        d, r = np.nonzero(rt["recv_src"] >= 0)
+        rows = d * cap + r
+    idx = torch.from_numpy(np.asarray(rows, np.int64)).cuda()
+    first = layer.expert_out.view(-1, H)[idx].clone()
+    out1 = layer.out.clone()
+    for _ in range(2):
+        layer.expert_out.zero_()
+        layer.expert_ffn()
+        layer.combine(case.w)
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        assert torch.equal(layer.expert_out.view(-1, H)[idx], first)
+        assert torch.equal(layer.out.view(torch.int16), out1.view(torch.int16))
 
 
 # ----------------------------------------------------------------------- edge cases
