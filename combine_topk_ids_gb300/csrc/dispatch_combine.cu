@@ -387,6 +387,102 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
     }
 }
 
+// RANK_MAJOR / FLAT combine that also forms the local-pick sums of received rows with
+// several local picks, in place of the rank reduction: for token t and each destination d
+// (ascending) that received it, row r, the term is expert_out[d*cap + r] when the row has
+// one local pick (the second GEMM wrote it), else the fmaf chain over its local picks j
+// ascending of recv_topk_w * y_j (y_j: the pick's second-GEMM row), rounded as the
+// reduction stores it (bf16 rows: to bf16); out[t] = bf16(sum of the terms).  These are the
+// reduction's and combine_kernel's operations in the same order, so the output is the
+// same bit for bit; expert_out's multi-pick rows are left unwritten.
+struct FusedCombineArgs {
+    const void *eo, *ypick;   // float32 or bf16 rows (the kernel's BF16 parameter)
+    const int32_t *recv_row, *recv_topk_idx, *pick_pos;
+    const float *recv_topk_w;
+    uint16_t *out;
+    int T, k, W, H, nchunk;
+    int64_t cap;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kCopyThreads) combine_fused_kernel(FusedCombineArgs a) {
+    pdl_begin();   // after the previous kernel in the stream (programmatic launch)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + warp;   // (token, chunk)
+    const int64_t t = gw / a.nchunk;
+    const int chunk = (int)(gw - t * a.nchunk);
+    if (t >= a.T) return;
+    const int nv = a.H / 4;   // float4 per row
+    const int c0 = chunk * 32 * kCopyU + lane;
+    float4 acc[kCopyU];
+#pragma unroll
+    for (int u = 0; u < kCopyU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int d = 0; d < a.W; ++d) {
+        const int r = a.recv_row[t * a.W + d];   // the same for every lane
+        if (r < 0) continue;
+        const int64_t gr = (int64_t)d * a.cap + r;
+        int64_t p = -1;   // lane j: pick j's position in the pick list if it is local to d
+        float w = 0.f;
+        if (lane < a.k && a.recv_topk_idx[gr * a.k + lane] >= 0) {
+            p = a.pick_pos[t * a.k + lane];
+            w = a.recv_topk_w[gr * a.k + lane];
+        }
+        unsigned bal = __ballot_sync(0xffffffffu, p >= 0);
+        float4 sd[kCopyU];
+        if (__popc(bal) == 1) {
+#pragma unroll
+            for (int u = 0; u < kCopyU; ++u)
+                if (c0 + 32 * u < nv) sd[u] = ld_row4<BF16>(a.eo, gr * a.H + 4 * (c0 + 32 * u));
+        } else {
+#pragma unroll
+            for (int u = 0; u < kCopyU; ++u) sd[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            while (bal) {
+                const int j = __ffs(bal) - 1;
+                bal &= bal - 1;
+                const int64_t pj = __shfl_sync(0xffffffffu, p, j);
+                const float wj = __shfl_sync(0xffffffffu, w, j);
+                float4 y[kCopyU];
+#pragma unroll
+                for (int u = 0; u < kCopyU; ++u)
+                    if (c0 + 32 * u < nv) y[u] = ld_row4<BF16>(a.ypick, pj * a.H + 4 * (c0 + 32 * u));
+#pragma unroll
+                for (int u = 0; u < kCopyU; ++u) {
+                    sd[u].x = fmaf(wj, y[u].x, sd[u].x);
+                    sd[u].y = fmaf(wj, y[u].y, sd[u].y);
+                    sd[u].z = fmaf(wj, y[u].z, sd[u].z);
+                    sd[u].w = fmaf(wj, y[u].w, sd[u].w);
+                }
+            }
+            if (BF16) {   // the reduction stores bf16 rows
+#pragma unroll
+                for (int u = 0; u < kCopyU; ++u)
+                    sd[u] = make_float4(__bfloat162float(__float2bfloat16_rn(sd[u].x)),
+                                        __bfloat162float(__float2bfloat16_rn(sd[u].y)),
+                                        __bfloat162float(__float2bfloat16_rn(sd[u].z)),
+                                        __bfloat162float(__float2bfloat16_rn(sd[u].w)));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u) {
+            acc[u].x += sd[u].x;
+            acc[u].y += sd[u].y;
+            acc[u].z += sd[u].z;
+            acc[u].w += sd[u].w;
+        }
+    }
+    uint2 *o = reinterpret_cast<uint2 *>(a.out + t * a.H);
+#pragma unroll
+    for (int u = 0; u < kCopyU; ++u) {
+        if (c0 + 32 * u >= nv) continue;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+        uint2 v;
+        v.x = *reinterpret_cast<uint32_t *>(&lo);
+        v.y = *reinterpret_cast<uint32_t *>(&hi);
+        o[c0 + 32 * u] = v;
+    }
+}
+
 // ------------------------------------------------------------ w1 gate/up interleave
 // w1p row (e, 256*b + q) = w1 row (e, 128*b + q) for q < 128 (gate), and
 // w1 row (e, I + 128*b + q - 128) for q >= 128 (up).
@@ -590,6 +686,17 @@ cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream
     CopyArgs a{x, r.recv_x, r.apick, r.slot, r.recv_row, r.pick_pos, r.recv_topk_idx, r.recv_topk_w,
                r.direct_row, r.direct_w, (int)p.T, (int)p.k, (int)p.W, (int)p.H, p.layout, nchunk, p.cap};
     return launch_pdl(dispatch_copy_kernel, dim3(blocks_for(p.T * nchunk)), dim3(kCopyThreads), 0, s, a);
+}
+
+cudaError_t launch_combine_fused(const Routing &r, const void *expert_out, uint16_t *out, cudaStream_t s) {
+    const Plan &p = *r.p;
+    if (p.T == 0) return cudaSuccess;
+    const int nchunk = (int)((p.H / 4 + 32 * kCopyU - 1) / (32 * kCopyU));
+    FusedCombineArgs a{expert_out, r.ypick, r.recv_row, r.recv_topk_idx, r.pick_pos, r.recv_topk_w, out,
+                       (int)p.T, (int)p.k, (int)p.W, (int)p.H, nchunk, p.cap};
+    if (p.eo_bf16)
+        return launch_pdl(combine_fused_kernel<true>, dim3(blocks_for(p.T * nchunk)), dim3(kCopyThreads), 0, s, a);
+    return launch_pdl(combine_fused_kernel<false>, dim3(blocks_for(p.T * nchunk)), dim3(kCopyThreads), 0, s, a);
 }
 
 cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, bool skip_single, cudaStream_t s) {

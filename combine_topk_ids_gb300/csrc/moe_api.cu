@@ -292,8 +292,12 @@ int moe_prepare_weights(const moe_geom *g, const void *w1_dev, void *w1_prepared
                : MOE_ERR_CUDA;
 }
 
-int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void *w2_dev,
-                   void *expert_out_dev, void *stream) {
+namespace moe {
+namespace {
+// The bf16 expert stage.  reduce = false (RANK_MAJOR / FLAT inside moe_forward_host): the
+// rank reduction is left to the fused combine, so expert_out's multi-pick rows stay unwritten.
+int expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void *w2_dev, void *expert_out_dev,
+               void *stream, bool reduce) {
     Plan p;
     int rc = handle_plan(h, &p);
     if (rc != MOE_OK) return rc;
@@ -312,9 +316,41 @@ int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void 
     if ((rc = launch_gemm2(r, static_cast<const uint16_t *>(w2_dev), expert_out_dev, s)) != MOE_OK)
         return rc;
     record(h, MOE_EV_GEMM2_END, s);
-    if (!em && launch_reduce_ranks(r, expert_out_dev, true, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!em && reduce && launch_reduce_ranks(r, expert_out_dev, true, s) != cudaSuccess) return MOE_ERR_CUDA;
     record(h, MOE_EV_FFN_END, s);
     return MOE_OK;
+}
+
+// moe_combine's launch; fused: RANK_MAJOR / FLAT combine that also forms the multi-pick
+// rows' sums (after expert_ffn with reduce = false)
+int combine(const moe_handle *h, const void *expert_out_dev, const float *topk_weights_dev, void *out_dev,
+            void *stream, bool fused) {
+    Plan p;
+    int rc = handle_plan(h, &p);
+    if (rc != MOE_OK) return rc;
+    const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
+    if (p.T > 0 && (!expert_out_dev || !out_dev || (em && !topk_weights_dev)))
+        return MOE_ERR_INVALID_ARGUMENT;
+    if ((expert_out_dev && !aligned(expert_out_dev, 16)) || (out_dev && !aligned(out_dev, 16)) ||
+        (topk_weights_dev && !aligned(topk_weights_dev, 4)))
+        return MOE_ERR_MISALIGNED;
+    if ((rc = check_device()) != MOE_OK) return rc;
+    Routing r = carve(p, h->workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    record(h, MOE_EV_COMBINE_BEGIN, s);
+    const cudaError_t ce = fused && !em
+                               ? launch_combine_fused(r, expert_out_dev, static_cast<uint16_t *>(out_dev), s)
+                               : launch_combine(r, expert_out_dev, topk_weights_dev, static_cast<uint16_t *>(out_dev), s);
+    if (ce != cudaSuccess) return MOE_ERR_CUDA;
+    record(h, MOE_EV_COMBINE_END, s);
+    return MOE_OK;
+}
+}  // namespace
+}  // namespace moe
+
+int moe_expert_ffn(const moe_handle *h, const void *w1_prepared_dev, const void *w2_dev,
+                   void *expert_out_dev, void *stream) {
+    return moe::expert_ffn(h, w1_prepared_dev, w2_dev, expert_out_dev, stream, true);
 }
 
 int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
@@ -394,24 +430,7 @@ int moe_prepare_weights_fp8(const moe_geom *g, const void *w1q_dev, const float 
 
 int moe_combine(const moe_handle *h, const void *expert_out_dev, const float *topk_weights_dev,
                 void *out_dev, void *stream) {
-    Plan p;
-    int rc = handle_plan(h, &p);
-    if (rc != MOE_OK) return rc;
-    const bool em = p.layout == MOE_LAYOUT_EXPERT_MAJOR;
-    if (p.T > 0 && (!expert_out_dev || !out_dev || (em && !topk_weights_dev)))
-        return MOE_ERR_INVALID_ARGUMENT;
-    if ((expert_out_dev && !aligned(expert_out_dev, 16)) || (out_dev && !aligned(out_dev, 16)) ||
-        (topk_weights_dev && !aligned(topk_weights_dev, 4)))
-        return MOE_ERR_MISALIGNED;
-    if ((rc = check_device()) != MOE_OK) return rc;
-    Routing r = carve(p, h->workspace);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    record(h, MOE_EV_COMBINE_BEGIN, s);
-    if (launch_combine(r, expert_out_dev, topk_weights_dev, static_cast<uint16_t *>(out_dev), s) !=
-        cudaSuccess)
-        return MOE_ERR_CUDA;
-    record(h, MOE_EV_COMBINE_END, s);
-    return MOE_OK;
+    return moe::combine(h, expert_out_dev, topk_weights_dev, out_dev, stream, false);
 }
 
 int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids_host,
@@ -440,8 +459,9 @@ int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids
             aligned(im, ids_dtype == MOE_IDS_INT64 ? 8 : 4) && aligned(wm, 4)) {
             int rc2 = moe_dispatch(g, xm, im, ids_dtype, static_cast<const float *>(wm), nullptr, workspace_dev,
                                    workspace_bytes, h, stream);
-            if (rc2 == MOE_OK) rc2 = moe_expert_ffn(h, w1_prepared_dev, w2_dev, expert_out_dev, stream);
-            if (rc2 == MOE_OK) rc2 = moe_combine(h, expert_out_dev, static_cast<const float *>(wm), om, stream);
+            if (rc2 == MOE_OK) rc2 = moe::expert_ffn(h, w1_prepared_dev, w2_dev, expert_out_dev, stream, false);
+            if (rc2 == MOE_OK)
+                rc2 = moe::combine(h, expert_out_dev, static_cast<const float *>(wm), om, stream, true);
             return rc2;
         }
     }
@@ -458,8 +478,8 @@ int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids
     if ((rc = moe_dispatch(g, x_dev, topk_ids_dev, ids_dtype, topk_weights_dev, nullptr,
                            workspace_dev, workspace_bytes, h, stream)) != MOE_OK)
         return rc;
-    if ((rc = moe_expert_ffn(h, w1_prepared_dev, w2_dev, expert_out_dev, stream)) != MOE_OK) return rc;
-    if ((rc = moe_combine(h, expert_out_dev, topk_weights_dev, out_dev, stream)) != MOE_OK) return rc;
+    if ((rc = moe::expert_ffn(h, w1_prepared_dev, w2_dev, expert_out_dev, stream, false)) != MOE_OK) return rc;
+    if ((rc = moe::combine(h, expert_out_dev, topk_weights_dev, out_dev, stream, true)) != MOE_OK) return rc;
     if (p.T > 0 &&
         cudaMemcpyAsync(out_host, out_dev, (size_t)p.T * p.H * 2, cudaMemcpyDeviceToHost, s) !=
             cudaSuccess)

@@ -72,6 +72,9 @@ cudaError_t launch_dispatch_copy(const Routing &r, const uint16_t *x, cudaStream
 cudaError_t launch_reduce_ranks(const Routing &r, void *expert_out, bool skip_single, cudaStream_t s);
 cudaError_t launch_combine(const Routing &r, const void *expert_out, const float *topk_w,
                            uint16_t *out, cudaStream_t s);
+// RANK_MAJOR / FLAT: the combine fused with the rank reduction (multi-pick rows summed from
+// the per-pick rows on the fly; bf16 geometries whose second GEMM wrote the one-pick rows)
+cudaError_t launch_combine_fused(const Routing &r, const void *expert_out, uint16_t *out, cudaStream_t s);
 cudaError_t launch_prepare_w1(const moe_geom &g, const uint16_t *w1, uint16_t *w1p,
                               cudaStream_t s);
 // Grouped SwiGLU FFN: GEMM1 (+SiLU*mul) into act, GEMM2 into expert_out (EM) or the

@@ -363,6 +363,10 @@ int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
  * like the other calls: out_host is valid once the stream has been synchronised; the
  * host inputs must stay unchanged until then.  Returns the first error of the
  * sequence.
+ * expert_out_dev is scratch here: for RANK_MAJOR / FLAT the rank reduction of received
+ * rows with several local picks is folded into the combine, which sums their per-pick
+ * rows on the fly in the same order, so out_host equals the three calls' output bit for
+ * bit while those rows of expert_out_dev are left unwritten.
  */
 int moe_forward_host(const moe_geom *g, const void *x_host, const void *topk_ids_host,
                      int ids_dtype, const float *topk_weights_host, void *out_host,

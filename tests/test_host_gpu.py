@@ -21,12 +21,21 @@ def built():
     moe.build()
 
 
-@pytest.mark.parametrize("name", ["small_em", "small_rm", "small_flat", "tiny_ll_em"])
+CASES = {n: gen.ALL[n] for n in ("small_em", "small_rm", "small_flat", "tiny_ll_em", "pair_flat", "blocks_flat")}
+CASES["small_flat_eo16"] = gen.ALL["small_flat"].with_(expert_out="bf16", seed=31)
+CASES["small_rm_eo16"] = gen.ALL["small_rm"].with_(expert_out="bf16", seed=32)
+
+
+@pytest.mark.parametrize("name", list(CASES))
 @pytest.mark.parametrize("pinned", [True, False])
 def test_forward_host_matches_device_path(name, pinned):
-    cfg = gen.ALL[name]
+    """For RANK_MAJOR / FLAT the host call folds the rank reduction into the combine; its
+    expert_out is scratch, filled with NaN before each call here, so that reading a row it
+    leaves unwritten would show in the output."""
+    cfg = CASES[name]
     case = make_case(cfg, "cuda")
-    layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout, cfg.algo)
+    layer = moe.MoELayer1GPU(cfg.W, cfg.Tr, cfg.tokens, cfg.H, cfg.E, cfg.k, cfg.I, cfg.layout, cfg.algo,
+                             expert_out=cfg.expert_out)
     layer.set_weights(case.w1, case.w2)
     layer.forward(case.x, case.ids, case.w)
     torch.cuda.synchronize()
@@ -45,6 +54,7 @@ def test_forward_host_matches_device_path(name, pinned):
     h = moe.MoeHandle()
     for _ in range(2):
         out_h.fill_(float("nan"))
+        layer.expert_out.fill_(float("nan"))
         moe.moe_forward_host(layer.geom, x_h, ids_h, w_h, out_h, *stage, layer.w1p, layer.w2,
                              layer.expert_out, layer.workspace, h)
         torch.cuda.synchronize()
