@@ -221,13 +221,22 @@ TRAFFIC_SOURCES = {"bf16": ("combine_topk_ids_gb300/csrc/ffn_tc.cu",) + TRAFFIC_
                    "fp8": ("combine_topk_ids_gb300/csrc/ffn_fp8.cu",) + TRAFFIC_COMMON}
 
 
+def strip_comments(src):
+    """C/C++ source without its comments and blank space, so that the traffic key follows
+    the code alone (a comment edit does not change what the counters measured)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def src_hash(quant="bf16"):
     import importlib
     B = importlib.import_module("combine_topk_ids_gb300.build")
     h = hashlib.sha256()
     for f in TRAFFIC_SOURCES[quant]:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f)) as fh:
+            h.update(strip_comments(fh.read()).encode())
     # the include path is absolute; hash it relative to the checkout so the key is the
     # same wherever the repository is copied
     h.update(repr([f.replace(B.ROOT, ".") for f in B._flags()]).encode())

@@ -26,8 +26,11 @@
 // Tiles: per expert ceil(n_e/128) m-blocks x (N/256) n-blocks, enumerated expert by expert,
 // n-block-major with the m-blocks of one weight tile adjacent (they run on neighbouring
 // SMs at the same time and share the weight tile through L2).  Experts with no rows issue
-// no tiles and read no weights.  Every mbarrier wait is bounded: on timeout the kernel
-// sets MOE_STATUS_TIMEOUT, drains and frees its tensor memory, and returns.
+// no tiles and read no weights.  CTAs take tiles round-robin, except the one-CTA 256-row
+// tiles, which are handed out in order from a device counter (so that the tiles in flight
+// stay a contiguous window when an expert's last, short tile takes one MMA per k-step
+// instead of two).  Every mbarrier wait is bounded: on timeout the kernel sets
+// MOE_STATUS_TIMEOUT, drains and frees its tensor memory, and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 

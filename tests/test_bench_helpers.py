@@ -79,3 +79,11 @@ def test_traffic_key_does_not_depend_on_the_checkout_path(monkeypatch):
 @pytest.mark.parametrize("tokens,steps,world,secs,want", [(1024, 20, 1, 0.5, 40960.0), (1024, 20, 2, 0.5, 81920.0)])
 def test_job_tokens_per_s(tokens, steps, world, secs, want):
     assert bench.job_tokens_per_s(tokens, steps, world, secs) == pytest.approx(want)
+
+
+def test_traffic_key_follows_code_not_comments():
+    src = "int f(int a) {  // add one\n    return a + 1; /* the result */\n}\n"
+    same = "int f(int a) {\n  return a + 1;\n}  // reformatted, comments changed\n"
+    other = "int f(int a) { return a + 2; }"
+    assert bench.strip_comments(src) == bench.strip_comments(same)
+    assert bench.strip_comments(src) != bench.strip_comments(other)
