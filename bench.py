@@ -448,15 +448,16 @@ def run_ours(args, cfg, rank, world, dist):
         raise RuntimeError("device status %d after the timed steps" % status)
     total_s = max_over_ranks(sum(steps_ms) / 1e3, dist, dev)
     kmean = {k: statistics.mean(d[k] for d in ktimes) for k in ktimes[0]}
+    kmedian = {k: statistics.median(d[k] for d in ktimes) for k in ktimes[0]}
     eager = {"value": job_tokens_per_s(cfg.tokens, args.steps, world, total_s), "unit": "tokens/s",
-             "ms_per_step": 1e3 * total_s / args.steps}
+             "ms_per_step": 1e3 * total_s / args.steps, "median_ms_per_step": statistics.median(steps_ms)}
     graph = None
     if cg is not None:
         if not torch.equal(layer.out.view(torch.int16), ref_out.view(torch.int16)):
             raise RuntimeError("graph replay differs from the eager steps")
         g_s = max_over_ranks(sum(g_ms) / 1e3, dist, dev)
         graph = {"value": job_tokens_per_s(cfg.tokens, args.steps, world, g_s), "unit": "tokens/s",
-                 "ms_per_step": 1e3 * g_s / args.steps}
+                 "ms_per_step": 1e3 * g_s / args.steps, "median_ms_per_step": statistics.median(g_ms)}
     clocks.end()
     clk = clocks.stop()
     head = graph if graph is not None else eager
@@ -586,6 +587,8 @@ def run_ours(args, cfg, rank, world, dist):
             "data": "synthetic", "impl": "ours",
             "config": workload_config(cfg, world),
             "stages_us": {k: round(v * 1e3, 2) for k, v in kmean.items()},
+            "stages_us_median": {k: round(v * 1e3, 2) for k, v in kmedian.items()},
+            "median_ms_per_step": head["median_ms_per_step"],
             "roofline": roof, "layer_roofline": layer_roof, "kernels_roofline": per_kernel,
             "moved_beyond_algorithmic_bytes": moved_beyond_algorithmic(cfg, rt),
             "cpu_baseline": cpu, "e2e": e2e,

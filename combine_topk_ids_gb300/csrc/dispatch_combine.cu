@@ -100,9 +100,8 @@ struct CopyArgs {
 // RM/FLAT: for every kept pick of token t, direct_row[p] = the received row d*cap + r
 // when the pick is the only local pick of that row (its expert_out row is then
 // weight * y, written by the second GEMM), else -1; direct_w[p] = its weight.  One warp
-// (lane j = pick j) per token.  Args: CopyArgs or QuantCopyArgs.
-template <typename Args>
-__device__ __forceinline__ void mark_direct_picks(const Args &a, int64_t t, int lane) {
+// (lane j = pick j) per token.
+__device__ __forceinline__ void mark_direct_picks(const CopyArgs &a, int64_t t, int lane) {
     for (int d = 0; d < a.W; ++d) {
         const int r = a.recv_row[t * a.W + d];
         if (r < 0) continue;
@@ -529,11 +528,6 @@ struct QuantCopyArgs {
     uint8_t *apick;         // RM/FLAT: [P, H] codes in pick-list order
     float *apick_scales;    // RM/FLAT: [H/128][P]
     const int32_t *slot, *recv_row, *pick_pos;
-    // RM/FLAT: received local ids and weights (read), the per-pick direct rows (written)
-    const int32_t *recv_topk_idx;
-    const float *recv_topk_w;
-    int32_t *direct_row;
-    float *direct_w;
     int T, k, W, H, layout, nchunk;
     int64_t cap, nrecv, P;
 };
@@ -558,7 +552,6 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_quant_kernel(QuantCopyA
         const int n0 = nd;
         nd = collect_rows(dst[warp], nd, a.k, lane, [&](int q) -> int64_t { return a.pick_pos[t * a.k + q]; });
         np = nd - n0;
-        if (chunk == 0 && a.direct_row) mark_direct_picks(a, t, lane);
     }
     __syncwarp();
     const int nv = a.H / 8;   // 8-column vectors per row; a 128-column block is 16 of them
@@ -751,9 +744,8 @@ cudaError_t launch_dispatch_quant(const Routing &r, const uint16_t *x, cudaStrea
     if (p.T == 0) return cudaSuccess;
     const int nchunk = (int)((p.H / 8 + 32 * kCopyU - 1) / (32 * kCopyU));
     QuantCopyArgs a{x, reinterpret_cast<uint8_t *>(r.recv_x), r.recv_scales, reinterpret_cast<uint8_t *>(r.apick),
-                    r.apick_scales, r.slot, r.recv_row, r.pick_pos, r.recv_topk_idx, r.recv_topk_w,
-                    r.direct_row, r.direct_w, (int)p.T, (int)p.k, (int)p.W, (int)p.H, p.layout, nchunk,
-                    p.cap, p.nrecv, p.P};
+                    r.apick_scales, r.slot, r.recv_row, r.pick_pos, (int)p.T, (int)p.k, (int)p.W, (int)p.H,
+                    p.layout, nchunk, p.cap, p.nrecv, p.P};
     return launch_pdl(dispatch_quant_kernel, dim3(blocks_for(p.T * nchunk)), dim3(kCopyThreads), 0, s, a);
 }
 

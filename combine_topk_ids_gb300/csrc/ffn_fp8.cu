@@ -96,22 +96,8 @@ struct F8Args {
     int64_t out_ld;           // elements per output row
     int out_mode;             // 0: row = e*out_cap + m; 1: row = offsets[e] + m
     int64_t out_cap;
-    // mode 1, out_mode 1 (RANK_MAJOR / FLAT per-pick rows) with staged stores, or NULL: a
-    // pick p with direct_row[p] >= 0 is the only local pick of its received row, so the row
-    // direct_row[p] of out_direct gets direct_w[p] * y (the local-pick sum, with the
-    // reduction's roundings) instead of out getting y
-    const int32_t *direct_row;
-    const float *direct_w;
-    void *out_direct;
     int32_t *status;
 };
-
-// The local-pick sum of a row with one local pick, as the rank reduction computes it:
-// fmaf(w, y, 0) from the stored per-pick value (bf16 rows: y rounded to bf16 first; the
-// caller's bf16 store rounds the sum).
-__device__ __forceinline__ float one_pick_sum(float w, float y, bool bf16) {
-    return __fmaf_rn(w, bf16 ? __bfloat162float(__float2bfloat16_rn(y)) : y, 0.0f);
-}
 
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t acc) {
@@ -328,50 +314,23 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 const int valid = min(F_BM, __ldg(a.counts + e) - m0);
                 const int64_t obase =
                     (a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e)) + m0;
-                // Rows of a pick that is the only local pick of its received row go to that
-                // expert_out row: this warp stores rows 2i + wsel; lane l holds the direct
-                // row and weight of i = l and i = l + 32, loaded before the wait below
-                const int wsel = warp - 2;
-                int dr0 = -1, dr1 = -1;
-                float dw0 = 0.f, dw1 = 0.f;
-                if (a.direct_row) {
-                    const int r0 = 2 * lane + wsel, r1 = r0 + 64;
-                    if (r0 < valid) { dr0 = __ldg(a.direct_row + obase + r0); dw0 = __ldg(a.direct_w + obase + r0); }
-                    if (r1 < valid) { dr1 = __ldg(a.direct_row + obase + r1); dw1 = __ldg(a.direct_w + obase + r1); }
-                }
                 for (int h = 0; h < 2; ++h) {
                     if (!mbar_wait(afull0 + 8 * h, (uint32_t)ntile & 1, abort_flag, a.status)) { ok = false; break; }
                     const int64_t col = (int64_t)nbk * a.bn + 128 * h + 4 * lane;
                     if (a.out_bf16) {
+                        __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) + col;
 #pragma unroll 4
-                        for (int i = 0; 2 * i + wsel < valid; ++i) {
-                            const int r = 2 * i + wsel;
-                            float4 v = act_s[r * 32 + (lane ^ (r & 31))];
-                            const int dr = __shfl_sync(0xffffffffu, i < 32 ? dr0 : dr1, i & 31);
-                            const float w = __shfl_sync(0xffffffffu, i < 32 ? dw0 : dw1, i & 31);
-                            __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(dr >= 0 ? a.out_direct : a.out) +
-                                                 (dr >= 0 ? (int64_t)dr : obase + r) * a.out_ld + col;
-                            if (dr >= 0)
-                                v = make_float4(one_pick_sum(w, v.x, true), one_pick_sum(w, v.y, true),
-                                                one_pick_sum(w, v.z, true), one_pick_sum(w, v.w, true));
+                        for (int r = warp - 2; r < valid; r += 2) {
+                            const float4 v = act_s[r * 32 + (lane ^ (r & 31))];
                             __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-                            *reinterpret_cast<uint2 *>(out) =
+                            *reinterpret_cast<uint2 *>(out + (obase + r) * a.out_ld) =
                                 make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
                         }
                     } else {
+                        float *out = reinterpret_cast<float *>(a.out) + col;
 #pragma unroll 4
-                        for (int i = 0; 2 * i + wsel < valid; ++i) {
-                            const int r = 2 * i + wsel;
-                            float4 v = act_s[r * 32 + (lane ^ (r & 31))];
-                            const int dr = __shfl_sync(0xffffffffu, i < 32 ? dr0 : dr1, i & 31);
-                            const float w = __shfl_sync(0xffffffffu, i < 32 ? dw0 : dw1, i & 31);
-                            float *out = reinterpret_cast<float *>(dr >= 0 ? a.out_direct : a.out) +
-                                         (dr >= 0 ? (int64_t)dr : obase + r) * a.out_ld + col;
-                            if (dr >= 0)
-                                v = make_float4(one_pick_sum(w, v.x, false), one_pick_sum(w, v.y, false),
-                                                one_pick_sum(w, v.z, false), one_pick_sum(w, v.w, false));
-                            *reinterpret_cast<float4 *>(out) = v;
-                        }
+                        for (int r = warp - 2; r < valid; r += 2)
+                            *reinterpret_cast<float4 *>(out + (obase + r) * a.out_ld) = act_s[r * 32 + (lane ^ (r & 31))];
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(aempty0 + 8 * h);
@@ -581,13 +540,6 @@ int launch_gemm1_fp8(const Routing &r, const uint8_t *w1qp, const float *w1sp, c
     return launch_gemm_fp8<0>(mA, mB, g, (p.P / F_BM + p.E) * g.nb, s);
 }
 
-// The second FP8 GEMM stages its tiles (256 columns, three k-blocks or more) and then writes
-// the rows of picks that are the only local pick of their received row straight into
-// expert_out (RANK_MAJOR / FLAT); with direct per-thread stores it writes every pick's row.
-bool fp8_gemm2_writes_direct_rows(const Plan &p) {
-    return p.layout != MOE_LAYOUT_EXPERT_MAJOR && p.H % 256 == 0 && p.I / F_BK >= 3;
-}
-
 int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, void *expert_out,
                      cudaStream_t s) {
     const Plan &p = *r.p;
@@ -603,12 +555,7 @@ int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, voi
     g.b_rows = p.H; g.b_scale = w2s;
     g.mode = 1; g.out_ld = p.H; g.out_bf16 = p.eo_bf16;
     if (em) { g.out = expert_out; g.out_mode = 0; g.out_cap = p.cap; }
-    else {
-        g.out = r.ypick; g.out_mode = 1; g.out_cap = 0;
-        if (fp8_gemm2_writes_direct_rows(p)) {
-            g.direct_row = r.direct_row; g.direct_w = r.direct_w; g.out_direct = expert_out;
-        }
-    }
+    else { g.out = r.ypick; g.out_mode = 1; g.out_cap = 0; }
     return launch_gemm_fp8<1>(mA, mB, g, (p.P / F_BM + p.E) * g.nb, s);
 }
 

@@ -379,9 +379,7 @@ int moe_expert_ffn_fp8(const moe_handle *h, const void *w1q_prepared_dev,
                                s)) != MOE_OK)
         return rc;
     record(h, MOE_EV_GEMM2_END, s);
-    // rows with one local pick were written by the second GEMM (direct_row) if it staged
-    if (!em && launch_reduce_ranks(r, expert_out_dev, fp8_gemm2_writes_direct_rows(p), s) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    if (!em && launch_reduce_ranks(r, expert_out_dev, false, s) != cudaSuccess) return MOE_ERR_CUDA;
     record(h, MOE_EV_FFN_END, s);
     return MOE_OK;
 }

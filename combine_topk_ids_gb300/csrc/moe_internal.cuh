@@ -93,9 +93,6 @@ cudaError_t launch_prepare_w1_fp8(const moe_geom &g, const uint8_t *w1q, const f
 int launch_gemm1_fp8(const Routing &r, const uint8_t *w1qp, const float *w1sp, cudaStream_t s);
 int launch_gemm2_fp8(const Routing &r, const uint8_t *w2q, const float *w2s, void *expert_out,
                      cudaStream_t s);
-// whether launch_gemm2_fp8 writes one-local-pick rows into expert_out itself (the rank
-// reduction then skips them)
-bool fp8_gemm2_writes_direct_rows(const Plan &p);
 
 int num_sms();   // SM count of the current device (cached per device)
 int check_device();   // MOE_OK on a compute capability 10.3 device, else a moe_error
