@@ -280,3 +280,29 @@ def test_every_pick_on_one_expert(layout, T):
     if cfg.act == "pair":
         # the default activation meets the plain bound with no allowance at all
         assert n_eo == 0 and n_out == 0
+
+
+@pytest.mark.parametrize("layout,act", [("EM", "pair"), ("RM", "pair"), ("FLAT", "pair"), ("EM", "bf16")])
+def test_two_sm_block_boundaries(layout, act):
+    """Experts with 256, 384, 385, 128, 129, 0, 1 and 317 rows (top-1, 1600 picks over 8
+    experts: two-SM 256-row tiles in both GEMMs): a last block that is full, holds exactly
+    128 or 129 rows (the second CTA's half empty or holding one row), a single row, or
+    nothing, and an empty expert."""
+    counts = [256, 384, 385, 128, 129, 0, 1, 317]
+    T = sum(counts)
+    cfg = gen.MoeConfig("tails", W=2, Tr=800, H=256, E=8, k=1, I=256, layout=layout,
+                        algo="HT" if layout == "FLAT" else "LL", routing="uniform", T=T,
+                        seed=61, act=act)
+    ids = np.repeat(np.arange(8), counts)
+    ids = np.random.default_rng(61).permutation(ids).reshape(T, 1).astype(np.int64)
+    case = make_case(cfg, "cuda", ids_override=ids)
+    layer = run_layer(case)
+    assert layer.status() == 0
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    assert list(rt["counts"]) == counts
+    check_routing(layer, rt, cfg)
+    check_dispatch_rows(layer, rt, case)
+    n_eo = check_expert_out(layer, rt, case)
+    n_out = check_out(layer, case)
+    if act == "pair":
+        assert n_eo == 0 and n_out == 0
