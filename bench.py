@@ -98,6 +98,10 @@ def algorithmic_work(cfg, rt):
     out_rows = R if em else nrecv
     w["gemm2"] = dict(bytes=active * H * I * (eb + ws) + R * I * (eb + rs) + out_rows * H * ob,
                       flops=2 * R * H * I)
+    if cfg.quant == "bf16" and cfg.act == "pair":
+        # the bf16-pair activation takes two MMAs per product (act_hi and act_lo): the
+        # tensor work the kernel issues, padding rows not counted
+        w["gemm2"]["mma_flops"] = 2 * w["gemm2"]["flops"]
     if not em:
         w["reduce_ranks"] = dict(bytes=0, flops=0)
     w["combine"] = dict(bytes=(R * H * ob + T * k * 4 if em else nrecv * H * ob) + T * H * 2, flops=0)
@@ -144,6 +148,10 @@ def kernel_roofline(wk, t_s, peaks, tc_ratio=1.0, sustained=False):
         ach, peak, nom = wk["bytes"] / t_s / 1e9, peaks["hbm_gbs"], NOMINAL_PEAKS["hbm_gbs"]
         r = {"bound": "hbm", "unit": "GB/s", "peak_kind": "copy"}
     r.update(achieved=ach, peak=peak, frac=ach / peak, nominal_peak=nom, frac_of_nominal=ach / nom)
+    if "mma_flops" in wk:
+        # the tensor work issued (beyond the algorithmic FLOPs) at the same tensor peak
+        r["issued_mma_tflops"] = wk["mma_flops"] / t_s / 1e12
+        r["issued_mma_frac"] = r["issued_mma_tflops"] / (peaks[key] * tc_ratio)
     return r
 
 

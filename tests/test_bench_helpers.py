@@ -26,6 +26,10 @@ def test_algorithmic_work_expert_major():
     # GEMM2: down weights, the activation, float32 expert_out rows
     assert w["gemm2"]["bytes"] == E * H * I * 2 + R * I * 2 + R * H * 4
     assert w["gemm2"]["flops"] == 2 * R * I * H
+    # the bf16-pair activation (the default) issues two MMAs per product
+    assert w["gemm2"]["mma_flops"] == 2 * w["gemm2"]["flops"]
+    assert "mma_flops" not in bench.algorithmic_work(cfg.with_(act="bf16"), {"R": R, "active_experts": E,
+                                                                         "n_recv": 0})["gemm2"]
     assert "reduce_ranks" not in w
     # combine: the expert_out rows, the routing weights, the bf16 output
     assert w["combine"]["bytes"] == R * H * 4 + T * k * 4 + T * H * 2
@@ -65,6 +69,8 @@ def test_kernel_roofline_picks_the_bound_and_the_peak():
     tc = bench.kernel_roofline({"bytes": 1e9, "flops": 1.6e13}, 10e-3, peaks, sustained=True)
     assert tc["bound"] == "tensor" and tc["peak_kind"] == "sustained" and tc["frac"] == pytest.approx(1.0)
     assert bench.kernel_roofline({"bytes": 1e9, "flops": 1.6e13}, 10e-3, peaks)["frac"] == pytest.approx(0.8)
+    pair = bench.kernel_roofline({"bytes": 1e9, "flops": 0.8e13, "mma_flops": 1.6e13}, 10e-3, peaks)
+    assert pair["frac"] == pytest.approx(0.4) and pair["issued_mma_frac"] == pytest.approx(0.8)
 
 
 def test_traffic_key_does_not_depend_on_the_checkout_path(monkeypatch):
