@@ -26,3 +26,24 @@ def test_random_configs_cover_the_tile_paths():
         paths.add(c.act)
     assert {"two-sm", "tall", "128-row", "fused-routing", "three-kernel-routing", "128-col", "256-col",
             "EM", "RM", "FLAT", "pair", "bf16"} <= paths, paths
+
+
+def test_fp8_random_configs_cover_the_paths():
+    """The FP8 sweep (test_random_geometries_fp8_gpu.py) reaches all three layouts, both
+    second-GEMM tile widths, a second GEMM of a single k-block, both routing paths and
+    masked picks."""
+    from test_random_geometries_fp8_gpu import SEEDS as F8_SEEDS, fp8_config
+    paths = set()
+    for seed in F8_SEEDS:
+        c = fp8_config(seed)
+        assert c.quant == "fp8"
+        P = c.tokens * c.k
+        paths.add(c.layout)
+        paths.add("128-col" if c.H % 256 else "256-col")
+        if c.I // 128 == 1:
+            paths.add("one-k-block GEMM2")
+        paths.add("fused-routing" if P <= 3072 and c.E <= 64 and c.E * c.W <= 4096 else "three-kernel-routing")
+        if c.mask_frac > 0:
+            paths.add("masked")
+    assert {"EM", "RM", "FLAT", "128-col", "256-col", "one-k-block GEMM2", "fused-routing",
+            "three-kernel-routing", "masked"} <= paths, paths
