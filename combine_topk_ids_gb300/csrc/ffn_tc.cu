@@ -685,7 +685,9 @@ bool use_pair(const Plan &p, int64_t K, int64_t N) {
 // (A/B, same build): DeepSeek-like prefill GEMM1 (K 7168, ~1024 rows per expert) -10%
 // clock for clock; on the Mixtral-like decode (~256 rows per expert, three of eight
 // experts a few rows over 256) GEMM1 +9% and GEMM2 +50%, since a 256-row block holding
-// a few tail rows streams the whole weight tile again and nothing hides its epilogue.
+// a few tail rows streams the whole weight tile again and nothing hides its epilogue.  At
+// K = 2048 instead of two-SM or 128-row tiles: ragged 16384-token GEMM1 +5% (bf16-pair
+// activation) / -1.5% (single bf16), DeepSeek-like prefill single-bf16 GEMM2 +1.4%.
 bool use_tall(const Plan &p, int64_t K) { return p.P >= 512 * p.E && K >= 4096; }
 
 // upper bound of the row blocks over all experts: sum ceil(n_e/rows) <= P/rows + E
