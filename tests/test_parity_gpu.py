@@ -197,6 +197,31 @@ def test_ffn_twice_on_one_dispatch(name):
         assert torch.equal(layer.out.view(torch.int16), out1.view(torch.int16))
 
 
+@pytest.mark.parametrize("name", ["tall_em", "tall_flat", "pair_em", "pair_flat", "small_flat"])
+def test_repeated_calls_alternating_batches(name):
+    """Forty forwards on one layer alternating between two batches of different routing:
+    each output equals the first output of its batch bit for bit and the status stays
+    clear, so nothing a call leaves behind (the 256-row tiles' tile counter and ring, the
+    two-SM clusters' hand-offs, the routing state in the workspace) changes a later call."""
+    cfg = SMALL_CASES[name]
+    cases = [make_case(cfg.with_(seed=70 + i, routing=r), "cuda")
+             for i, r in enumerate(["zipf", "uniform"])]
+    layer = run_layer(cases[0])
+    first = [layer.out.clone(), None]
+    run_layer(cases[1], layer)
+    first[1] = layer.out.clone()
+    assert not torch.equal(first[0].view(torch.int16), first[1].view(torch.int16))
+    outs = []
+    for i in range(40):   # back to back on the stream; each output copied on the stream too
+        c = i % 2
+        layer.forward(cases[c].x, cases[c].ids, cases[c].w)
+        outs.append(layer.out.clone())
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    for i, o in enumerate(outs):
+        assert torch.equal(o.view(torch.int16), first[i % 2].view(torch.int16)), i
+
+
 # ----------------------------------------------------------------------- edge cases
 def test_empty_batch():
     cfg = SMALL_CASES["small_rm"].with_(T=0)
