@@ -48,8 +48,7 @@ __device__ __forceinline__ uint2 ld_nc_v2(const void *p) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Four consecutive elements (index elem, a multiple of 4) of a float32 or bf16 row as fp32,
-// and the store back (bf16: round to nearest even).
+// Four consecutive elements (index elem, a multiple of 4) of a float32 or bf16 row as fp32.
 template <bool BF16>
 __device__ __forceinline__ float4 ld_row4(const void *base, int64_t elem) {
     if (BF16) {
@@ -57,20 +56,6 @@ __device__ __forceinline__ float4 ld_row4(const void *base, int64_t elem) {
         return make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
     }
     return ld_nc_f4(reinterpret_cast<const float *>(base) + elem);
-}
-
-template <bool BF16>
-__device__ __forceinline__ void st_row4(void *base, int64_t elem, float4 v) {
-    if (BF16) {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-        uint2 w;
-        w.x = *reinterpret_cast<uint32_t *>(&lo);
-        w.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(base) + elem) = w;
-    } else {
-        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(base) + elem) = v;
-    }
 }
 
 // ---------------------------------------------------------------- dispatch row scatter
