@@ -42,10 +42,6 @@ class MoeConfig:
     def tokens(self) -> int:
         return self.W * self.Tr if self.T < 0 else self.T
 
-    @property
-    def local_experts(self) -> int:
-        return self.E // self.W
-
     def with_(self, **kw) -> "MoeConfig":
         return replace(self, **kw)
 
