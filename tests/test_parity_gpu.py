@@ -57,6 +57,13 @@ SMALL_CASES = {
                                 layout="RM", algo="LL", routing="zipf", T=250),
     "world64_flat": gen.MoeConfig("world64_flat", W=64, Tr=4, H=256, E=128, k=4, I=128,
                                   layout="FLAT", algo="HT", routing="uniform", T=256),
+    # the most experts the library accepts (MOE_MAX_EXPERTS = 2048): 2048-entry count and
+    # offset scans over the routing chunks, tile enumeration over mostly empty experts
+    # (0-4 rows each); FLAT also at world 64 (32 local experts per rank)
+    "emax_em": gen.MoeConfig("emax_em", W=8, Tr=64, H=256, E=2048, k=8, I=128,
+                             layout="EM", algo="LL", routing="zipf", T=500),
+    "emax_flat": gen.MoeConfig("emax_flat", W=64, Tr=8, H=256, E=2048, k=8, I=128,
+                               layout="FLAT", algo="HT", routing="dirichlet", T=512),
     # the widest hidden the library accepts (MOE_MAX_HIDDEN = 65536): a 65536-long K loop
     # in the first GEMM (1024 k-blocks), 256 n-tiles in the second, 64 copy chunks per row
     "hmax_em": gen.MoeConfig("hmax_em", W=2, Tr=8, H=65536, E=4, k=2, I=128,
