@@ -37,6 +37,9 @@ CASES = {
                                     layout="FLAT", algo="HT", routing="uniform", T=64, quant="fp8"),
     "f8_world64_rm": gen.MoeConfig("f8_world64_rm", W=64, Tr=4, H=256, E=64, k=4, I=128,
                                    layout="RM", algo="LL", routing="zipf", T=250, quant="fp8"),
+    # 2048 experts (the limit), most with 0-4 rows, one Zipf-hot expert with a few hundred
+    "f8_emax_em": gen.MoeConfig("f8_emax_em", W=8, Tr=64, H=256, E=2048, k=8, I=128,
+                                layout="EM", algo="LL", routing="zipf", T=500, quant="fp8"),
 }
 
 
