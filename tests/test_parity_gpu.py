@@ -279,6 +279,27 @@ def test_inactive_ranks_are_masked(name):
     check_out(layer, case, active=active)
 
 
+@pytest.mark.parametrize("name", ["small_em", "small_rm", "small_flat", "pair_flat"])
+def test_duplicate_experts_in_a_token(name):
+    """Ids drawn with replacement (-1 included): a token may name one expert twice or more
+    (reading 7: separate picks in (t, j) order).  On RANK_MAJOR / FLAT such picks share one
+    received row and are summed there in ascending j; the rest is the usual path."""
+    cfg = SMALL_CASES[name].with_(seed=57)
+    rng = np.random.default_rng(57)
+    ids = rng.integers(-1, cfg.E, size=(cfg.tokens, cfg.k)).astype(np.int64)
+    dup = sum(len(r[r >= 0]) - len(set(r[r >= 0].tolist())) for r in ids)
+    assert dup > 0
+    case = make_case(cfg, "cuda", ids_override=ids)
+    layer = run_layer(case)
+    assert layer.status() == 0
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    check_routing(layer, rt, cfg)
+    check_dispatch_rows(layer, rt, case)
+    n_eo = check_expert_out(layer, rt, case)
+    n_out = check_out(layer, case)
+    assert n_eo == 0 and n_out == 0
+
+
 def test_expert_major_region_overflow():
     """A token naming one expert twice can overflow the W*Tr-row EM region: the extra picks
     are dropped and flagged, the rest matches the oracle."""
