@@ -105,6 +105,12 @@ struct FfnArgs {
     int32_t *sched;
 };
 constexpr int kRing = 4;   // tiles in flight from the producer to the MMA and epilogue warps
+// A tile whose row block holds at most 64 rows (an expert's last block) takes M = 64 MMAs on
+// one SM (128-row tiles; the one-CTA 256-row tiles' short blocks).  An M = 64 accumulator
+// holds row r in tensor-memory lane 32 * (r / 16) + r % 16: each epilogue warp's lane
+// quarter carries 16 rows in its first 16 lanes.
+constexpr bool kM64Tails = true;
+constexpr int kM64Rows = 64;
 
 // --- two-SM (cluster of two CTAs) variants
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -327,19 +333,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t tx = PAIR ? 2 * tx_cta : tx_cta;   // the leader's barrier sees both CTAs
         int seq = 0;
         for (int tile = first_tile; ok;) {
-            bool short_tile = false;
+            bool short_tile = false, m64_tile = false;
             int e = 0, mb = 0, nbk = 0;
             if (tile < total) {
                 decode_tile(a, tile, e, mb, nbk);
                 // a tile whose rows end in its first 128 loads only those, through the
                 // 128-row box of tmA2, and the MMA issuer skips the second half
-                short_tile = dyn && __ldg(a.counts + e) - mb * P::kMRows <= BM;
+                const int rows = __ldg(a.counts + e) - mb * P::kMRows;
+                short_tile = dyn && rows <= BM;
+                m64_tile = kM64Tails && dyn && rows <= kM64Rows;
             }
             if (dyn) {   // publish the tile (or the end) to the MMA and epilogue warps
                 const int slot = seq & (kRing - 1);
                 if (!mbar_wait(rempty0 + 8 * slot, ((seq / kRing) & 1) ^ 1, abort_flag, a.status)) break;
                 ring_tile[slot] = tile < total ? tile : -1;
-                ring_short[slot] = short_tile ? 1 : 0;
+                ring_short[slot] = m64_tile ? 2 : short_tile ? 1 : 0;
                 mbar_arrive(rfull0 + 8 * slot);
                 ++seq;
             }
@@ -383,21 +391,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        const uint32_t idesc = make_idesc(TALL ? BM : P::kMRows, a.bn);
+        const uint32_t idesc_full = make_idesc(TALL ? BM : P::kMRows, a.bn);
+        const uint32_t idesc_m64 = make_idesc(kM64Rows, a.bn);
         int seq = 0;
         for (int tile = first_tile; ok; tile += tile_step) {
             bool second_half = TALL;   // TALL: rows 128..255 of the tile hold data
+            bool m64 = false;
             if (dyn) {
                 const int slot = seq & (kRing - 1);
                 if (!mbar_wait(rfull0 + 8 * slot, (seq / kRing) & 1, abort_flag, a.status)) break;
                 tile = ring_tile[slot];
                 second_half = ring_short[slot] == 0;
+                m64 = ring_short[slot] == 2;
                 mbar_arrive(rempty0 + 8 * slot);
                 ++seq;
                 if (tile < 0) break;
             } else if (tile >= total) {
                 break;
+            } else if (kM64Tails && !PAIR && !TALL) {
+                int e, mb, nbk;
+                decode_tile(a, tile, e, mb, nbk);
+                m64 = __ldg(a.counts + e) - mb * P::kMRows <= kM64Rows;
             }
+            const uint32_t idesc = m64 ? idesc_m64 : idesc_full;
             if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -462,6 +478,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             int e, mb, nbk;
             decode_tile(a, tile, e, mb, nbk);
             const int count = __ldg(a.counts + e);
+            // the MMA issuer's choice: M = 64 for a block of at most 64 rows
+            const bool m64 = kM64Tails && !PAIR && (dyn || !TALL) && count - mb * P::kMRows <= kM64Rows;
+            const int rq = m64 ? 16 : 32;   // rows per epilogue warp
             const int64_t obase = a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e);
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, a.status)) break;
             tc_fence_after();
@@ -469,8 +488,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 1
             for (int half = 0; half < (TALL ? 2 : 1); ++half) {
             // first row of this warp: PAIR tiles split rows by CTA, TALL tiles by accumulator
-            const int m0 = mb * P::kMRows + (int)rank * BM + half * BM + quad * 32;
-            const int nvalid = min(32, count - m0);   // rows this warp stores
+            const int m0 = mb * P::kMRows + (int)rank * BM + half * BM + quad * rq;
+            const int nvalid = min(rq, count - m0);   // rows this warp stores (its lanes 0 .. nvalid-1)
             const int64_t orow0 = obase + m0;
             const uint32_t tbase = tmem_base + (uint32_t)((acc + half) * BN) + ((uint32_t)(quad * 32) << 16);
             if (nvalid <= 0) {
