@@ -262,11 +262,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * P::kStageBytes);
     // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], then (dynamic tile order)
     // rfull[kRing], rempty[kRing]; then the TMEM address, the abort flag, the ring's tiles
-    // and their short-tile flags
+    // and the rows of their row blocks
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4 + 2 * kRing);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *ring_tile = reinterpret_cast<volatile int *>(tmem_slot + 2);
-    volatile int *ring_short = ring_tile + kRing;
+    volatile int *ring_rows = ring_tile + kRing;
     const bool dyn = TALL && a.sched != nullptr;
     const uint32_t rfull0 = smem_u32(bars + 2 * STAGES + 4), rempty0 = rfull0 + 8 * kRing;
 
@@ -333,21 +333,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t tx = PAIR ? 2 * tx_cta : tx_cta;   // the leader's barrier sees both CTAs
         int seq = 0;
         for (int tile = first_tile; ok;) {
-            bool short_tile = false, m64_tile = false;
-            int e = 0, mb = 0, nbk = 0;
+            bool short_tile = false;
+            int e = 0, mb = 0, nbk = 0, rows = 0;
             if (tile < total) {
                 decode_tile(a, tile, e, mb, nbk);
                 // a tile whose rows end in its first 128 loads only those, through the
                 // 128-row box of tmA2, and the MMA issuer skips the second half
-                const int rows = __ldg(a.counts + e) - mb * P::kMRows;
+                rows = __ldg(a.counts + e) - mb * P::kMRows;
                 short_tile = dyn && rows <= BM;
-                m64_tile = kM64Tails && dyn && rows <= kM64Rows;
             }
             if (dyn) {   // publish the tile (or the end) to the MMA and epilogue warps
                 const int slot = seq & (kRing - 1);
                 if (!mbar_wait(rempty0 + 8 * slot, ((seq / kRing) & 1) ^ 1, abort_flag, a.status)) break;
                 ring_tile[slot] = tile < total ? tile : -1;
-                ring_short[slot] = m64_tile ? 2 : short_tile ? 1 : 0;
+                ring_rows[slot] = rows;
                 mbar_arrive(rfull0 + 8 * slot);
                 ++seq;
             }
@@ -396,13 +395,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         int seq = 0;
         for (int tile = first_tile; ok; tile += tile_step) {
             bool second_half = TALL;   // TALL: rows 128..255 of the tile hold data
-            bool m64 = false;
+            bool m64 = false, m64_2 = false;   // M = 64 for the first / the second 128 rows
             if (dyn) {
                 const int slot = seq & (kRing - 1);
                 if (!mbar_wait(rfull0 + 8 * slot, (seq / kRing) & 1, abort_flag, a.status)) break;
                 tile = ring_tile[slot];
-                second_half = ring_short[slot] == 0;
-                m64 = ring_short[slot] == 2;
+                const int rows = ring_rows[slot];
+                second_half = rows > BM;
+                m64 = kM64Tails && rows <= kM64Rows;
+                m64_2 = kM64Tails && rows - BM <= kM64Rows;
                 mbar_arrive(rempty0 + 8 * slot);
                 ++seq;
                 if (tile < 0) break;
@@ -414,6 +415,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 m64 = __ldg(a.counts + e) - mb * P::kMRows <= kM64Rows;
             }
             const uint32_t idesc = m64 ? idesc_m64 : idesc_full;
+            const uint32_t idesc2 = m64_2 ? idesc_m64 : idesc_full;
             if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -436,7 +438,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // rows 128..255 of the tile: the second 16 KB of the A tile, the
                         // second accumulator
                         if (TALL && second_half)
-                            mma_bf16(d_tmem + BN, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc, accum);
+                            mma_bf16(d_tmem + BN, sw128_desc(a0 + A_BYTES + kk * 32), bd, idesc2, accum);
                     }
                 }
                 // the stage is reusable (in both CTAs) once these MMAs finish
@@ -478,9 +480,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             int e, mb, nbk;
             decode_tile(a, tile, e, mb, nbk);
             const int count = __ldg(a.counts + e);
-            // the MMA issuer's choice: M = 64 for a block of at most 64 rows
-            const bool m64 = kM64Tails && !PAIR && (dyn || !TALL) && count - mb * P::kMRows <= kM64Rows;
-            const int rq = m64 ? 16 : 32;   // rows per epilogue warp
+            // the MMA issuer's choice: M = 64 for 128 rows of the tile that hold at most 64
+            const int blk_rows = count - mb * P::kMRows;
+            const bool m64_ok = kM64Tails && !PAIR && (dyn || !TALL);
             const int64_t obase = a.out_mode == 0 ? (int64_t)e * a.out_cap : (int64_t)__ldg(a.offsets + e);
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, a.status)) break;
             tc_fence_after();
@@ -488,6 +490,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 1
             for (int half = 0; half < (TALL ? 2 : 1); ++half) {
             // first row of this warp: PAIR tiles split rows by CTA, TALL tiles by accumulator
+            const int rq = m64_ok && blk_rows - half * BM <= kM64Rows ? 16 : 32;   // rows per epilogue warp
             const int m0 = mb * P::kMRows + (int)rank * BM + half * BM + quad * rq;
             const int nvalid = min(rq, count - m0);   // rows this warp stores (its lanes 0 .. nvalid-1)
             const int64_t orow0 = obase + m0;
