@@ -14,9 +14,10 @@
 //   warp 0      TMA producer: 128x64 A tile(s) + 256x64 B tile per stage (SWIZZLE_128B),
 //               a 192 KB mbarrier ring: 4 stages of 48 KB (128-row tiles), 3 of 64 KB
 //               (256-row tiles, or the bf16-pair A operand), 6 of 32 KB (two-SM tiles)
-//   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16, M=128,
-//               N=256, K=16, bf16 x bf16 -> fp32 into one of two 256-column TMEM
-//               accumulators, tcgen05.commit frees smem stages and hands tiles over
+//   warp 1      MMA issuer (one thread): tcgen05.mma.cta_group::1.kind::f16, M=128 (M=64
+//               for 128 rows of a tile that hold at most 64), N=256, K=16, bf16 x bf16 ->
+//               fp32 into one of two 256-column TMEM accumulators, tcgen05.commit frees
+//               smem stages and hands tiles over
 //   warp 2      TMEM allocator (512 columns)
 //   warps 4-11  epilogue, two warps per TMEM lane quarter, each on half of the tile's
 //               columns: tcgen05.ld 32x32b rows -> registers -> SwiGLU / fp32 or bf16
