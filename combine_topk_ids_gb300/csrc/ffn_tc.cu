@@ -106,10 +106,10 @@ struct FfnArgs {
     int32_t *sched;
 };
 constexpr int kRing = 4;   // tiles in flight from the producer to the MMA and epilogue warps
-// A tile whose row block holds at most 64 rows (an expert's last block) takes M = 64 MMAs on
-// one SM (128-row tiles; the one-CTA 256-row tiles' short blocks).  An M = 64 accumulator
+// 128 rows of a tile that hold at most 64 (in an expert's last block) take M = 64 MMAs on
+// one SM: a 128-row tile, or either half of a one-CTA 256-row tile.  An M = 64 accumulator
 // holds row r in tensor-memory lane 32 * (r / 16) + r % 16: each epilogue warp's lane
-// quarter carries 16 rows in its first 16 lanes.
+// quarter carries 16 rows in its first 16 lanes.  (The two-SM tiles keep M = 256.)
 constexpr bool kM64Tails = true;
 constexpr int kM64Rows = 64;
 
