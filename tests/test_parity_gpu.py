@@ -204,6 +204,42 @@ def test_ffn_twice_on_one_dispatch(name):
         assert torch.equal(layer.out.view(torch.int16), out1.view(torch.int16))
 
 
+M64_CASES = {
+    # 128-row tiles (under 192 rows per expert on average): last blocks of 64 / 65 rows,
+    # a second block of 64 / 65, one row, 63 and 127 rows, an empty expert
+    "m64_rows128_em": (dict(W=2, Tr=400, H=256, E=8, k=1, I=256, layout="EM", algo="LL"),
+                       [64, 65, 192, 193, 1, 0, 63, 127]),
+    "m64_rows128_flat": (dict(W=2, Tr=400, H=256, E=8, k=1, I=256, layout="FLAT", algo="HT"),
+                         [64, 65, 192, 193, 1, 0, 63, 127]),
+    # one-CTA 256-row tiles in the first GEMM (K 4096, >= 512 rows per expert on average):
+    # last blocks of 64 and 65 rows (M = 64 or 128 on the first half) and of 192 and 193
+    # rows (M = 64 or 128 on the second half); the second GEMM's 128-row tiles see 64/65 too
+    "m64_tall_em": (dict(W=2, Tr=1100, H=4096, E=4, k=1, I=256, layout="EM", algo="LL"),
+                    [576, 577, 448, 449]),
+}
+
+
+@pytest.mark.parametrize("name", list(M64_CASES))
+def test_m64_block_boundaries(name):
+    """Blocks of 64 rows or fewer take M = 64 MMAs (accumulator rows 16 per lane quarter):
+    every boundary of that rule, against the oracle at the plain bound."""
+    geo, counts = M64_CASES[name]
+    T = sum(counts)
+    cfg = gen.MoeConfig(name, routing="uniform", T=T, seed=63, **geo)
+    ids = np.repeat(np.arange(len(counts)), counts)
+    ids = np.random.default_rng(63).permutation(ids).reshape(T, 1).astype(np.int64)
+    case = make_case(cfg, "cuda", ids_override=ids)
+    layer = run_layer(case)
+    assert layer.status() == 0
+    rt = oracle.route(geom_dict(cfg), case.ids_np, case.w_np)
+    assert list(rt["counts"]) == counts
+    check_routing(layer, rt, cfg)
+    check_dispatch_rows(layer, rt, case)
+    n_eo = check_expert_out(layer, rt, case)
+    n_out = check_out(layer, case)
+    assert n_eo == 0 and n_out == 0
+
+
 @pytest.mark.parametrize("name", ["tall_em", "tall_flat", "pair_em", "pair_flat", "small_flat"])
 def test_repeated_calls_alternating_batches(name):
     """Forty forwards on one layer alternating between two batches of different routing:
