@@ -601,7 +601,9 @@ def run_ours(args, cfg, rank, world, dist):
             "moved_beyond_algorithmic_bytes": moved_beyond_algorithmic(cfg, rt),
             "cpu_baseline": cpu, "e2e": e2e,
             "timing": "cuda_graph_replay" if graph is not None else "eager", "eager": eager,
-            "gpu_launches": per_step * args.steps, "clocks": clk}
+            "gpu_launches": per_step * args.steps, "gpu_launches_per_step": per_step, "clocks": clk}
+    if line["eager"] is not None:   # the interleaved eager steps launch the same kernels again
+        line["eager"]["gpu_launches"] = per_step * args.steps
     if rank == 0:
         print(json.dumps(line), flush=True)
 
